@@ -1,0 +1,362 @@
+"""Layer-step benchmark of the GB300 Flash-dLLM hot path.
+
+Workload (the LLaDA-8B-shaped single layer, bf16, batch 1, prompt 512 + gen
+256): one step = fused QKV + RoPE + KV scatter for 64 refresh rows (32
+masked-window + 32 tracked), scheduled attention over the 768 cached keys
+with the Eq. (2) tracker, tracker top-32, and eps unmasking of the 32 window
+rows over vocab 126464. Metric: query rows per second of whole layer-steps.
+
+Timing: W warm-up steps, then exactly K timed steps between CUDA events on
+the launching stream, bracketed by a barrier and torch.cuda.synchronize().
+Weights, caches, hidden rows and logits rotate over enough copies that the
+step's working set is several times the L2 size, so no step reads a
+previous step's data out of L2. The dominant kernel (the QKV projection,
+which streams the 100.7 MB weight) is bracketed by its own events every
+step for the roofline figure. SM clocks and throttle reasons are sampled
+with nvidia-smi during the timed region.
+
+--impl reference times the float64 CPU oracle (the reference arm of this
+build; there is no upstream implementation to install) on bounded samples
+of the same workload on the host cores.
+
+Multi-GPU (torchrun): every rank runs an independent replica of the
+workload (the path shards by sequence with no exchange); value is the total
+rows of all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "layer-step query-tokens/s at LLaDA-8B shapes; % of bf16 TC peak / HBM GB/s"
+WORKLOAD = "llada8b_layer_bf16_b1_p512_g256_w32_t32"
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+class Clocks:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out = ""
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:6]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if os.environ.get("FDL_BENCH_BACKEND", "nccl") == "nccl" else "gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle leg
+# ---------------------------------------------------------------------------
+def oracle_step(wl, n_rows: int):
+    """One oracle layer-step of the workload restricted to its first n_rows
+    query rows (the bounded sample); returns the rows processed."""
+    import oracle
+    e, s, g = wl.extra, wl.shape, wl.geom
+    rows = e["rows"]
+    sel = slice(0, n_rows)
+    x = e["x"].values()[sel]
+    q, kc, vc = oracle.qkv_rope_cache_write(
+        x, e["w_vals"], s.n_heads, s.head_dim, s.rope_theta, rows.row_rope_pos[sel], rows.row_seq[sel],
+        rows.row_cache_pos[sel], g.block_table, g.page_size, e["kc_vals"], e["vc_vals"], s.dtype)
+    cu = np.array([0, n_rows], np.int32)
+    _, _, tr = oracle.sched_attn(q, kc, vc, g.block_table, g.page_size, cu, wl.seq_len, rows.row_kind[sel],
+                                 max_seq=wl.max_seq, dtype=s.dtype)
+    oracle.track_topk(tr.astype(np.float32), e["eligible"], wl.seq_len, e["topk"])
+    n_logit_rows = min(n_rows, 32)
+    oracle.unmask(e["logit_vals"][:n_logit_rows], np.zeros(n_logit_rows, np.int32),
+                  e["window_pos"][:n_logit_rows], 1, e["eps"], False, e["max_search"])
+    return n_rows
+
+
+def cpu_leg(wl, budget_s: float):
+    """Times the oracle as it stands on the host cores for about budget_s."""
+    e = wl.extra
+    e.setdefault("w_vals", e["w"].values())
+    e.setdefault("kc_vals", e["k_cache"].values())
+    e.setdefault("vc_vals", e["v_cache"].values())
+    e.setdefault("logit_vals", e["logits"].values())
+    n_rows = e["rows"].n_rows
+    done, t0 = 0, time.perf_counter()
+    steps = 0
+    while True:
+        done += oracle_step(wl, n_rows)
+        steps += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return done / dt, steps, dt
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import synth
+    wl = synth.llada_layer()
+    for _ in range(args.warmup):
+        cpu_leg(wl, 0.0)
+    value, steps, dt = cpu_leg(wl, max(1.0, min(60.0, 4.0 * args.steps)))
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "query-rows/s", "n_gpus": args.gpus,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch": 1, "seq_len": 768, "rows_per_step": 64},
+        "cpu_baseline": {"value": value, "unit": "query-rows/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{steps} full layer-steps (64 rows) of the float64 numpy oracle"},
+        "e2e": {"value": value, "unit": "query-rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU leg
+# ---------------------------------------------------------------------------
+def run_gpu(args, world, rank, local):
+    import torch
+
+    import kv_cache_attention_gb300 as fdl
+    import synth
+    from kv_cache_attention_gb300 import build as fdl_build
+
+    torch.cuda.set_device(local)
+    fdl_build.build()
+    wl = synth.llada_layer(seed=1002)
+    e, s, g = wl.extra, wl.shape, wl.geom
+    Hh, hd, N, d = s.n_heads, s.head_dim, wl.max_seq, s.d_model
+    rows = e["rows"]
+    R = rows.n_rows
+    Rw, ms, k, V = 32, e["max_search"], e["topk"], e["vocab"]
+    stream = torch.cuda.current_stream()
+    ctx = fdl.fdl_create(d, Hh, hd, s.rope_theta, 1, N, wl.max_views, g.page_size, g.n_pages, R, V, "bf16",
+                         stream=stream)
+
+    def bf(t):
+        return torch.from_numpy(np.ascontiguousarray(t.data).view(np.int16)).view(torch.bfloat16)
+
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size
+    w_host, x_host, l_host = bf(e["w"]), bf(e["x"]), bf(e["logits"])
+    kc_host, vc_host = bf(e["k_cache"]), bf(e["v_cache"])
+    per_copy = (w_host.numel() + x_host.numel() + l_host.numel() + 2 * kc_host.numel()) * 2
+    n_copies = max(2, int(np.ceil(4 * l2 / per_copy)))
+    Ws = [w_host.cuda() for _ in range(n_copies)]
+    Xs = [x_host.cuda() for _ in range(n_copies)]
+    Ls = [l_host.cuda() for _ in range(n_copies)]
+    KC = [kc_host.cuda() for _ in range(n_copies)]
+    VC = [vc_host.cuda() for _ in range(n_copies)]
+    i32 = lambda a: torch.as_tensor(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+    row_seq, row_rope, row_cache, row_kind = (i32(rows.row_seq), i32(rows.row_rope_pos),
+                                              i32(rows.row_cache_pos), i32(rows.row_kind))
+    cu, kv_len, bt = i32(rows.cu_seqlens), i32([N]), i32(g.block_table)
+    elig = torch.as_tensor(e["eligible"]).cuda()
+    seq_len = i32([N])
+    win_seq, win_pos = i32(np.zeros(Rw)), i32(e["window_pos"])
+    q = torch.empty((R, Hh, hd), dtype=torch.bfloat16, device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty((R, Hh), dtype=torch.float32, device="cuda")
+    track = torch.zeros((1, N), dtype=torch.float32, device="cuda")
+    idx = torch.empty((1, k), dtype=torch.int32, device="cuda")
+    cnt = torch.empty((1,), dtype=torch.int32, device="cuda")
+    conf = torch.empty(Rw, dtype=torch.float32, device="cuda")
+    arg = torch.empty(Rw, dtype=torch.int32, device="cuda")
+    com = torch.empty(Rw, dtype=torch.uint8, device="cuda")
+    srows = torch.empty((1, ms), dtype=torch.int32, device="cuda")
+    nsr = torch.empty((1,), dtype=torch.int32, device="cuda")
+    launches_per_step = 5  # qkv, work-list build, attention, top-k, unmask (our kernels)
+
+    def step(c, ev=None, X=None, L=None):
+        X = Xs[c] if X is None else X
+        L = Ls[c] if L is None else L
+        track.zero_()
+        if ev is not None:
+            ev[0].record(stream)
+        ctx.qkv_rope_cache_write(X, Ws[c], row_seq, row_rope, row_cache, bt, KC[c], VC[c], q)
+        if ev is not None:
+            ev[1].record(stream)
+        ctx.sched_attn(q, KC[c], VC[c], bt, cu, kv_len, row_kind, o, lse_out=lse, track_scores=track)
+        ctx.track_topk(track, elig, seq_len, k, idx, cnt)
+        ctx.unmask_verify(1, ms, logits=L, row_seq=win_seq, row_pos=win_pos, eps=e["eps"], force_progress=False,
+                          conf=conf, argmax=arg, commit=com, search_rows=srows, n_search=nsr)
+
+    for i in range(args.warmup):
+        step(i % n_copies)
+    ctx.sync_status()
+    K = args.steps
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        t0.record(stream)
+        for i in range(K):
+            step(i % n_copies, kev[i])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ctx.sync_status()
+    ms_total = t0.elapsed_time(t1)
+    qkv_ms = [a.elapsed_time(b) for a, b in kev]
+    ms_total = max_over_ranks(ms_total, world)
+    ms_step = ms_total / K
+    value = world * R * K / (ms_total * 1e-3)
+
+    # end to end: pinned host inputs in, step results out, every step
+    x_pin = x_host.pin_memory()
+    l_pin = l_host.pin_memory()
+    out_pin = [t.new_empty(t.shape, device="cpu").pin_memory() for t in (conf, arg, com, srows, nsr, idx, cnt)]
+    xd, ld_ = torch.empty_like(Xs[0]), torch.empty_like(Ls[0])
+    h2d = x_pin.numel() * 2 + l_pin.numel() * 2
+    d2h = sum(t.numel() * t.element_size() for t in out_pin)
+
+    def e2e_step(c):
+        xd.copy_(x_pin, non_blocking=True)
+        ld_.copy_(l_pin, non_blocking=True)
+        step(c, X=xd, L=ld_)
+        for src, dst in zip((conf, arg, com, srows, nsr, idx, cnt), out_pin):
+            dst.copy_(src, non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i % n_copies)
+    barrier(world)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(K):
+        e2e_step(i % n_copies)
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(a.elapsed_time(b), world)
+    e2e_value = world * R * K / (e2e_ms * 1e-3)
+
+    if rank != 0:
+        return
+    hbm, tc, src = peaks()
+    qkv_bytes = 3 * d * d * 2 + R * d * 2 + R * d * 2 + 2 * R * d * 2
+    qkv_avg = statistics.mean(qkv_ms)
+    achieved = qkv_bytes / (qkv_avg * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "query-rows/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch": world, "seq_len": N, "rows_per_step": R,
+                   "parallelism": f"replicas{world}", "l2_hygiene": f"{n_copies} rotating copies of W/X/cache/logits "
+                   f"({per_copy * n_copies / 1e9:.2f} GB > 4x L2 {l2 / 1e6:.0f} MB)"},
+        "e2e": {"value": e2e_value, "unit": "query-rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * K,
+        "roofline": {"kernel": "qkv_rope_cache_write", "bound": "hbm", "achieved": achieved, "peak": hbm,
+                     "unit": "GB/s", "frac": achieved / hbm, "traffic": None, "peak_source": src,
+                     "algorithmic_bytes": qkv_bytes, "avg_launch_us": qkv_avg * 1e3},
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        cpu_value, cpu_steps, cpu_dt = cpu_leg(wl, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": cpu_value, "unit": "query-rows/s", "cores": os.cpu_count(),
+                                "kind": "oracle",
+                                "sample": f"{cpu_steps} full layer-steps (64 rows) of the float64 numpy oracle "
+                                          f"in {cpu_dt:.1f} s"}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="fdl", choices=["fdl", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    world, rank, local = dist_init()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_gpu(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,230 @@
+/*
+ * fdl.h -- C ABI of the GB300 (sm_103a) Flash-dLLM layer-step hot path.
+ *
+ * The library computes, for one diffusion-LLM denoising step, the per-layer
+ * Flash-Cache path and the per-step decoding decisions described by
+ * "Flash-dLLM: IO-Aware KV Caching and Parallel Decoding for Fast,
+ * Memory-Efficient Diffusion LLMs" (paper digest; sections "Core method" and
+ * "Method steps in detail", Algorithm 2 steps 1-4 and Eq. (2)):
+ *
+ *   fdl_qkv_rope_cache_write  fused QKV projection + RoPE + K/V cache scatter
+ *   fdl_sched_attn            block-table scheduled attention over the cache,
+ *                             with the Flash-Verify two-view mask and the
+ *                             Eq. (2) attention-mass tracker
+ *   fdl_track_topk            top-k of the tracker scores (next tracked set)
+ *   fdl_unmask_verify         confidence-threshold unmasking (search list) and
+ *                             Flash-Verify prefix acceptance
+ *
+ * Conventions shared by every entry point
+ *   - All tensor arguments are DEVICE pointers owned by the caller (for
+ *     example PyTorch allocations); the library never frees them.
+ *   - Every call is asynchronous on the context's CUDA stream.
+ *   - The return value reports host-side validation only: a NULL required
+ *     pointer, a size beyond the limits fixed at fdl_create, an unsupported
+ *     shape. On error nothing is launched and fdl_last_error() says why.
+ *   - Data-dependent problems found on the device (a block-table entry
+ *     outside the page pool, a position past the cache, inconsistent
+ *     cu_seqlens, a bounded wait that gave up) never trap: the offending
+ *     access is skipped and a device error word is set. fdl_sync_status()
+ *     synchronises the stream and reports (and clears) that word as
+ *     FDL_ERR_DEVICE_INDEX or FDL_ERR_TIMEOUT.
+ *   - Floating-point tensors use the context dtype (FDL_F32 or FDL_BF16);
+ *     accumulation is fp32. Index tensors are int32, masks are uint8.
+ *   - A context is not thread-safe; use one per host thread.
+ */
+#ifndef FDL_H_
+#define FDL_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FDL_OK = 0,
+  FDL_ERR_INVALID_ARG = 1,   /* bad pointer / size / shape; nothing launched   */
+  FDL_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. head_dim 96)   */
+  FDL_ERR_OOM = 3,           /* workspace allocation failed in fdl_create      */
+  FDL_ERR_CUDA = 4,          /* a CUDA runtime call failed                     */
+  FDL_ERR_DEVICE_INDEX = 5,  /* device saw an out-of-range index (skipped)     */
+  FDL_ERR_TIMEOUT = 6        /* a bounded device wait gave up                  */
+} fdl_status;
+
+typedef enum { FDL_F32 = 0, FDL_BF16 = 1 } fdl_dtype;
+
+/* Row kinds (row_kind arrays). j is the 0-based index of a search token in
+ * the acceptance order of its sequence. */
+#define FDL_KIND_NORMAL 0                 /* tracked / T_v / full-refresh row   */
+#define FDL_KIND_WINDOW 1                 /* masked-window row: feeds Eq. (2)    */
+#define FDL_KIND_DRAFT_VIEW(j) (2 + 2 * (j))
+#define FDL_KIND_MASK_VIEW(j) (3 + 2 * (j))
+
+/* Shape limits fixed for the life of a context. */
+typedef struct {
+  int d_model;        /* = n_heads * head_dim                                   */
+  int n_heads;
+  int head_dim;       /* 64 or 128                                              */
+  double rope_theta;  /* RoPE base (LLaDA: 5e5)                                 */
+  int max_batch;      /* most sequences in one call                             */
+  int max_seq;        /* N_max: base cache positions per sequence               */
+  int max_views;      /* view-key cache positions past a sequence's kv_len      */
+  int page_size;      /* cache slots per block-table page                       */
+  int n_pages;        /* pages in the pool: each cache holds n_pages*page_size  */
+                      /* rows of d_model elements                               */
+  int max_rows;       /* most query rows in one call                            */
+  int vocab;          /* logits row length                                      */
+  fdl_dtype dtype;    /* storage type of X, W, Q, caches, O and logits          */
+} fdl_config;
+
+typedef struct fdl_ctx fdl_ctx;
+
+/* Creates a context on the current CUDA device and allocates its workspace
+ * (RoPE cos/sin table for positions 0..max_seq+max_views-1 computed in
+ * double on the host, the scheduled-attention work list, counters and the
+ * device error word). cuda_stream is a cudaStream_t (NULL = legacy default
+ * stream). Returns FDL_ERR_INVALID_ARG for inconsistent limits,
+ * FDL_ERR_OOM / FDL_ERR_CUDA if allocation fails. */
+fdl_status fdl_create(const fdl_config* cfg, void* cuda_stream, fdl_ctx** out);
+void fdl_destroy(fdl_ctx* ctx);
+fdl_status fdl_set_stream(fdl_ctx* ctx, void* cuda_stream);
+/* Human-readable reason for the last non-OK status of this context. */
+const char* fdl_last_error(const fdl_ctx* ctx);
+/* Synchronises the context stream, then returns and clears the device error
+ * word: FDL_OK, FDL_ERR_DEVICE_INDEX or FDL_ERR_TIMEOUT (FDL_ERR_CUDA if the
+ * stream itself reported an error). */
+fdl_status fdl_sync_status(fdl_ctx* ctx);
+/* Query rows per scheduled-attention work item (the oracle rebuilds the
+ * work list with this tile). */
+int fdl_tile_m(const fdl_ctx* ctx);
+/* Number of int32 a worklist_out buffer needs for R rows over B sequences:
+ * 1 (item count) + 4 per possible item. */
+int fdl_worklist_capacity(const fdl_ctx* ctx, int R, int B);
+
+/* ------------------------------------------------------------------------
+ * Flash-Cache fused projection (paper digest, "Core method": QKV projection,
+ * RoPE and cache write fused so K/V go straight into the preallocated cache;
+ * "Method steps" step 2: the refresh rows are the masked window plus the
+ * tracked set).
+ *
+ * For every query row r (0 <= r < R):
+ *   [q | k | v] = X[r] . Wqkv^T                    (fp32 accumulation)
+ *   q, k <- RoPE(q, k) at position row_rope_pos[r]: rotate-half pairs
+ *           (i, i + head_dim/2) by angle pos * rope_theta^(-2i/head_dim)
+ *   q_out[r] = q                                   ([R, n_heads, head_dim])
+ *   if row_cache_pos[r] >= 0:  with b = row_seq[r], c = row_cache_pos[r],
+ *     slot = block_table[b*bt_stride + c/page_size]*page_size + c%page_size
+ *     k_cache[slot] = k, v_cache[slot] = v         (rows of d_model)
+ *
+ * X: [R, d_model]; Wqkv: [3*d_model, d_model] row-major, Q rows then K rows
+ * then V rows, head h in rows h*head_dim..(h+1)*head_dim-1 of each block.
+ * R <= max_rows. Row r's writes are skipped (device error word set) when
+ * its page lies outside [0, n_pages), c/page_size >= bt_stride, or its RoPE
+ * position is outside the table. Two rows writing the same slot race.
+ * ---------------------------------------------------------------------- */
+fdl_status fdl_qkv_rope_cache_write(fdl_ctx* ctx, const void* X, const void* Wqkv, int R,
+                                    const int* row_seq, const int* row_rope_pos,
+                                    const int* row_cache_pos, const int* block_table,
+                                    int bt_stride, void* k_cache, void* v_cache, void* q_out);
+
+/* ------------------------------------------------------------------------
+ * Scheduled attention (paper digest, "Background": exact IO-aware attention;
+ * "Core method": block-table scheduled attention over ragged per-sequence
+ * query blocks, and the two-view verify mask; "Method steps" step 4, Eq. (2)).
+ *
+ * Sequence b owns query rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 of q
+ * ([R, n_heads, head_dim]); its base keys are cache positions
+ * 0..kv_len[b]-1. When search_pos is not NULL, sequence b has
+ * m = n_search[b] search tokens at base positions search_pos[b*search_ld + j]
+ * (j < m <= min(search_ld, max_views/2), in acceptance order) whose draft-view keys sit at cache positions
+ * kv_len[b]+j and mask-view keys at kv_len[b]+m+j.
+ * Visibility by row_kind:
+ *   NORMAL, WINDOW      all base keys;
+ *   DRAFT_VIEW(k)       base keys except the search positions, draft keys
+ *                       j <= k, mask keys j > k;
+ *   MASK_VIEW(k)        base keys except the search positions, draft keys
+ *                       j < k, mask keys j >= k.
+ * For each row and head: o = softmax(q.K^T / sqrt(head_dim)) V over the
+ * visible keys, lse = log sum exp of the scaled scores (natural log).
+ * Tracker (track_scores != NULL): for every base key i of sequence b,
+ *   track_scores[b*track_ld + i] += sum_h sum_{WINDOW rows j} p_{h,j,i} / (H*M_b)
+ * with M_b the number of WINDOW rows of b; the caller zeroes the buffer
+ * once per step and every layer's call accumulates into it.
+ * o_out: [R, n_heads, head_dim] (context dtype); lse_out: [R, n_heads] fp32
+ * (nullable); worklist_out (nullable, fdl_worklist_capacity ints): count,
+ * then (b, q_start, q_len, n_keys) per item, n_keys = kv_len[b] + 2m.
+ * Requires B <= max_batch, R <= max_rows; R must equal cu_seqlens_q[B]
+ * (checked on the device).
+ * ---------------------------------------------------------------------- */
+fdl_status fdl_sched_attn(fdl_ctx* ctx, const void* q, const void* k_cache, const void* v_cache,
+                          const int* block_table, int bt_stride, const int* cu_seqlens_q,
+                          const int* kv_len, int B, int R, const int* row_kind,
+                          const int* search_pos, int search_ld, const int* n_search, void* o_out,
+                          float* lse_out, float* track_scores, int track_ld,
+                          int* worklist_out);
+
+/* ------------------------------------------------------------------------
+ * Tracker top-k (paper digest, "Method steps" step 4: the top-k decoded
+ * tokens by attention mass become the next tracked set).
+ *
+ * For each sequence b: among positions i < seq_len[b] with
+ * eligible[b*ld + i] != 0, the k with the largest scores[b*ld + i], ordered
+ * by score descending then position ascending. idx_out[b*k + t] holds the
+ * t-th position (-1 past cnt_out[b] = min(k, #eligible)). 1 <= k <= 1024.
+ * Scores must not be NaN; -0.0 and +0.0 compare equal.
+ * ---------------------------------------------------------------------- */
+fdl_status fdl_track_topk(fdl_ctx* ctx, const float* scores, const unsigned char* eligible,
+                          int ld, const int* seq_len, int B, int k, int* idx_out, int* cnt_out);
+
+/* ------------------------------------------------------------------------
+ * Confidence unmasking and Flash-Verify acceptance (paper digest, "Method
+ * steps" steps 2 and 3; Fast-dLLM "confidence-aware parallel decoding" for
+ * the forced-progress fallback).
+ *
+ * Unmask phase (logits != NULL): for each window row r < R_w (rows grouped
+ * by sequence: row_seq non-decreasing):
+ *   conf[r] = max_v softmax(logits[r])_v = 1 / sum_v exp(l_v - max l)
+ *   argmax[r] = lowest v attaining max l
+ *   commit[r] = conf[r] >= eps
+ *   if force_progress and sequence b committed nothing: commit its row of
+ *   highest conf (lowest row_pos on ties).
+ *   search_rows[b*max_search + j] = the uncommitted rows of b ordered by conf
+ *   descending then row_pos ascending, j < n_search[b] <= max_search; -1 pad.
+ * Verify phase (mask_logits != NULL): row b*max_search + j (j < n_search[b])
+ *   of mask_logits is the mask view of b's j-th search token and
+ *   draft_tok[b*max_search + j] its draft token. With c~ and x~ the mask
+ *   view's confidence and argmax, accept[b*max_search + j] = 1 for the
+ *   longest prefix j = 0, 1, ... with draft_tok == x~ and c~ >= gamma;
+ *   n_accept[b] is its length. mask_conf / mask_argmax receive c~ and x~. If both phases run in one call, the verify phase reads the
+ *   n_search the unmask phase wrote.
+ * Logits rows have config.vocab entries of the context dtype.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  int B;
+  int max_search;
+  /* unmask phase */
+  const void* logits;          /* [R_w, vocab] or NULL to skip the phase */
+  int R_w;
+  const int* row_seq;          /* [R_w] */
+  const int* row_pos;          /* [R_w] */
+  float eps;
+  int force_progress;
+  float* conf;                 /* [R_w] */
+  int* argmax;                 /* [R_w] */
+  unsigned char* commit;       /* [R_w] */
+  int* search_rows;            /* [B*max_search] */
+  int* n_search;               /* [B]; output of unmask, input of verify */
+  /* verify phase */
+  const void* mask_logits;     /* [B*max_search, vocab] or NULL to skip */
+  const int* draft_tok;        /* [B*max_search] */
+  float gamma;
+  unsigned char* accept;       /* [B*max_search] */
+  int* n_accept;               /* [B] */
+  float* mask_conf;            /* [B*max_search] */
+  int* mask_argmax;            /* [B*max_search] */
+} fdl_unmask_args;
+
+fdl_status fdl_unmask_verify(fdl_ctx* ctx, const fdl_unmask_args* args);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FDL_H_ */

@@ -1,0 +1,251 @@
+"""Python binding of libfdl, the GB300 Flash-dLLM layer-step hot path.
+
+Argument marshalling only: every function forwards torch device tensors as
+raw pointers to the C ABI declared in ``include/fdl.h``; all computation
+happens in the library's CUDA kernels. The names mirror the C entry points.
+Importing this module does not load the library; the first call does, and it
+raises ``FdlError`` if ``libfdl.so`` has not been built (there is no other
+implementation to fall back on).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libfdl.so")
+
+FDL_OK = 0
+FDL_ERR_INVALID_ARG = 1
+FDL_ERR_UNSUPPORTED = 2
+FDL_ERR_OOM = 3
+FDL_ERR_CUDA = 4
+FDL_ERR_DEVICE_INDEX = 5
+FDL_ERR_TIMEOUT = 6
+
+FDL_F32 = 0
+FDL_BF16 = 1
+
+FDL_KIND_NORMAL = 0
+FDL_KIND_WINDOW = 1
+
+
+def FDL_KIND_DRAFT_VIEW(j: int) -> int:
+    return 2 + 2 * j
+
+
+def FDL_KIND_MASK_VIEW(j: int) -> int:
+    return 3 + 2 * j
+
+
+# Every symbol include/fdl.h declares.
+EXPORTS = (
+    "fdl_create", "fdl_destroy", "fdl_set_stream", "fdl_last_error", "fdl_sync_status",
+    "fdl_tile_m", "fdl_worklist_capacity", "fdl_qkv_rope_cache_write", "fdl_sched_attn",
+    "fdl_track_topk", "fdl_unmask_verify",
+)
+
+
+class FdlError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"fdl status {status}: {msg}")
+        self.status = status
+
+
+class fdl_config(ctypes.Structure):
+    _fields_ = [
+        ("d_model", ctypes.c_int), ("n_heads", ctypes.c_int), ("head_dim", ctypes.c_int),
+        ("rope_theta", ctypes.c_double), ("max_batch", ctypes.c_int), ("max_seq", ctypes.c_int),
+        ("max_views", ctypes.c_int), ("page_size", ctypes.c_int), ("n_pages", ctypes.c_int),
+        ("max_rows", ctypes.c_int), ("vocab", ctypes.c_int), ("dtype", ctypes.c_int),
+    ]
+
+
+_P = ctypes.c_void_p
+
+
+class fdl_unmask_args(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int), ("max_search", ctypes.c_int),
+        ("logits", _P), ("R_w", ctypes.c_int), ("row_seq", _P), ("row_pos", _P),
+        ("eps", ctypes.c_float), ("force_progress", ctypes.c_int),
+        ("conf", _P), ("argmax", _P), ("commit", _P), ("search_rows", _P), ("n_search", _P),
+        ("mask_logits", _P), ("draft_tok", _P), ("gamma", ctypes.c_float),
+        ("accept", _P), ("n_accept", _P), ("mask_conf", _P), ("mask_argmax", _P),
+    ]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads libfdl.so and declares its C signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise FdlError(FDL_ERR_UNSUPPORTED, f"{path} is not built; run kv_cache_attention_gb300.build.build()")
+    L = ctypes.CDLL(path)
+    i, p, f, d = ctypes.c_int, _P, ctypes.c_float, ctypes.c_double
+    L.fdl_create.argtypes = [ctypes.POINTER(fdl_config), p, ctypes.POINTER(p)]
+    L.fdl_create.restype = i
+    L.fdl_destroy.argtypes = [p]
+    L.fdl_destroy.restype = None
+    L.fdl_set_stream.argtypes = [p, p]
+    L.fdl_set_stream.restype = i
+    L.fdl_last_error.argtypes = [p]
+    L.fdl_last_error.restype = ctypes.c_char_p
+    L.fdl_sync_status.argtypes = [p]
+    L.fdl_sync_status.restype = i
+    L.fdl_tile_m.argtypes = [p]
+    L.fdl_tile_m.restype = i
+    L.fdl_worklist_capacity.argtypes = [p, i, i]
+    L.fdl_worklist_capacity.restype = i
+    L.fdl_qkv_rope_cache_write.argtypes = [p, p, p, i, p, p, p, p, i, p, p, p]
+    L.fdl_qkv_rope_cache_write.restype = i
+    L.fdl_sched_attn.argtypes = [p, p, p, p, p, i, p, p, i, i, p, p, i, p, p, p, p, i, p]
+    L.fdl_sched_attn.restype = i
+    L.fdl_track_topk.argtypes = [p, p, p, i, p, i, i, p, p]
+    L.fdl_track_topk.restype = i
+    L.fdl_unmask_verify.argtypes = [p, ctypes.POINTER(fdl_unmask_args)]
+    L.fdl_unmask_verify.restype = i
+    _lib = L
+    return L
+
+
+def _ptr(t) -> int | None:
+    """Device pointer of a tensor (None stays NULL)."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise FdlError(FDL_ERR_INVALID_ARG, "tensor arguments must live on the GPU")
+    if not t.is_contiguous():
+        raise FdlError(FDL_ERR_INVALID_ARG, "tensor arguments must be contiguous")
+    return t.data_ptr()
+
+
+class Context:
+    """Owns one ``fdl_ctx``. Methods mirror the C entry points."""
+
+    def __init__(self, handle: int, cfg: fdl_config):
+        self.handle = ctypes.c_void_p(handle)
+        self.cfg = cfg
+
+    def _check(self, st: int, what: str):
+        if st != FDL_OK:
+            msg = load_library().fdl_last_error(self.handle)
+            raise FdlError(st, f"{what}: {msg.decode() if msg else ''}")
+
+    def close(self):
+        if self.handle:
+            load_library().fdl_destroy(self.handle)
+            self.handle = ctypes.c_void_p(0)
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def tile_m(self) -> int:
+        return load_library().fdl_tile_m(self.handle)
+
+    def worklist_capacity(self, R: int, B: int) -> int:
+        return load_library().fdl_worklist_capacity(self.handle, R, B)
+
+    def set_stream(self, stream) -> None:
+        self._check(load_library().fdl_set_stream(self.handle, _stream_handle(stream)), "fdl_set_stream")
+
+    def sync_status(self) -> None:
+        self._check(load_library().fdl_sync_status(self.handle), "fdl_sync_status")
+
+    def qkv_rope_cache_write(self, X, Wqkv, row_seq, row_rope_pos, row_cache_pos, block_table,
+                             k_cache, v_cache, q_out) -> None:
+        R = int(X.shape[0])
+        st = load_library().fdl_qkv_rope_cache_write(
+            self.handle, _ptr(X), _ptr(Wqkv), R, _ptr(row_seq), _ptr(row_rope_pos), _ptr(row_cache_pos),
+            _ptr(block_table), int(block_table.shape[-1]), _ptr(k_cache), _ptr(v_cache), _ptr(q_out))
+        self._check(st, "fdl_qkv_rope_cache_write")
+
+    def sched_attn(self, q, k_cache, v_cache, block_table, cu_seqlens_q, kv_len, row_kind, o_out,
+                   lse_out=None, track_scores=None, search_pos=None, n_search=None,
+                   worklist_out=None) -> None:
+        B = int(kv_len.shape[0])
+        R = int(q.shape[0])
+        search_ld = int(search_pos.shape[-1]) if search_pos is not None else 0
+        track_ld = int(track_scores.shape[-1]) if track_scores is not None else 0
+        st = load_library().fdl_sched_attn(
+            self.handle, _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), int(block_table.shape[-1]),
+            _ptr(cu_seqlens_q), _ptr(kv_len), B, R, _ptr(row_kind), _ptr(search_pos), search_ld,
+            _ptr(n_search), _ptr(o_out), _ptr(lse_out), _ptr(track_scores), track_ld, _ptr(worklist_out))
+        self._check(st, "fdl_sched_attn")
+
+    def track_topk(self, scores, eligible, seq_len, k: int, idx_out, cnt_out) -> None:
+        B = int(seq_len.shape[0])
+        st = load_library().fdl_track_topk(self.handle, _ptr(scores), _ptr(eligible), int(scores.shape[-1]),
+                                           _ptr(seq_len), B, int(k), _ptr(idx_out), _ptr(cnt_out))
+        self._check(st, "fdl_track_topk")
+
+    def unmask_verify(self, B: int, max_search: int, *, logits=None, row_seq=None, row_pos=None,
+                      eps: float = 0.9, force_progress: bool = False, conf=None, argmax=None, commit=None,
+                      search_rows=None, n_search=None, mask_logits=None, draft_tok=None, gamma: float = 0.8,
+                      accept=None, n_accept=None, mask_conf=None, mask_argmax=None) -> None:
+        a = fdl_unmask_args()
+        a.B, a.max_search = int(B), int(max_search)
+        a.logits = _ptr(logits)
+        a.R_w = int(logits.shape[0]) if logits is not None else 0
+        a.row_seq, a.row_pos = _ptr(row_seq), _ptr(row_pos)
+        a.eps, a.force_progress = float(eps), int(bool(force_progress))
+        a.conf, a.argmax, a.commit = _ptr(conf), _ptr(argmax), _ptr(commit)
+        a.search_rows, a.n_search = _ptr(search_rows), _ptr(n_search)
+        a.mask_logits, a.draft_tok, a.gamma = _ptr(mask_logits), _ptr(draft_tok), float(gamma)
+        a.accept, a.n_accept = _ptr(accept), _ptr(n_accept)
+        a.mask_conf, a.mask_argmax = _ptr(mask_conf), _ptr(mask_argmax)
+        self._check(load_library().fdl_unmask_verify(self.handle, ctypes.byref(a)), "fdl_unmask_verify")
+
+
+def _stream_handle(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+def fdl_create(d_model: int, n_heads: int, head_dim: int, rope_theta: float, max_batch: int, max_seq: int,
+               max_views: int, page_size: int, n_pages: int, max_rows: int, vocab: int, dtype: str,
+               stream=None) -> Context:
+    """Creates a context on the current device (dtype 'f32' or 'bf16')."""
+    L = load_library()
+    cfg = fdl_config(d_model, n_heads, head_dim, float(rope_theta), max_batch, max_seq, max_views,
+                     page_size, n_pages, max_rows, vocab, FDL_BF16 if dtype == "bf16" else FDL_F32)
+    h = ctypes.c_void_p()
+    st = L.fdl_create(ctypes.byref(cfg), _stream_handle(stream), ctypes.byref(h))
+    if st != FDL_OK:
+        raise FdlError(st, "fdl_create failed (see stderr for the rejected limit)")
+    return Context(h.value, cfg)
+
+
+# C-named module functions over a Context.
+def fdl_destroy(ctx: Context) -> None:
+    ctx.close()
+
+
+def fdl_sync_status(ctx: Context) -> None:
+    ctx.sync_status()
+
+
+def fdl_qkv_rope_cache_write(ctx: Context, *a, **k) -> None:
+    ctx.qkv_rope_cache_write(*a, **k)
+
+
+def fdl_sched_attn(ctx: Context, *a, **k) -> None:
+    ctx.sched_attn(*a, **k)
+
+
+def fdl_track_topk(ctx: Context, *a, **k) -> None:
+    ctx.track_topk(*a, **k)
+
+
+def fdl_unmask_verify(ctx: Context, *a, **k) -> None:
+    ctx.unmask_verify(*a, **k)

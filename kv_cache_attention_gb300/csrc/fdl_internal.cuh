@@ -1,0 +1,100 @@
+// Internal declarations shared by the translation units of libfdl.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/fdl.h"
+
+// Device error-word bits (fdl_sync_status maps them to fdl_status).
+#define FDL_DEVERR_INDEX 1u    // out-of-range page / position / row index
+#define FDL_DEVERR_TIMEOUT 2u  // a bounded wait gave up
+#define FDL_DEVERR_SHAPE 4u    // inconsistent device-side shape data (cu_seqlens, kinds)
+
+// Rows per scheduled-attention work item.
+#define FDL_TILE_M_SIMT 16
+#define FDL_TILE_M_TC 128
+
+struct fdl_ctx {
+  fdl_config cfg;
+  cudaStream_t stream;
+  int device;
+  int num_sms;
+  int rope_positions;   // rows of the RoPE tables
+  float* rope_cos;      // [rope_positions][head_dim/2]
+  float* rope_sin;
+  unsigned* err_word;   // device error word
+  int attn_tile_m;      // query rows per attention work item
+  int* worklist;        // [1 + 4 * worklist_items]: count then items
+  int worklist_items;
+  int* n_masked;        // [max_batch] WINDOW rows per sequence
+  unsigned* tickets;    // [8] last-block tickets (left at zero between calls)
+  char last_error[512];
+};
+
+namespace fdl {
+
+__device__ __forceinline__ void raise_error(unsigned* err, unsigned bit) {
+  if (err) atomicOr(err, bit);
+}
+
+template <typename T>
+struct io;
+
+template <>
+struct io<float> {
+  static __device__ __forceinline__ float load(const float* p) { return *p; }
+  static __device__ __forceinline__ void store(float* p, float v) { *p = v; }
+};
+
+template <>
+struct io<__nv_bfloat16> {
+  static __device__ __forceinline__ float load(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+  static __device__ __forceinline__ void store(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+};
+
+// Slot of (sequence b, cache position c); -1 (and the error bit) when the
+// block table maps it outside the pool.
+__device__ __forceinline__ long long cache_slot(const int* block_table, int bt_stride, int page_size,
+                                                int n_pages, int b, int c, unsigned* err) {
+  if (c < 0) return -1;
+  int pi = c / page_size;
+  if (pi >= bt_stride) {
+    raise_error(err, FDL_DEVERR_INDEX);
+    return -1;
+  }
+  int page = block_table[(long long)b * bt_stride + pi];
+  if (page < 0 || page >= n_pages) {
+    raise_error(err, FDL_DEVERR_INDEX);
+    return -1;
+  }
+  return (long long)page * page_size + (c % page_size);
+}
+
+// Order-preserving map of a float onto uint32 (-0.0 folded onto +0.0).
+__device__ __forceinline__ unsigned float_order_key(float f) {
+  unsigned u = __float_as_uint(f);
+  if ((u << 1) == 0u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+}  // namespace fdl
+
+// Launchers implemented by the kernel translation units. Each returns a
+// cudaError_t from the launch.
+cudaError_t fdl_launch_qkv(fdl_ctx* ctx, const void* X, const void* W, int R, const int* row_seq,
+                           const int* row_rope_pos, const int* row_cache_pos,
+                           const int* block_table, int bt_stride, void* k_cache, void* v_cache,
+                           void* q_out);
+
+cudaError_t fdl_launch_attn(fdl_ctx* ctx, const void* q, const void* k_cache, const void* v_cache,
+                            const int* block_table, int bt_stride, const int* cu_seqlens_q,
+                            const int* kv_len, int B, int R, const int* row_kind,
+                            const int* search_pos, int search_ld, const int* n_search, void* o_out,
+                            float* lse_out, float* track, int track_ld, int* worklist_out);
+
+cudaError_t fdl_launch_topk(fdl_ctx* ctx, const float* scores, const unsigned char* eligible, int ld,
+                            const int* seq_len, int B, int k, int* idx_out, int* cnt_out);
+
+cudaError_t fdl_launch_unmask_verify(fdl_ctx* ctx, const fdl_unmask_args* a);

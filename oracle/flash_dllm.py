@@ -241,12 +241,14 @@ def sched_attn(q, k_cache, v_cache, block_table, page_size, cu_seqlens, kv_len,
             K = np.asarray(k_cache, np.float64)[slots].reshape(len(pos), H, hd)
             V = np.asarray(v_cache, np.float64)[slots].reshape(len(pos), H, hd)
             rows = np.asarray(rows)
-            s = np.einsum("rhd,nhd->hrn", q[rows], K) * scale
+            # s[h, r, n] = q[r, h, :] . K[n, h, :] / sqrt(hd)
+            s = np.matmul(q[rows].transpose(1, 0, 2), K.transpose(1, 2, 0)) * scale
             mx = s.max(axis=-1, keepdims=True)
             e = np.exp(s - mx)
             l = e.sum(axis=-1, keepdims=True)
             p = e / l
-            o[rows] = np.einsum("hrn,nhd->rhd", p, V)
+            # o[r, h, :] = sum_n p[h, r, n] V[n, h, :]
+            o[rows] = np.matmul(p, V.transpose(1, 0, 2)).transpose(1, 0, 2)
             lse[rows] = (mx + np.log(l))[..., 0].T
             if key == "plain" and n_masked:
                 sel = np.array([kinds[r - lo] == KIND_WINDOW for r in rows])
