@@ -1,7 +1,353 @@
-// tcgen05 path of the fused QKV projection (placeholder until written).
-#include "fdl_internal.cuh"
+// Fused QKV projection + RoPE + KV-cache scatter on the 5th-generation
+// tensor cores (tcgen05, accumulators in TMEM, operands staged by TMA).
+//
+// Paper digest "Flash-dLLM: IO-Aware KV Caching and Parallel Decoding ...",
+// section "Core method": the projection, RoPE and cache write are one kernel;
+// K and V leave the chip only as rows of the preallocated cache, Q only as
+// the attention input. "Method steps in detail", step 2: the rows are the
+// per-step refresh set (masked window + tracked tokens).
+//
+// Orientation ("swap AB"): the MMA computes D = W_tile . X_tile^T with the
+// 128 output features of a tile on the TMEM lanes and up to BN query rows
+// on the TMEM columns, so a refresh set of 64 rows still fills the M = 128
+// datapath. A tile is aligned to whole heads, so every RoPE pair (i, i +
+// head_dim/2) lives in the same CTA (exchanged through shared memory).
+//
+// Warp roles (192 threads): warp 0 issues TMA loads into a STAGES-deep
+// ring, warp 1 owns TMEM and issues tcgen05.mma (one elected lane), warps
+// 2-5 run the epilogue (TMEM -> registers -> RoPE -> bf16 -> 16-byte stores).
+// When the tiles cannot fill the GPU (the small refresh sets of the cache
+// phase), K is split across a thread-block cluster and partial sums meet in
+// the leader CTA's shared memory (DSMEM), in rank order, so results do not
+// depend on timing.
+#include <cudaTypedefs.h>
 
-cudaError_t fdl_launch_qkv_tc(fdl_ctx*, const void*, const void*, int, const int*, const int*, const int*,
-                              const int*, int, void*, void*, void*) {
-  return cudaErrorNotSupported;
+#include "fdl_internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kThreads = 192;
+constexpr int kEpiThreads = 128;
+constexpr int kXStride = 33;  // fp32 exchange buffer row stride (conflict-free)
+
+template <int BN>
+struct Cfg {
+  static constexpr int A_BYTES = kBM * kBK * 2;
+  static constexpr int B_BYTES = BN * kBK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = BN == 64 ? 3 : (BN == 128 ? 5 : 4);
+  static constexpr int PIPE_BYTES = STAGES * STAGE_BYTES;
+  static constexpr int XBUF_BYTES = kBM * kXStride * 4;
+  static constexpr int META_BYTES = BN * 16;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int SMEM_BYTES = 1024 + PIPE_BYTES + XBUF_BYTES + META_BYTES + BAR_BYTES;
+  static constexpr int MAX_SPLIT = 1 + PIPE_BYTES / (kBM * BN * 4);
+};
+
+struct TcParams {
+  int R, d, hd, nkb, ksplit;
+  const int* row_seq;
+  const int* row_rope_pos;
+  const int* row_cache_pos;
+  const int* block_table;
+  int bt_stride, page_size, n_pages;
+  __nv_bfloat16* q_out;
+  __nv_bfloat16* k_cache;
+  __nv_bfloat16* v_cache;
+  const float* rope_cos;
+  const float* rope_sin;
+  int rope_positions;
+  unsigned* err;
+};
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    qkv_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
+                  const TcParams p) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* pipe = smem;
+  float* xbuf = reinterpret_cast<float*>(smem + C::PIPE_BYTES);
+  int* col_pos = reinterpret_cast<int*>(smem + C::PIPE_BYTES + C::XBUF_BYTES);
+  long long* col_dst = reinterpret_cast<long long*>(col_pos + BN);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::PIPE_BYTES + C::XBUF_BYTES + C::META_BYTES);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + C::STAGES;
+  uint64_t* tmem_full = bars + 2 * C::STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tmem_full + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ks = p.ksplit;
+  const uint32_t rank = ks > 1 ? tc::cluster_ctarank() : 0u;
+  const int tile_r = blockIdx.y, tile_f = blockIdx.z;
+  const int f0 = tile_f * kBM;
+  const int section = f0 / p.d;  // 0 = Q, 1 = K, 2 = V (tiles never straddle)
+  const int kb0 = (int)(rank * p.nkb / ks), kb1 = (int)((rank + 1) * p.nkb / ks);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    tc::mbar_init(tmem_full, 1);
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_slot, BN);
+    tc::tmem_relinquish();
+  }
+  if (warp >= 2 && rank == 0) {
+    // per-column (query row) destination and RoPE position
+    for (int c = threadIdx.x - 64; c < BN; c += kEpiThreads) {
+      const int r = tile_r * BN + c;
+      int pos = -1;
+      long long dst = -1;
+      if (r < p.R) {
+        pos = p.row_rope_pos[r];
+        if (pos < 0 || pos >= p.rope_positions) {
+          fdl::raise_error(p.err, FDL_DEVERR_INDEX);
+          pos = -1;
+        } else if (section == 0) {
+          dst = (long long)r * p.d + f0;
+        } else {
+          const int cp = p.row_cache_pos[r];
+          if (cp >= 0) {
+            long long slot = fdl::cache_slot(p.block_table, p.bt_stride, p.page_size, p.n_pages, p.row_seq[r], cp,
+                                             p.err);
+            if (slot >= 0) dst = slot * p.d + (f0 - section * p.d);
+          }
+        }
+      }
+      col_pos[c] = pos;
+      col_dst[c] = pos >= 0 ? dst : -1;
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tc::prefetch_tensormap(&tmap_w);
+      tc::prefetch_tensormap(&tmap_x);
+      int it = 0;
+      for (int kb = kb0; kb < kb1; ++kb, ++it) {
+        const int s = it % C::STAGES;
+        const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
+        if (!tc::mbar_wait(&empty[s], ph ^ 1u, abort_flag)) break;
+        uint8_t* a = pipe + s * C::STAGE_BYTES;
+        tc::mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+        tc::tma_load_2d(a, &tmap_w, kb * kBK, f0, &full[s]);
+        tc::tma_load_2d(a + C::A_BYTES, &tmap_x, kb * kBK, tile_r * BN, &full[s]);
+      }
+      if (*abort_flag) {
+        // let loads already in flight land before this CTA's memory is reused
+        for (int j = max(0, it - C::STAGES); j < it; ++j) {
+          long long t0 = clock64();
+          while (!tc::mbar_try_wait(&full[j % C::STAGES], (uint32_t)(j / C::STAGES) & 1u) &&
+                 clock64() - t0 < tc::kWaitBudgetCycles / 8) {
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(kBM, BN);
+      int it = 0;
+      for (int kb = kb0; kb < kb1; ++kb, ++it) {
+        const int s = it % C::STAGES;
+        const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
+        if (!tc::mbar_wait(&full[s], ph, abort_flag)) break;
+        tc::fence_after_sync();
+        const uint32_t a = tc::smem_addr(pipe + s * C::STAGE_BYTES);
+        const uint64_t ad = tc::desc_kmajor_sw128(a);
+        const uint64_t bd = tc::desc_kmajor_sw128(a + C::A_BYTES);
+#pragma unroll
+        for (int k = 0; k < kBK / 16; ++k)
+          tc::mma_bf16_ss(tmem, ad + 2 * k, bd + 2 * k, idesc, (it > 0 || k > 0) ? 1u : 0u);
+        tc::mma_commit(&empty[s]);
+      }
+      tc::mma_commit(tmem_full);
+    }
+    __syncwarp();
+  } else {
+    tc::mbar_wait(tmem_full, 0, abort_flag);
+    tc::fence_after_sync();
+  }
+
+  const int q = warp & 3;          // TMEM lane quadrant of this warp
+  const int t = q * 32 + lane;     // tile row = output feature f0 + t
+  const uint32_t t_lane = tmem + ((uint32_t)(q * 32) << 16);
+  float* recv = reinterpret_cast<float*>(pipe);  // [ks-1][BN][128], valid after cluster barrier 1
+
+  if (ks > 1) {
+    tc::cluster_sync();  // every CTA's MMAs are complete: pipeline memory is free
+    if (rank != 0 && warp >= 2 && !*abort_flag) {
+      const uint32_t remote = tc::map_cluster(tc::smem_addr(recv), 0);
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        float v[32];
+        tc::tmem_ld_32x32b_x32(t_lane + c0, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          tc::st_cluster_f32(remote + 4u * (uint32_t)((((int)rank - 1) * BN + c0 + j) * kBM + t), v[j]);
+      }
+    }
+    tc::cluster_sync();  // partial sums have landed in the leader
+  }
+
+  if (rank == 0 && warp >= 2 && !*abort_flag) {
+    const int half = p.hd / 2;
+    const int i = (f0 + t) % p.hd;
+    const int jj = i % half;
+    const bool low = i < half;
+    const int partner = t ^ half;
+    __nv_bfloat16* out = section == 0 ? p.q_out : (section == 1 ? p.k_cache : p.v_cache);
+    __nv_bfloat16* obuf = reinterpret_cast<__nv_bfloat16*>(xbuf);  // [32][128] bf16, aliases xbuf
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+      float v[32];
+      tc::tmem_ld_32x32b_x32(t_lane + c0, v);
+      for (int src = 0; src < ks - 1; ++src)
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] += recv[(src * BN + c0 + j) * kBM + t];
+      tc::named_bar(1, kEpiThreads);  // previous chunk's readers of xbuf/obuf are done
+      if (section < 2) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) xbuf[t * kXStride + j] = v[j];
+        tc::named_bar(1, kEpiThreads);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int pos = col_pos[c0 + j];
+          if (pos < 0) continue;
+          const float cs = __ldg(p.rope_cos + (size_t)pos * half + jj);
+          const float sn = __ldg(p.rope_sin + (size_t)pos * half + jj);
+          const float other = xbuf[partner * kXStride + j];
+          v[j] = low ? (v[j] * cs - other * sn) : (other * sn + v[j] * cs);
+        }
+        tc::named_bar(1, kEpiThreads);  // exchange reads done before obuf overwrites xbuf
+      }
+#pragma unroll
+      for (int j = 0; j < 32; ++j) obuf[j * kBM + t] = __float2bfloat16_rn(v[j]);
+      tc::named_bar(1, kEpiThreads);
+      // 32 rows x 256 bytes: 16-byte chunks, consecutive threads on consecutive chunks
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int id = t + kEpiThreads * u;
+        const int j = id >> 4, part = id & 15;
+        const long long dst = col_dst[c0 + j];
+        if (dst >= 0)
+          *reinterpret_cast<int4*>(out + dst + part * 8) = *reinterpret_cast<const int4*>(obuf + j * kBM + part * 8);
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) fdl::raise_error(p.err, FDL_DEVERR_TIMEOUT);
+  if (warp == 1) tc::tmem_dealloc(tmem, BN);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+// 2-D bf16 row-major [rows, cols] map, box = 64 columns x box_rows rows,
+// 128-byte swizzle (the layout desc_kmajor_sw128 describes).
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN>
+cudaError_t launch(fdl_ctx* ctx, const TcParams& p0, const void* X, const void* W) {
+  using Cf = Cfg<BN>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(qkv_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const fdl_config& c = ctx->cfg;
+  CUtensorMap mw, mx;
+  if (!make_map(&mw, W, (uint64_t)3 * c.d_model, c.d_model, kBM) || !make_map(&mx, X, p0.R, c.d_model, BN))
+    return cudaErrorInvalidValue;
+  TcParams p = p0;
+  const int tiles_r = (p.R + BN - 1) / BN, tiles_f = 3 * c.d_model / kBM;
+  const int tiles = tiles_r * tiles_f;
+  const int per_sm = Cf::SMEM_BYTES * 2 <= 227 * 1024 ? 2 : 1;
+  int ks = 1;
+  if (tiles < ctx->num_sms * per_sm) ks = (ctx->num_sms * per_sm) / tiles;
+  ks = max(1, min(ks, min(Cf::MAX_SPLIT, min(p.nkb, 8))));
+  p.ksplit = ks;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ks, tiles_r, tiles_f);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Cf::SMEM_BYTES;
+  cfg.stream = ctx->stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = ks;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = ks > 1 ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, qkv_tc_kernel<BN>, mw, mx, p);
+}
+
+}  // namespace
+
+cudaError_t fdl_launch_qkv_tc(fdl_ctx* ctx, const void* X, const void* W, int R, const int* row_seq,
+                              const int* row_rope_pos, const int* row_cache_pos, const int* block_table,
+                              int bt_stride, void* k_cache, void* v_cache, void* q_out) {
+  const fdl_config& c = ctx->cfg;
+  if (c.d_model % kBM != 0 || (c.head_dim != 64 && c.head_dim != 128)) return cudaErrorNotSupported;
+  if ((reinterpret_cast<uintptr_t>(X) & 15) || (reinterpret_cast<uintptr_t>(W) & 15) ||
+      (reinterpret_cast<uintptr_t>(q_out) & 15) || (reinterpret_cast<uintptr_t>(k_cache) & 15) ||
+      (reinterpret_cast<uintptr_t>(v_cache) & 15))
+    return cudaErrorNotSupported;
+  TcParams p;
+  p.R = R;
+  p.d = c.d_model;
+  p.hd = c.head_dim;
+  p.nkb = c.d_model / kBK;
+  p.ksplit = 1;
+  p.row_seq = row_seq;
+  p.row_rope_pos = row_rope_pos;
+  p.row_cache_pos = row_cache_pos;
+  p.block_table = block_table;
+  p.bt_stride = bt_stride;
+  p.page_size = c.page_size;
+  p.n_pages = c.n_pages;
+  p.q_out = reinterpret_cast<__nv_bfloat16*>(q_out);
+  p.k_cache = reinterpret_cast<__nv_bfloat16*>(k_cache);
+  p.v_cache = reinterpret_cast<__nv_bfloat16*>(v_cache);
+  p.rope_cos = ctx->rope_cos;
+  p.rope_sin = ctx->rope_sin;
+  p.rope_positions = ctx->rope_positions;
+  p.err = ctx->err_word;
+  if (R <= 64) return launch<64>(ctx, p, X, W);
+  if (R <= 128) return launch<128>(ctx, p, X, W);
+  return launch<256>(ctx, p, X, W);
 }

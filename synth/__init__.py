@@ -440,3 +440,30 @@ def flash_verify(seed: int = 1005, batch: int = 32) -> Workload:
         window_rows=np.arange(n_w, dtype=np.int32),
         window_row_seq=np.repeat(np.arange(batch, dtype=np.int32), window),
         window_row_pos=np.tile(window_pos, batch).astype(np.int32)))
+
+
+def projection_case(seed: int, d_model: int, n_heads: int, n_rows: int, batch: int = 3,
+                    seq_len: int = 300, page_size: int = 64, theta: float = LLADA_THETA,
+                    dtype: str = "bf16") -> Workload:
+    """Generic fused-projection case: random rows over a paged cache.
+
+    Rows belong to ``batch`` sequences (sorted by sequence), sit at random
+    positions below ``seq_len``, and one row in seven is not written to the
+    cache (cache_pos -1) as for rows that only need their query.
+    """
+    rng = np.random.default_rng(seed)
+    hd = d_model // n_heads
+    shape = LayerShape(d_model, n_heads, hd, theta, dtype)
+    geom = paged_geometry(rng, [seq_len] * batch, page_size)
+    w = make_tensor(normal(rng, (3 * d_model, d_model), 0.02), dtype)
+    x = make_tensor(normal(rng, (n_rows, d_model)), dtype)
+    seq = np.sort(rng.integers(0, batch, n_rows)).astype(np.int32)
+    per_seq = []
+    for b in range(batch):
+        n_b = int(np.sum(seq == b))
+        pos = rng.choice(seq_len, size=n_b, replace=False)
+        per_seq.append([(int(p), int(p) if rng.uniform() > 1 / 7 else -1, KIND_NORMAL) for p in pos])
+    rows = build_rows(per_seq)
+    kc, vc = _cache_fill(rng, geom.n_pages * geom.page_size, d_model, dtype)
+    return Workload("projection_case", shape, batch, np.full(batch, seq_len, np.int32), seq_len, 0, geom,
+                    dict(w=w, x=x, rows=rows, k_cache=kc, v_cache=vc))
