@@ -181,6 +181,7 @@ fdl_status fdl_sched_attn(fdl_ctx* ctx, const void* q, const void* k_cache, cons
     return fail(ctx, FDL_ERR_INVALID_ARG, "B=%d outside [0, max_batch=%d]", B, ctx->cfg.max_batch);
   if (R < 0 || R > ctx->cfg.max_rows)
     return fail(ctx, FDL_ERR_INVALID_ARG, "R=%d outside [0, max_rows=%d]", R, ctx->cfg.max_rows);
+  if (B == 0 || R == 0) return FDL_OK;
   if (!q || !k_cache || !v_cache || !block_table || !cu_seqlens_q || !kv_len || !row_kind || !o_out)
     return fail(ctx, FDL_ERR_INVALID_ARG, "fdl_sched_attn: NULL pointer argument");
   if (bt_stride <= 0) return fail(ctx, FDL_ERR_INVALID_ARG, "bt_stride must be positive");
@@ -190,7 +191,6 @@ fdl_status fdl_sched_attn(fdl_ctx* ctx, const void* q, const void* k_cache, cons
     return fail(ctx, FDL_ERR_INVALID_ARG, "search_pos given but the context has max_views = 0");
   if (track_scores && track_ld < ctx->cfg.max_seq)
     return fail(ctx, FDL_ERR_INVALID_ARG, "track_ld=%d below max_seq=%d", track_ld, ctx->cfg.max_seq);
-  if (B == 0 || R == 0) return FDL_OK;
   return launched(ctx, fdl_launch_attn(ctx, q, k_cache, v_cache, block_table, bt_stride, cu_seqlens_q,
                                        kv_len, B, R, row_kind, search_pos, search_ld, n_search, o_out,
                                        lse_out, track_scores, track_ld, worklist_out),

@@ -1,0 +1,166 @@
+"""32-layer attention path (LLaDA-8B shapes, bf16, batch 8, prompt 256 +
+gen 512, window 32) with chained denoising steps: each step refreshes the
+window and the previous step's top-32 tracked tokens in every layer, and the
+tracker scores are summed over layers (Eq. (2)).
+
+test_chain_teacher_forced: 2 layers x (init + 2 steps); at every stage the
+GPU consumes exactly the oracle's inputs (its stored caches and Q, its
+float32 scores) so each kernel is held to the stage tolerances, and the
+tracked sets feeding the next step are identical on both sides.
+
+test_chain_full_size: the full 32 layers x 16 steps on the GPU alone, checked
+by properties that hold at any size: every sequence's scores sum to the
+number of layers, top-32 equals a full sort of the scores the kernel got,
+sampled projection rows match the oracle, and a re-run is bit-identical."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests import _harness as H
+
+pytestmark = pytest.mark.gpu
+
+
+def _setup(n_layers, n_steps):
+    import kv_cache_attention_gb300 as fdl
+    wl = synth.layer_chain(n_layers=n_layers, n_steps=n_steps)
+    s, g, e = wl.shape, wl.geom, wl.extra
+    R_init = wl.batch * wl.max_seq
+    ctx = fdl.fdl_create(s.d_model, s.n_heads, s.head_dim, s.rope_theta, wl.batch, wl.max_seq, 0, g.page_size,
+                         g.n_pages, R_init, 16, s.dtype)
+    return wl, ctx
+
+
+def _rows(wl, step, tracked):
+    e = wl.extra
+    if step == 0:
+        return synth.build_rows([synth.full_rows(wl.max_seq, e["window_pos"]) for _ in range(wl.batch)])
+    return synth.build_rows([synth.draft_rows(e["window_pos"], tracked[b]) for b in range(wl.batch)])
+
+
+def test_chain_teacher_forced():
+    import torch
+    L, S = 2, 2
+    wl, ctx = _setup(L, S)
+    s, g, e = wl.shape, wl.geom, wl.extra
+    Hh, hd, d, dt, B, N = s.n_heads, s.head_dim, s.d_model, s.dtype, wl.batch, wl.max_seq
+    seed = e["seed"]
+    bt = H.ints(g.block_table)
+    kv_len = wl.seq_len
+    n_slots = g.n_pages * g.page_size
+    caches = [(np.zeros((n_slots, d)), np.zeros((n_slots, d))) for _ in range(L)]
+    tracked = None
+    k = e["topk"]
+    for step in range(S + 1):
+        rows = _rows(wl, step, tracked)
+        R = rows.n_rows
+        score_o = np.zeros((B, N))
+        score_g = torch.zeros((B, N), dtype=torch.float32, device="cuda")
+        for layer in range(L):
+            w = synth.chain_weight(seed, layer, d)
+            x = synth.chain_hidden(seed, step, layer, R, d)
+            kc_o, vc_o = caches[layer]
+            kc, vc = H.dev(synth.make_tensor(kc_o, dt)), H.dev(synth.make_tensor(vc_o, dt))
+            q = H.empty((R, Hh, hd), dt)
+            ctx.qkv_rope_cache_write(H.dev(x), H.dev(w), H.ints(rows.row_seq), H.ints(rows.row_rope_pos),
+                                     H.ints(rows.row_cache_pos), bt, kc, vc, q)
+            ctx.sync_status()
+            q_o, kc_o, vc_o = oracle.qkv_rope_cache_write(
+                x.values(), w.values(), Hh, hd, s.rope_theta, rows.row_rope_pos, rows.row_seq, rows.row_cache_pos,
+                g.block_table, g.page_size, kc_o, vc_o, dt)
+            H.assert_close(H.host(q), q_o, dt, f"q step {step} layer {layer}")
+            written = oracle.slot_map(rows.row_seq, rows.row_cache_pos, g.block_table, g.page_size)
+            H.assert_close(H.host(kc)[written], kc_o[written], dt, f"k step {step} layer {layer}")
+            H.assert_close(H.host(vc)[written], vc_o[written], dt, f"v step {step} layer {layer}")
+            caches[layer] = (kc_o, vc_o)
+            q = H.dev(synth.make_tensor(q_o, dt))
+            kc, vc = H.dev(synth.make_tensor(kc_o, dt)), H.dev(synth.make_tensor(vc_o, dt))
+            o = H.empty((R, Hh, hd), dt)
+            lse = torch.empty((R, Hh), dtype=torch.float32, device="cuda")
+            before = score_g.clone()
+            ctx.sched_attn(q, kc, vc, bt, H.ints(rows.cu_seqlens), H.ints(kv_len), H.ints(rows.row_kind), o,
+                           lse_out=lse, track_scores=score_g)
+            ctx.sync_status()
+            o_o, lse_o, tr_o = oracle.sched_attn(q_o, kc_o, vc_o, g.block_table, g.page_size, rows.cu_seqlens,
+                                                 kv_len, rows.row_kind, max_seq=N, dtype=dt)
+            H.assert_close(H.host(o), o_o, dt, f"O step {step} layer {layer}")
+            H.assert_close(H.host(lse), lse_o, "f32", f"LSE step {step} layer {layer}")
+            H.assert_close(H.host(score_g) - H.host(before), tr_o, "f32", f"tracker step {step} layer {layer}")
+            score_o += tr_o
+        np.testing.assert_allclose(score_o.sum(1), L, atol=1e-9)
+        sc32 = score_o.astype(np.float32)
+        idx = torch.empty((B, k), dtype=torch.int32, device="cuda")
+        cnt = torch.empty((B,), dtype=torch.int32, device="cuda")
+        ctx.track_topk(H.dev(sc32), H.u8(e["eligible"]), H.ints(kv_len), k, idx, cnt)
+        ctx.sync_status()
+        idx_o, cnt_o = oracle.track_topk(sc32, e["eligible"], kv_len, k)
+        assert H.host(idx).tolist() == idx_o.tolist()
+        assert H.host(cnt).tolist() == cnt_o.tolist()
+        tracked = [idx_o[b, :cnt_o[b]] for b in range(B)]
+    ctx.close()
+
+
+@pytest.mark.slow
+def test_chain_full_size():
+    import torch
+    L, S = 32, 16
+    wl, ctx = _setup(L, S)
+    s, g, e = wl.shape, wl.geom, wl.extra
+    Hh, hd, d, dt, B, N = s.n_heads, s.head_dim, s.d_model, s.dtype, wl.batch, wl.max_seq
+    seed = e["seed"]
+    bt = H.ints(g.block_table)
+    kv_len = H.ints(wl.seq_len)
+    n_slots = g.n_pages * g.page_size
+    W = [H.dev(synth.chain_weight(seed, l, d)) for l in range(L)]
+    elig = H.u8(e["eligible"])
+    k = e["topk"]
+    sample_layers = (0, 15, 31)
+
+    def run(check):
+        caches = [(torch.zeros((n_slots, d), dtype=torch.bfloat16, device="cuda"),
+                   torch.zeros((n_slots, d), dtype=torch.bfloat16, device="cuda")) for _ in range(L)]
+        tracked, hist = None, []
+        for step in range(S + 1):
+            rows = _rows(wl, step, tracked)
+            R = rows.n_rows
+            score = torch.zeros((B, N), dtype=torch.float32, device="cuda")
+            rs, rp, rc, rk, cu = (H.ints(rows.row_seq), H.ints(rows.row_rope_pos), H.ints(rows.row_cache_pos),
+                                  H.ints(rows.row_kind), H.ints(rows.cu_seqlens))
+            q = H.empty((R, Hh, hd), dt)
+            o = H.empty((R, Hh, hd), dt)
+            for layer in range(L):
+                x = synth.chain_hidden(seed, step, layer, R, d)
+                kc, vc = caches[layer]
+                ctx.qkv_rope_cache_write(H.dev(x), W[layer], rs, rp, rc, bt, kc, vc, q)
+                if check and layer in sample_layers and step in (0, S):
+                    ctx.sync_status()
+                    pick = np.random.default_rng(step * 100 + layer).choice(R, size=16, replace=False)
+                    w = synth.chain_weight(seed, layer, d)
+                    q_o, _, _ = oracle.qkv_rope_cache_write(
+                        x.values()[pick], w.values(), Hh, hd, s.rope_theta, rows.row_rope_pos[pick],
+                        rows.row_seq[pick], np.full(16, -1), g.block_table, g.page_size,
+                        np.zeros((1, d)), np.zeros((1, d)), dt)
+                    H.assert_close(H.host(q)[pick], q_o, dt, f"sampled q step {step} layer {layer}")
+                ctx.sched_attn(q, kc, vc, bt, cu, kv_len, rk, o, track_scores=score)
+            idx = torch.empty((B, k), dtype=torch.int32, device="cuda")
+            cnt = torch.empty((B,), dtype=torch.int32, device="cuda")
+            ctx.track_topk(score, elig, kv_len, k, idx, cnt)
+            ctx.sync_status()
+            sc, ih = H.host(score), H.host(idx)
+            if check:
+                np.testing.assert_allclose(sc.sum(1), L, rtol=1e-4)
+                for b in range(B):
+                    pos = np.nonzero(e["eligible"][b])[0]
+                    order = pos[np.lexsort((pos, -sc[b, pos].astype(np.float64)))]
+                    assert ih[b].tolist() == order[:k].tolist()
+            hist.append((sc, ih))
+            tracked = [ih[b] for b in range(B)]
+        return hist
+
+    first = run(True)
+    second = run(False)
+    for (s1, i1), (s2, i2) in zip(first, second):
+        assert np.array_equal(i1, i2)
+        np.testing.assert_allclose(s1, s2, rtol=0, atol=1e-6)
+    ctx.close()
