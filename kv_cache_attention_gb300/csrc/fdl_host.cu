@@ -96,6 +96,13 @@ fdl_status fdl_create(const fdl_config* cfg, void* cuda_stream, fdl_ctx** out) {
   e = e ? e : cudaMalloc(&ctx->worklist, (1 + 4 * (size_t)ctx->worklist_items) * sizeof(int));
   e = e ? e : cudaMalloc(&ctx->n_masked, cfg->max_batch * sizeof(int));
   e = e ? e : cudaMalloc(&ctx->tickets, 8 * sizeof(unsigned));
+  if (cfg->dtype == FDL_BF16) {
+    ctx->qkv_partial_floats = fdl_qkv_partial_floats(ctx->num_sms);
+    ctx->qkv_tickets = 4 * ctx->num_sms;
+    e = e ? e : cudaMalloc(&ctx->qkv_partials, ctx->qkv_partial_floats * sizeof(float));
+    e = e ? e : cudaMalloc(&ctx->qkv_ticket_buf, ctx->qkv_tickets * sizeof(unsigned));
+    e = e ? e : cudaMemset(ctx->qkv_ticket_buf, 0, ctx->qkv_tickets * sizeof(unsigned));
+  }
   e = e ? e : cudaMemcpy(ctx->rope_cos, hc.data(), n_tab * sizeof(float), cudaMemcpyHostToDevice);
   e = e ? e : cudaMemcpy(ctx->rope_sin, hs.data(), n_tab * sizeof(float), cudaMemcpyHostToDevice);
   e = e ? e : cudaMemset(ctx->err_word, 0, sizeof(unsigned));
@@ -116,6 +123,8 @@ void fdl_destroy(fdl_ctx* ctx) {
   cudaFree(ctx->worklist);
   cudaFree(ctx->n_masked);
   cudaFree(ctx->tickets);
+  cudaFree(ctx->qkv_partials);
+  cudaFree(ctx->qkv_ticket_buf);
   free(ctx);
 }
 

@@ -30,6 +30,10 @@ struct fdl_ctx {
   int worklist_items;
   int* n_masked;        // [max_batch] WINDOW rows per sequence
   unsigned* tickets;    // [8] last-block tickets (left at zero between calls)
+  float* qkv_partials;  // split-K partial tiles of the tensor-core projection
+  size_t qkv_partial_floats;
+  unsigned* qkv_ticket_buf;  // per-tile arrival counters (zero between calls)
+  int qkv_tickets;
   char last_error[512];
 };
 
@@ -98,3 +102,6 @@ cudaError_t fdl_launch_topk(fdl_ctx* ctx, const float* scores, const unsigned ch
                             const int* seq_len, int B, int k, int* idx_out, int* cnt_out);
 
 cudaError_t fdl_launch_unmask_verify(fdl_ctx* ctx, const fdl_unmask_args* a);
+
+// Workspace floats the tensor-core projection needs for split-K partials.
+size_t fdl_qkv_partial_floats(int num_sms);

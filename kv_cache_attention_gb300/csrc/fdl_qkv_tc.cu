@@ -17,13 +17,17 @@
 // ring, warp 1 owns TMEM and issues tcgen05.mma (one elected lane), warps
 // 2-5 run the epilogue (TMEM -> registers -> RoPE -> bf16 -> 16-byte stores).
 // When the tiles cannot fill the GPU (the small refresh sets of the cache
-// phase), K is split across a thread-block cluster and partial sums meet in
-// the leader CTA's shared memory (DSMEM), in rank order, so results do not
-// depend on timing.
+// phase), K is split across ks CTAs that stay resident together (two per
+// SM for 64-row tiles). Each writes its fp32 partial tile to a workspace
+// slot; the last CTA of a tile to arrive (an atomic ticket it resets) sums
+// the ks partials in split order, so results do not depend on timing, and
+// runs the epilogue. The ticket is a plain counter, never waited on.
 #include <cudaTypedefs.h>
 
 #include "fdl_internal.cuh"
 #include "tc_ptx.cuh"
+
+int qkv_ctas_per_sm(int bn);
 
 namespace {
 
@@ -38,13 +42,13 @@ struct Cfg {
   static constexpr int A_BYTES = kBM * kBK * 2;
   static constexpr int B_BYTES = BN * kBK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = BN == 64 ? 3 : (BN == 128 ? 5 : 4);
+  static constexpr int STAGES = BN == 64 ? 4 : (BN == 128 ? 6 : 4);
   static constexpr int PIPE_BYTES = STAGES * STAGE_BYTES;
-  static constexpr int XBUF_BYTES = kBM * kXStride * 4;
+  static constexpr int XBUF_BYTES = kBM * kXStride * 4;  // aliases the drained ring
   static constexpr int META_BYTES = BN * 16;
   static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM_BYTES = 1024 + PIPE_BYTES + XBUF_BYTES + META_BYTES + BAR_BYTES;
-  static constexpr int MAX_SPLIT = 1 + PIPE_BYTES / (kBM * BN * 4);
+  static constexpr int SMEM_BYTES = 1024 + PIPE_BYTES + META_BYTES + BAR_BYTES;
+  static_assert(XBUF_BYTES <= PIPE_BYTES, "exchange buffer must fit in the ring");
 };
 
 struct TcParams {
@@ -60,31 +64,35 @@ struct TcParams {
   const float* rope_cos;
   const float* rope_sin;
   int rope_positions;
+  float* partials;     // [tiles * ksplit][BN][128] fp32 split-K partial tiles
+  unsigned* tickets;   // [tiles] arrival counters, zero between launches
   unsigned* err;
 };
 
 template <int BN>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, BN == 64 ? 2 : 1)
     qkv_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
                   const TcParams p) {
   using C = Cfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* pipe = smem;
-  float* xbuf = reinterpret_cast<float*>(smem + C::PIPE_BYTES);
-  int* col_pos = reinterpret_cast<int*>(smem + C::PIPE_BYTES + C::XBUF_BYTES);
+  float* xbuf = reinterpret_cast<float*>(pipe);  // used only after the ring has drained
+  int* col_pos = reinterpret_cast<int*>(smem + C::PIPE_BYTES);
   long long* col_dst = reinterpret_cast<long long*>(col_pos + BN);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::PIPE_BYTES + C::XBUF_BYTES + C::META_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::PIPE_BYTES + C::META_BYTES);
   uint64_t* full = bars;
   uint64_t* empty = bars + C::STAGES;
   uint64_t* tmem_full = bars + 2 * C::STAGES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tmem_full + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* is_last = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ks = p.ksplit;
-  const uint32_t rank = ks > 1 ? tc::cluster_ctarank() : 0u;
+  const uint32_t rank = blockIdx.x;  // split index along K
   const int tile_r = blockIdx.y, tile_f = blockIdx.z;
+  const int tile_lin = tile_f * gridDim.y + tile_r;
   const int f0 = tile_f * kBM;
   const int section = f0 / p.d;  // 0 = Q, 1 = K, 2 = V (tiles never straddle)
   const int kb0 = (int)(rank * p.nkb / ks), kb1 = (int)((rank + 1) * p.nkb / ks);
@@ -96,13 +104,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc::mbar_init(tmem_full, 1);
     *abort_flag = 0;
+    *is_last = ks == 1;
     tc::fence_mbar_init();
   }
   if (warp == 1) {
     tc::tmem_alloc(tmem_slot, BN);
     tc::tmem_relinquish();
   }
-  if (warp >= 2 && rank == 0) {
+  if (warp >= 2) {
     // per-column (query row) destination and RoPE position
     for (int c = threadIdx.x - 64; c < BN; c += kEpiThreads) {
       const int r = tile_r * BN + c;
@@ -186,59 +195,88 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q = warp & 3;          // TMEM lane quadrant of this warp
   const int t = q * 32 + lane;     // tile row = output feature f0 + t
   const uint32_t t_lane = tmem + ((uint32_t)(q * 32) << 16);
-  float* recv = reinterpret_cast<float*>(pipe);  // [ks-1][BN][128], valid after cluster barrier 1
+  const bool epi = warp >= 2 && !*abort_flag;
 
-  if (ks > 1) {
-    tc::cluster_sync();  // every CTA's MMAs are complete: pipeline memory is free
-    if (rank != 0 && warp >= 2 && !*abort_flag) {
-      const uint32_t remote = tc::map_cluster(tc::smem_addr(recv), 0);
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        float v[32];
-        tc::tmem_ld_32x32b_x32(t_lane + c0, v);
+  if (ks > 1 && epi) {
+    // publish this split's partial tile, then take a ticket
+    float* mine = p.partials + ((size_t)tile_lin * ks + rank) * BN * kBM;
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+      float v[32];
+      tc::tmem_ld_32x32b_x32(t_lane + c0, v);
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          tc::st_cluster_f32(remote + 4u * (uint32_t)((((int)rank - 1) * BN + c0 + j) * kBM + t), v[j]);
-      }
+      for (int j = 0; j < 32; ++j) __stcg(mine + (c0 + j) * kBM + t, v[j]);
     }
-    tc::cluster_sync();  // partial sums have landed in the leader
+    __threadfence();
+    tc::named_bar(1, kEpiThreads);
+    if (t == 0) {
+      const unsigned prev = atomicAdd(p.tickets + tile_lin, 1u);
+      *is_last = prev == (unsigned)(ks - 1);
+      if (*is_last) p.tickets[tile_lin] = 0u;  // every split has arrived: reset for the next launch
+    }
+    tc::named_bar(1, kEpiThreads);
+    if (*is_last) __threadfence();
   }
 
-  if (rank == 0 && warp >= 2 && !*abort_flag) {
+  if (epi && *is_last) {
     const int half = p.hd / 2;
     const int i = (f0 + t) % p.hd;
     const int jj = i % half;
     const bool low = i < half;
     const int partner = t ^ half;
     __nv_bfloat16* out = section == 0 ? p.q_out : (section == 1 ? p.k_cache : p.v_cache);
-    __nv_bfloat16* obuf = reinterpret_cast<__nv_bfloat16*>(xbuf);  // [32][128] bf16, aliases xbuf
-    for (int c0 = 0; c0 < BN; c0 += 32) {
-      float v[32];
-      tc::tmem_ld_32x32b_x32(t_lane + c0, v);
-      for (int src = 0; src < ks - 1; ++src)
+    __nv_bfloat16* obuf = reinterpret_cast<__nv_bfloat16*>(xbuf);  // [16][128] bf16, aliases xbuf
+    const float* parts = p.partials + (size_t)tile_lin * ks * BN * kBM;
+    constexpr int CH = 16;  // columns per epilogue chunk
+    for (int c0 = 0; c0 < BN; c0 += CH) {
+      // issue this chunk's RoPE table loads first so their latency overlaps
+      // the TMEM and partial-sum loads (one round trip per chunk)
+      float cs[CH], sn[CH];
+      if (section < 2) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] += recv[(src * BN + c0 + j) * kBM + t];
+        for (int j = 0; j < CH; ++j) {
+          const int pos = max(col_pos[c0 + j], 0);
+          cs[j] = __ldg(p.rope_cos + (size_t)pos * half + jj);
+          sn[j] = __ldg(p.rope_sin + (size_t)pos * half + jj);
+        }
+      }
+      float v[CH];
+      tc::tmem_ld_32x32b_x16(t_lane + c0, v);
+      if (ks > 1) {
+        // fixed split order: sum = p_0 + p_1 + ... (own split from TMEM)
+        float acc[CH];
+#pragma unroll
+        for (int j = 0; j < CH; ++j) acc[j] = 0.f;
+        for (int sp = 0; sp < ks; ++sp) {
+          if (sp == (int)rank) {
+#pragma unroll
+            for (int j = 0; j < CH; ++j) acc[j] += v[j];
+          } else {
+            const float* ps = parts + (size_t)sp * BN * kBM;
+#pragma unroll
+            for (int j = 0; j < CH; ++j) acc[j] += __ldcg(ps + (c0 + j) * kBM + t);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < CH; ++j) v[j] = acc[j];
+      }
       tc::named_bar(1, kEpiThreads);  // previous chunk's readers of xbuf/obuf are done
       if (section < 2) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) xbuf[t * kXStride + j] = v[j];
+        for (int j = 0; j < CH; ++j) xbuf[t * kXStride + j] = v[j];
         tc::named_bar(1, kEpiThreads);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int pos = col_pos[c0 + j];
-          if (pos < 0) continue;
-          const float cs = __ldg(p.rope_cos + (size_t)pos * half + jj);
-          const float sn = __ldg(p.rope_sin + (size_t)pos * half + jj);
+        for (int j = 0; j < CH; ++j) {
           const float other = xbuf[partner * kXStride + j];
-          v[j] = low ? (v[j] * cs - other * sn) : (other * sn + v[j] * cs);
+          v[j] = low ? (v[j] * cs[j] - other * sn[j]) : (other * sn[j] + v[j] * cs[j]);
         }
         tc::named_bar(1, kEpiThreads);  // exchange reads done before obuf overwrites xbuf
       }
 #pragma unroll
-      for (int j = 0; j < 32; ++j) obuf[j * kBM + t] = __float2bfloat16_rn(v[j]);
+      for (int j = 0; j < CH; ++j) obuf[j * kBM + t] = __float2bfloat16_rn(v[j]);
       tc::named_bar(1, kEpiThreads);
-      // 32 rows x 256 bytes: 16-byte chunks, consecutive threads on consecutive chunks
+      // CH rows x 256 bytes: 16-byte chunks, consecutive threads on consecutive chunks
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < CH * 16 / kEpiThreads; ++u) {
         const int id = t + kEpiThreads * u;
         const int j = id >> 4, part = id & 15;
         const long long dst = col_dst[c0 + j];
@@ -282,6 +320,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
 
 template <int BN>
 cudaError_t launch(fdl_ctx* ctx, const TcParams& p0, const void* X, const void* W) {
+  static_assert(Cfg<BN>::SMEM_BYTES <= 227 * 1024, "shared memory budget");
   using Cf = Cfg<BN>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -296,27 +335,31 @@ cudaError_t launch(fdl_ctx* ctx, const TcParams& p0, const void* X, const void* 
   TcParams p = p0;
   const int tiles_r = (p.R + BN - 1) / BN, tiles_f = 3 * c.d_model / kBM;
   const int tiles = tiles_r * tiles_f;
-  const int per_sm = Cf::SMEM_BYTES * 2 <= 227 * 1024 ? 2 : 1;
+  const int per_sm = qkv_ctas_per_sm(BN);
   int ks = 1;
   if (tiles < ctx->num_sms * per_sm) ks = (ctx->num_sms * per_sm) / tiles;
-  ks = max(1, min(ks, min(Cf::MAX_SPLIT, min(p.nkb, 8))));
+  ks = max(1, min(ks, min(p.nkb, 8)));
+  if ((size_t)tiles * ks * BN * kBM > ctx->qkv_partial_floats || tiles > ctx->qkv_tickets) ks = 1;
   p.ksplit = ks;
+  p.partials = ctx->qkv_partials;
+  p.tickets = ctx->qkv_ticket_buf;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ks, tiles_r, tiles_f);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = Cf::SMEM_BYTES;
   cfg.stream = ctx->stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = ks;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = ks > 1 ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, qkv_tc_kernel<BN>, mw, mx, p);
 }
 
 }  // namespace
+
+int qkv_ctas_per_sm(int bn) { return bn == 64 ? 2 : 1; }
+
+size_t fdl_qkv_partial_floats(int num_sms) {
+  // split-K is used only while tiles * ks <= resident CTAs
+  size_t a = (size_t)2 * num_sms * 64 * kBM, b = (size_t)num_sms * 256 * kBM;
+  return a > b ? a : b;
+}
 
 cudaError_t fdl_launch_qkv_tc(fdl_ctx* ctx, const void* X, const void* W, int R, const int* row_seq,
                               const int* row_rope_pos, const int* row_cache_pos, const int* block_table,
