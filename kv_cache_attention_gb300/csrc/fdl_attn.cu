@@ -280,6 +280,12 @@ __global__ void __launch_bounds__(kWarps * 32) attn_simt_kernel(AttnParams p) {
 
 }  // namespace
 
+bool fdl_attn_tc_supported(const fdl_config& c);
+cudaError_t fdl_launch_attn_tc(fdl_ctx* ctx, const void* q, const void* k_cache, const void* v_cache,
+                               const int* block_table, int bt_stride, const int* kv_len, int B, int R,
+                               const int* row_kind, const int* search_pos, int search_ld, const int* n_search,
+                               void* o_out, float* lse_out, float* track, int track_ld, int cap);
+
 cudaError_t fdl_launch_attn(fdl_ctx* ctx, const void* q, const void* k_cache, const void* v_cache,
                             const int* block_table, int bt_stride, const int* cu_seqlens_q,
                             const int* kv_len, int B, int R, const int* row_kind,
@@ -299,6 +305,9 @@ cudaError_t fdl_launch_attn(fdl_ctx* ctx, const void* q, const void* k_cache, co
                         cudaMemcpyDeviceToDevice, ctx->stream);
     if (e != cudaSuccess) return e;
   }
+  if (ctx->attn_tile_m == FDL_TILE_M_TC)
+    return fdl_launch_attn_tc(ctx, q, k_cache, v_cache, block_table, bt_stride, kv_len, B, R, row_kind,
+                              search_pos, search_ld, n_search, o_out, lse_out, track, track_ld, cap);
   AttnParams p;
   p.q = q;
   p.k_cache = k_cache;

@@ -1,0 +1,686 @@
+// Block-table scheduled attention on the 5th-generation tensor cores, with the
+// Flash-Verify two-view mask and the Eq. (2) attention-mass tracker fused in.
+//
+// Paper digest "Flash-dLLM: IO-Aware KV Caching and Parallel Decoding ...":
+//   "Background"  exact softmax(QK^T/sqrt(d))V computed tile by tile, the
+//                 score matrix never written to HBM;
+//   "Core method" block-table scheduling of ragged per-sequence query blocks
+//                 against their cached K/V; verify rows see the shared tracked
+//                 context but not each other's view of the same token;
+//   "Method steps in detail", step 4, Eq. (2): masked-window rows' attention
+//                 probabilities, averaged over heads and rows, summed over
+//                 layers.
+//
+// One CTA = (work item of <= 128 query rows of one sequence, head, KV split).
+// The KV splits of an item form a thread-block cluster of C CTAs (C = 1 when
+// items x heads already fill the GPU). Two passes over the CTA's key tiles:
+//   pass A  S = Q K^T (tcgen05, fp32 in TMEM) -> running row max and sum;
+//           the C partial (max, sum) pairs meet through distributed shared
+//           memory and every CTA forms the exact log-sum-exp of each row;
+//   pass B  S again -> P = exp(S - lse) (final probabilities, no rescaling)
+//           -> bf16 P staged in shared memory -> O += P V (tcgen05); the
+//           tracker column sums of the masked-window rows come from the same
+//           P. K is read twice (the second time mostly from L2); V once.
+// The C partial O tiles are summed through distributed shared memory in rank
+// order, so results do not depend on timing.
+//
+// Warp roles (192 threads): warp 0 TMA producer (Q once, then a 3-stage K/V
+// ring), warp 1 TMEM owner and MMA issuer (one lane), warps 2-5 softmax and
+// epilogue, one query row per thread (TMEM lane quadrant = warp % 4).
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include "fdl_internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace {
+
+constexpr int kBM = 128;    // query rows per item
+constexpr int kBN = 64;     // keys per tile
+constexpr int kHD = 128;    // head dim handled here
+constexpr int kThreads = 192;
+constexpr int kStages = 3;
+constexpr int kMaxC = 8;
+
+constexpr int Q_BYTES = kBM * kHD * 2;          // two 64-column halves of 16 KB
+constexpr int KT_BYTES = kBN * kHD * 2;         // K tile: two halves of 8 KB
+constexpr int VT_BYTES = kBN * kHD * 2;         // V tile: two halves of 8 KB
+constexpr int STAGE_BYTES = KT_BYTES + VT_BYTES;
+constexpr int P_BYTES = kBM * kBN * 2;          // bf16 P tile, 128 B rows
+constexpr int ML_BYTES = kMaxC * kBM * 2 * 4;   // (max, sum) from every split
+
+constexpr int OFF_Q = 0;
+constexpr int OFF_RING = OFF_Q + Q_BYTES;
+constexpr int OFF_P = OFF_RING + kStages * STAGE_BYTES;
+constexpr int OFF_ML = OFF_P + P_BYTES;
+constexpr int OFF_MISC = OFF_ML + ML_BYTES;
+constexpr int MISC_BYTES = 4096;
+constexpr int SMEM_BYTES = 1024 + OFF_MISC + MISC_BYTES;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+static_assert(kStages * STAGE_BYTES >= kBM * kHD * 4, "ring must hold an fp32 O tile for the cluster sum");
+
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct TcAttnParams {
+  const int* wl;            // count, then (b, q_start, q_len, n_keys)
+  const int* kv_len;
+  const int* row_kind;
+  const int* search_pos;
+  int search_ld;
+  const int* block_table;
+  int bt_stride, page_size, n_pages, n_slots;
+  const int* n_masked;
+  __nv_bfloat16* o;
+  float* lse;
+  float* track;
+  int track_ld;
+  int H, d, R;
+  int C;                    // splits per item (cluster size)
+  float scale_log2;         // log2(e) / sqrt(head_dim)
+  int bitmap_words;         // search-position bitmap size
+  unsigned* err;
+};
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  long long t0 = clock64();
+  for (;;) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(tc::smem_addr(bar)), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if (*abort) return false;
+    if (clock64() - t0 > tc::kWaitBudgetCycles) {
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void mbar_arrive_remote(uint64_t* bar, uint32_t rank) {
+  const uint32_t a = tc::map_cluster(tc::smem_addr(bar), rank);
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(a) : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_v2(uint32_t caddr, float a, float b) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(caddr), "f"(a), "f"(b) : "memory");
+}
+
+__device__ __forceinline__ float4 ld_cluster_v4(uint32_t caddr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(caddr)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Instruction descriptor for O += P V: bf16 operands, fp32 D, A (P) K-major,
+// B (V, stored keys x head_dim) MN-major.
+__host__ __device__ constexpr uint32_t idesc_pv(int M, int N) {
+  return tc::idesc_bf16_f32(M, N) | (1u << 16);
+}
+
+// MN-major operand in the 128-byte swizzle layout: 64-element (128 B) rows
+// along MN, one row per K index; 8-row groups 1024 B apart (stride byte
+// offset); the next 64-wide MN block lbo bytes further (leading byte offset).
+__device__ __forceinline__ uint64_t desc_mnmajor_sw128(uint32_t saddr, uint32_t lbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)(1024u >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Visibility of key position c to a row of `kind` in a sequence with kvl
+// base keys and m search tokens (is_search: c is a search position).
+__device__ __forceinline__ bool visible(int kind, int c, int kvl, int m, bool is_search) {
+  if (kind < 0) return false;
+  if (kind < 2) return c < kvl;
+  if (c < kvl) return !is_search;
+  const int v = c - kvl;
+  if (v >= 2 * m) return false;
+  const int k = (kind - 2) >> 1;
+  const bool mask_view = (kind - 2) & 1;
+  if (v < m) return mask_view ? (v < k) : (v <= k);
+  const int j = v - m;
+  return mask_view ? (j >= k) : (j > k);
+}
+
+// Reduce-scatter of 64 per-lane values over the warp: afterwards lane l holds
+// the warp sums of columns 2l (v[0]) and 2l+1 (v[1]).
+__device__ __forceinline__ void warp_colsum64(float (&v)[64], int lane) {
+#pragma unroll
+  for (int step = 0; step < 5; ++step) {
+    const int off = 16 >> step;
+    const int half = 32 >> step;
+    const bool hi = lane & off;
+#pragma unroll
+    for (int k = 0; k < half; ++k) {
+      const float send = hi ? v[k] : v[k + half];
+      const float keep = hi ? v[k + half] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+}
+
+// 64-bit mask of the search positions in the tile starting at c0.
+__device__ __forceinline__ uint64_t tile_search_bits(const uint32_t* bm, int words, int c0, int kvl) {
+  if (c0 >= kvl) return 0ull;
+  const int w = c0 >> 5;
+  uint64_t lo = w < words ? (uint64_t)bm[w] : 0ull;
+  uint64_t hi = w + 1 < words ? (uint64_t)bm[w + 1] : 0ull;
+  return lo | (hi << 32);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const TcAttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sq = smem + OFF_Q;
+  uint8_t* ring = smem + OFF_RING;
+  uint8_t* sp = smem + OFF_P;
+  float* ml = reinterpret_cast<float*>(smem + OFF_ML);  // [C][128][2]
+  uint8_t* misc = smem + OFF_MISC;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(misc);
+  uint64_t* q_full = bars + 0;
+  uint64_t* kv_full = bars + 1;                 // [kStages]
+  uint64_t* kv_empty = bars + 1 + kStages;      // [kStages]
+  uint64_t* s_full = bars + 1 + 2 * kStages;    // [2]
+  uint64_t* s_free = bars + 3 + 2 * kStages;    // [2]
+  uint64_t* p_full = bars + 5 + 2 * kStages;
+  uint64_t* pv_done = bars + 6 + 2 * kStages;
+  uint64_t* ml_ready = bars + 7 + 2 * kStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8 + 2 * kStages);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* kinds = reinterpret_cast<int*>(misc + 256);              // [128]
+  float* colacc = reinterpret_cast<float*>(misc + 768);         // [64]
+  uint32_t* bitmap = reinterpret_cast<uint32_t*>(misc + 1024);  // [bitmap_words] (<= 768)
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int C = p.C;
+  const uint32_t rank = C > 1 ? tc::cluster_ctarank() : 0u;
+  const int item = blockIdx.x / C;
+  const int h = blockIdx.y;
+  if (item >= p.wl[0]) return;  // uniform over the cluster
+  const int* it = p.wl + 1 + 4 * item;
+  const int b = it[0], q0 = it[1], qlen = it[2], nkeys = it[3];
+  const int kvl = min(p.kv_len[b], nkeys);
+  const int m_search = p.search_pos ? (nkeys - kvl) / 2 : 0;
+  const int n_tiles = (nkeys + kBN - 1) / kBN;
+  const int t0 = (int)(rank * n_tiles / C), t1 = (int)((rank + 1) * n_tiles / C);
+  const int n_my = t1 - t0;
+
+  // ---------------------------------------------------------------- setup
+  if (threadIdx.x == 0) {
+    tc::mbar_init(q_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(&kv_full[s], 1);
+      tc::mbar_init(&kv_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(&s_full[s], 1);
+      tc::mbar_init(&s_free[s], 4);
+    }
+    tc::mbar_init(p_full, 4);
+    tc::mbar_init(pv_done, 1);
+    tc::mbar_init(ml_ready, 128 * C);
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_slot, 256);
+    tc::tmem_relinquish();
+  }
+  for (int r = threadIdx.x; r < kBM; r += kThreads) {
+    int k = -1;
+    if (r < qlen) {
+      k = p.row_kind[q0 + r];
+      if (k >= 2 && ((k - 2) >> 1) >= m_search) {
+        fdl::raise_error(p.err, FDL_DEVERR_SHAPE);
+        k = -1;
+      }
+    }
+    kinds[r] = k;
+  }
+  for (int w = threadIdx.x; w < p.bitmap_words; w += kThreads) bitmap[w] = 0u;
+  if (threadIdx.x < 64) colacc[threadIdx.x] = 0.f;
+  __syncthreads();
+  for (int j = threadIdx.x; j < m_search; j += kThreads) {
+    const int s = p.search_pos[(size_t)b * p.search_ld + j];
+    if (s >= 0 && s < kvl && (s >> 5) < p.bitmap_words) atomicOr(&bitmap[s >> 5], 1u << (s & 31));
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (C > 1) tc::cluster_sync();  // peers' barriers and buffers exist before any remote access
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tm_o = tmem;            // columns [0, 128)
+  const uint32_t tm_s = tmem + 128;      // two 64-column S buffers
+  const bool do_track = p.track != nullptr && p.n_masked[b] > 0;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && n_my > 0) {
+      tc::prefetch_tensormap(&tm_q);
+      tc::prefetch_tensormap(&tm_k);
+      tc::prefetch_tensormap(&tm_v);
+      tc::mbar_arrive_expect_tx(q_full, Q_BYTES);
+      tc::tma_load_2d(sq, &tm_q, h * kHD, q0, q_full);
+      tc::tma_load_2d(sq + Q_BYTES / 2, &tm_q, h * kHD + 64, q0, q_full);
+      int lc = 0;
+      for (int pass = 0; pass < 2; ++pass) {
+        for (int j = t0; j < t1; ++j, ++lc) {
+          const int s = lc % kStages;
+          const uint32_t ph = (uint32_t)(lc / kStages) & 1u;
+          if (!tc::mbar_wait(&kv_empty[s], ph ^ 1u, abort_flag)) break;
+          // slot of the tile's first key; an unmapped page points past the
+          // cache so the TMA zero-fills the tile (and the error word says so)
+          const int c0 = j * kBN;
+          const int pi = c0 / p.page_size;
+          const int page = pi < p.bt_stride ? p.block_table[(size_t)b * p.bt_stride + pi] : -1;
+          int slot = p.n_slots;
+          if (page >= 0 && page < p.n_pages) slot = page * p.page_size + c0 % p.page_size;
+          else if (pass == 0) fdl::raise_error(p.err, FDL_DEVERR_INDEX);
+          uint8_t* st = ring + s * STAGE_BYTES;
+          tc::mbar_arrive_expect_tx(&kv_full[s], pass == 0 ? KT_BYTES : STAGE_BYTES);
+          tc::tma_load_2d(st, &tm_k, h * kHD, slot, &kv_full[s]);
+          tc::tma_load_2d(st + KT_BYTES / 2, &tm_k, h * kHD + 64, slot, &kv_full[s]);
+          if (pass == 1) {
+            tc::tma_load_2d(st + KT_BYTES, &tm_v, h * kHD, slot, &kv_full[s]);
+            tc::tma_load_2d(st + KT_BYTES + VT_BYTES / 2, &tm_v, h * kHD + 64, slot, &kv_full[s]);
+          }
+        }
+        if (*abort_flag) break;
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n_my > 0) {
+      constexpr uint32_t id_s = tc::idesc_bf16_f32(kBM, kBN);
+      constexpr uint32_t id_pv = idesc_pv(kBM, kHD);
+      const uint32_t aq = tc::smem_addr(sq);
+      const uint32_t ap = tc::smem_addr(sp);
+      bool ok = tc::mbar_wait(q_full, 0, abort_flag);
+      int sc = 0;
+      // S #sc = Q K(load_idx)^T into TMEM buffer sc & 1
+      auto issue_s = [&](int load_idx) -> bool {
+        const int s = load_idx % kStages;
+        if (!tc::mbar_wait(&kv_full[s], (uint32_t)(load_idx / kStages) & 1u, abort_flag)) return false;
+        const int sb = sc & 1;
+        if (sc >= 2 && !tc::mbar_wait(&s_free[sb], (uint32_t)((sc - 2) >> 1) & 1u, abort_flag)) return false;
+        tc::fence_after_sync();
+        const uint32_t ak = tc::smem_addr(ring + s * STAGE_BYTES);
+#pragma unroll
+        for (int k = 0; k < kHD / 16; ++k) {
+          const uint32_t half = (uint32_t)(k >> 2), kk = (uint32_t)(k & 3) * 32u;
+          tc::mma_bf16_ss(tm_s + 64 * sb, tc::desc_kmajor_sw128(aq + half * (Q_BYTES / 2) + kk),
+                          tc::desc_kmajor_sw128(ak + half * (KT_BYTES / 2) + kk), id_s, k > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(&s_full[sb]);
+        ++sc;
+        return true;
+      };
+      // pass A: scores only; each stage is released once its S MMAs finish
+      for (int i = 0; ok && i < n_my; ++i) {
+        ok = issue_s(i);
+        if (ok) tc::mma_commit(&kv_empty[i % kStages]);
+      }
+      // pass B: S(i+1) is issued before O += P(i) V(i) so the softmax overlaps
+      const int lb = n_my;
+      if (ok) ok = issue_s(lb);
+      for (int i = 0; ok && i < n_my; ++i) {
+        if (i + 1 < n_my) ok = issue_s(lb + i + 1);
+        if (!ok) break;
+        if (!tc::mbar_wait(p_full, (uint32_t)i & 1u, abort_flag)) break;
+        tc::fence_after_sync();
+        const int s = (lb + i) % kStages;
+        const uint32_t av = tc::smem_addr(ring + s * STAGE_BYTES + KT_BYTES);
+#pragma unroll
+        for (int k = 0; k < kBN / 16; ++k)
+          tc::mma_bf16_ss(tm_o, tc::desc_kmajor_sw128(ap + k * 32), desc_mnmajor_sw128(av + k * 2048, VT_BYTES / 2),
+                          id_pv, (i > 0 || k > 0) ? 1u : 0u);
+        tc::mma_commit(pv_done);
+        tc::mma_commit(&kv_empty[s]);
+      }
+    }
+    __syncwarp();
+  }
+
+  // ------------------------------------------------------------ softmax warps
+  const int qd = warp & 3;
+  const int row = qd * 32 + lane;
+  const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
+  float lse2 = -INFINITY;  // log2-domain log-sum-exp of this row over all splits
+  if (warp >= 2) {
+    const int kind = kinds[row];
+    float mrow = -INFINITY, lrow = 0.f;
+    int sc = 0;
+    // ---- pass A
+    for (int i = 0; i < n_my; ++i, ++sc) {
+      const int sb = sc & 1;
+      // tcgen05.ld is warp-collective: the whole warp proceeds or none of it
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&s_full[sb], (uint32_t)(sc >> 1) & 1u, abort_flag))) break;
+      tc::fence_after_sync();
+      float s[64];
+      {
+        float a[32];
+        tc::tmem_ld_32x32b_x32(tm_s + 64 * sb + lane_off, a);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) s[k] = a[k];
+        tc::tmem_ld_32x32b_x32(tm_s + 64 * sb + 32 + lane_off, a);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) s[32 + k] = a[k];
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&s_free[sb]);
+      const int c0 = (t0 + i) * kBN;
+      const uint64_t sbits = tile_search_bits(bitmap, p.bitmap_words, c0, kvl);
+      float tmax = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 64; ++k) {
+        const bool v = visible(kind, c0 + k, kvl, m_search, (sbits >> k) & 1ull);
+        s[k] = v ? s[k] * p.scale_log2 : -INFINITY;
+        tmax = fmaxf(tmax, s[k]);
+      }
+      if (tmax == -INFINITY) continue;
+      const float mnew = fmaxf(mrow, tmax);
+      float acc = 0.f;
+#pragma unroll
+      for (int k = 0; k < 64; ++k) acc += exp2f(s[k] - mnew);
+      lrow = (mrow == -INFINITY ? 0.f : lrow * exp2f(mrow - mnew)) + acc;
+      mrow = mnew;
+    }
+    // ---- combine (max, sum) over the cluster
+    if (C > 1) {
+      // push this row's (max, sum) into every split, then release-arrive there
+      const uint32_t mine = tc::smem_addr(ml + ((size_t)rank * kBM + row) * 2);
+      for (int r = 0; r < C; ++r) st_cluster_v2(tc::map_cluster(mine, (uint32_t)r), mrow, lrow);
+      for (int r = 0; r < C; ++r) mbar_arrive_remote(ml_ready, (uint32_t)r);
+      mbar_wait_cluster(ml_ready, 0, abort_flag);
+      float mm = -INFINITY;
+      for (int r = 0; r < C; ++r) mm = fmaxf(mm, ml[((size_t)r * kBM + row) * 2]);
+      float ll = 0.f;
+      if (mm != -INFINITY)
+        for (int r = 0; r < C; ++r) {
+          const float mr = ml[((size_t)r * kBM + row) * 2], lr = ml[((size_t)r * kBM + row) * 2 + 1];
+          if (mr != -INFINITY) ll += lr * exp2f(mr - mm);
+        }
+      lse2 = ll > 0.f ? mm + log2f(ll) : -INFINITY;
+    } else {
+      lse2 = lrow > 0.f ? mrow + log2f(lrow) : -INFINITY;
+    }
+    if (p.lse && rank == 0 && row < qlen) p.lse[(size_t)(q0 + row) * p.H + h] = lse2 * kLn2;
+
+    // ---- pass B
+    const float wscale = do_track ? 1.f / ((float)p.H * (float)p.n_masked[b]) : 0.f;
+    const bool track_row = do_track && kind == FDL_KIND_WINDOW;
+    const int t_local = threadIdx.x - 64;  // 0..127 over the softmax warps
+    for (int i = 0; i < n_my; ++i, ++sc) {
+      // a wait that gives up (abort) skips the work but never the barriers
+      const int sb = sc & 1;
+      bool ok = __all_sync(0xffffffffu, tc::mbar_wait(&s_full[sb], (uint32_t)(sc >> 1) & 1u, abort_flag));
+      float pr[64];
+      const int c0 = (t0 + i) * kBN;
+      if (ok) {
+        tc::fence_after_sync();
+        float a[32];
+        tc::tmem_ld_32x32b_x32(tm_s + 64 * sb + lane_off, a);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) pr[k] = a[k];
+        tc::tmem_ld_32x32b_x32(tm_s + 64 * sb + 32 + lane_off, a);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) pr[32 + k] = a[k];
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&s_free[sb]);
+        const uint64_t sbits = tile_search_bits(bitmap, p.bitmap_words, c0, kvl);
+#pragma unroll
+        for (int k = 0; k < 64; ++k) {
+          const bool v = lse2 != -INFINITY && visible(kind, c0 + k, kvl, m_search, (sbits >> k) & 1ull);
+          pr[k] = v ? exp2f(pr[k] * p.scale_log2 - lse2) : 0.f;
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 64; ++k) pr[k] = 0.f;
+      }
+      // the previous P V must have consumed the P buffer
+      ok = ok && (i == 0 || tc::mbar_wait(pv_done, (uint32_t)(i - 1) & 1u, abort_flag));
+      if (ok) {
+        // P in the 128-byte swizzled K-major layout: row r, 16-byte chunk q at q ^ (r & 7)
+        uint8_t* prow = sp + row * 128;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(pr[q * 8 + 2 * e], pr[q * 8 + 2 * e + 1]);
+            w[e] = *reinterpret_cast<uint32_t*>(&h2);
+          }
+          *reinterpret_cast<uint4*>(prow + ((q ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        // keys past the sequence end may hold anything: zero their V rows so
+        // that 0 * V stays 0 in the P V product
+        if (c0 + kBN > nkeys) {
+          const int s = (n_my + i) % kStages;
+          uint8_t* vt = ring + s * STAGE_BYTES + KT_BYTES;
+          const int first = max(0, nkeys - c0);
+          for (int e = lane; e < (kBN - first) * 16; e += 32) {
+            const int r = first + e / 16, part = e % 16;
+            if ((r & 3) != qd) continue;  // the four warps split the rows
+            *reinterpret_cast<uint4*>(vt + (part >> 3) * (VT_BYTES / 2) + r * 128 + (part & 7) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      if (ok && lane == 0) tc::mbar_arrive(p_full);
+      if (do_track) {
+        if (!track_row) {
+#pragma unroll
+          for (int k = 0; k < 64; ++k) pr[k] = 0.f;
+        }
+        warp_colsum64(pr, lane);
+        atomicAdd(&colacc[2 * lane], pr[0]);
+        atomicAdd(&colacc[2 * lane + 1], pr[1]);
+        tc::named_bar(1, 128);
+        if (t_local < 64) {
+          const int c = c0 + t_local;
+          const float v = colacc[t_local];
+          colacc[t_local] = 0.f;
+          if (c < kvl && v != 0.f) atomicAdd(p.track + (size_t)b * p.track_ld + c, v * wscale);
+        }
+        tc::named_bar(1, 128);
+      }
+    }
+    if (n_my > 0) tc::mbar_wait(pv_done, (uint32_t)(n_my - 1) & 1u, abort_flag);
+    tc::fence_after_sync();
+  }
+
+  // ------------------------------------------------------------ output
+  if (C == 1) {
+    // TMEM loads are warp-collective: issued by whole warps (n_my is uniform),
+    // per-row conditions only select values and guard the stores
+    if (warp >= 2) {
+      const bool store = row < qlen && !*abort_flag;
+      __nv_bfloat16* orow = p.o + (size_t)(q0 + row) * p.d + h * kHD;
+#pragma unroll
+      for (int c0 = 0; c0 < kHD; c0 += 32) {
+        float a[32];
+        if (n_my > 0) tc::tmem_ld_32x32b_x32(tm_o + c0 + lane_off, a);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) a[e] = (n_my > 0 && lse2 != -INFINITY) ? a[e] : 0.f;
+        if (!store) continue;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(a[q * 8 + 2 * e], a[q * 8 + 2 * e + 1]);
+            w[e] = *reinterpret_cast<uint32_t*>(&h2);
+          }
+          *reinterpret_cast<uint4*>(orow + c0 + q * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+    }
+  } else {
+    // every split stages its fp32 partial O (already normalised) in its ring;
+    // split r then sums rows [r*128/C, (r+1)*128/C) over all splits in rank order
+    float* ostage = reinterpret_cast<float*>(ring);  // [128][128]
+    if (warp >= 2) {
+#pragma unroll
+      for (int c0 = 0; c0 < kHD; c0 += 32) {
+        float a[32];
+        if (n_my > 0) tc::tmem_ld_32x32b_x32(tm_o + c0 + lane_off, a);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) a[e] = (n_my > 0 && lse2 != -INFINITY) ? a[e] : 0.f;
+        // rotate the 16-byte chunks by row to spread shared-memory banks
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int e0 = 4 * ((q + row) & 7);
+          *reinterpret_cast<float4*>(ostage + row * kHD + c0 + e0) = make_float4(a[e0], a[e0 + 1], a[e0 + 2], a[e0 + 3]);
+        }
+      }
+    }
+    tc::cluster_sync();
+    if (warp >= 2) {
+      const int rows_per = kBM / C;
+      const int t_local = threadIdx.x - 64;
+      const uint32_t base = tc::smem_addr(ostage);
+      for (int e = t_local; e < rows_per * (kHD / 4); e += 128) {
+        const int r = (int)rank * rows_per + e / (kHD / 4);
+        const int col = (e % (kHD / 4)) * 4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int src = 0; src < C; ++src) {
+          const float4 v = ld_cluster_v4(tc::map_cluster(base + (uint32_t)(r * kHD + col) * 4u, (uint32_t)src));
+          acc.x += v.x;
+          acc.y += v.y;
+          acc.z += v.z;
+          acc.w += v.w;
+        }
+        if (r < qlen && !*abort_flag) {
+          __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+          uint2 w = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+          *reinterpret_cast<uint2*>(p.o + (size_t)(q0 + r) * p.d + h * kHD + col) = w;
+        }
+      }
+    }
+    tc::cluster_sync();  // peers finished reading this CTA's staged O
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) fdl::raise_error(p.err, FDL_DEVERR_TIMEOUT);
+  if (warp == 1) tc::tmem_dealloc(tmem, 256);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+bool map2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool fdl_attn_tc_supported(const fdl_config& c) {
+  // head_dim 128, bf16, and every 64-key tile inside one page: pages are a
+  // multiple of 64 slots, or one page holds a whole sequence plus its views
+  return c.dtype == FDL_BF16 && c.head_dim == kHD &&
+         (c.page_size % kBN == 0 || c.page_size >= c.max_seq + c.max_views) &&
+         (c.max_seq + c.max_views + 31) / 32 <= 768;
+}
+
+cudaError_t fdl_launch_attn_tc(fdl_ctx* ctx, const void* q, const void* k_cache, const void* v_cache,
+                               const int* block_table, int bt_stride, const int* kv_len, int B, int R,
+                               const int* row_kind, const int* search_pos, int search_ld, const int* n_search,
+                               void* o_out, float* lse_out, float* track, int track_ld, int cap) {
+  (void)n_search;  // the work list already carries kv_len + 2 * n_search per item
+  const fdl_config& c = ctx->cfg;
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) |
+       reinterpret_cast<uintptr_t>(v_cache) | reinterpret_cast<uintptr_t>(o_out)) & 15)
+    return cudaErrorMisalignedAddress;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int n_slots = c.n_pages * c.page_size;
+  CUtensorMap mq, mk, mv;
+  if (!map2d(&mq, q, R, c.d_model, kBM) || !map2d(&mk, k_cache, n_slots, c.d_model, kBN) ||
+      !map2d(&mv, v_cache, n_slots, c.d_model, kBN))
+    return cudaErrorInvalidValue;
+  TcAttnParams p;
+  p.wl = ctx->worklist;
+  p.kv_len = kv_len;
+  p.row_kind = row_kind;
+  p.search_pos = search_pos;
+  p.search_ld = search_ld;
+  p.block_table = block_table;
+  p.bt_stride = bt_stride;
+  p.page_size = c.page_size;
+  p.n_pages = c.n_pages;
+  p.n_slots = n_slots;
+  p.n_masked = ctx->n_masked;
+  p.o = reinterpret_cast<__nv_bfloat16*>(o_out);
+  p.lse = lse_out;
+  p.track = track;
+  p.track_ld = track_ld;
+  p.H = c.n_heads;
+  p.d = c.d_model;
+  p.R = R;
+  p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)c.head_dim));
+  p.bitmap_words = (c.max_seq + c.max_views + 31) / 32;
+  p.err = ctx->err_word;
+  // splits per item: fill the SMs when items x heads alone cannot
+  const int est_items = (R + kBM - 1) / kBM + B - 1;
+  int C = 1;
+  while (C < kMaxC && est_items * c.n_heads * (2 * C) <= ctx->num_sms) C *= 2;
+  p.C = C;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(cap * C), (unsigned)c.n_heads, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = ctx->stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = C > 1 ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, attn_tc_kernel, mq, mk, mv, p);
+}

@@ -9,6 +9,8 @@
 
 #include "fdl_internal.cuh"
 
+bool fdl_attn_tc_supported(const fdl_config& c);
+
 namespace {
 
 fdl_status fail(fdl_ctx* ctx, fdl_status st, const char* fmt, ...) {
@@ -87,7 +89,7 @@ fdl_status fdl_create(const fdl_config* cfg, void* cuda_stream, fdl_ctx** out) {
       hs[(size_t)p * half + i] = (float)sin(a);
     }
   }
-  ctx->attn_tile_m = FDL_TILE_M_SIMT;
+  ctx->attn_tile_m = fdl_attn_tc_supported(*cfg) ? FDL_TILE_M_TC : FDL_TILE_M_SIMT;
   ctx->worklist_items = (cfg->max_rows + ctx->attn_tile_m - 1) / ctx->attn_tile_m + cfg->max_batch;
   cudaError_t e = cudaSuccess;
   e = e ? e : cudaMalloc(&ctx->rope_cos, n_tab * sizeof(float));
