@@ -224,6 +224,41 @@ typedef struct {
 
 fdl_status fdl_unmask_verify(fdl_ctx* ctx, const fdl_unmask_args* args);
 
+/* ------------------------------------------------------------------------
+ * Scheduled attention without any device allocation. The paper has no
+ * counterpart: this is a deployment variant of fdl_sched_attn.
+ *
+ * For callers that cannot call cudaMalloc: code running under an external
+ * memory manager that owns the whole device heap, or on a latency-critical
+ * path where an allocation (which may synchronise the device) is not
+ * acceptable. It needs no context (fdl_create allocates one) and allocates
+ * nothing on any call. Its scratch (the device-built work list and the
+ * per-sequence masked-row counts) lives in a static device array of about
+ * 70 KB that every GPU loading the library holds until the process exits.
+ *
+ * Arguments and results are those of fdl_sched_attn (same kernels), with the
+ * limits taken from *cfg (max_batch and max_rows are ignored; the call's B
+ * and R apply) and the work list not exported. Limits of the static scratch:
+ * B <= 1024 and ceil(R / fdl_tile_m) + B <= 4096 work items, where the tile
+ * is 128 rows for bf16 contexts with head_dim 128 and 16 rows otherwise;
+ * larger calls return FDL_ERR_INVALID_ARG (reason on stderr). Device-side
+ * index errors are OR-ed into *device_error (a caller-owned device word, may
+ * be NULL; the caller zeroes and reads it) with the bits of the device error
+ * word: 1 index, 2 timeout, 4 shape.
+ *
+ * The first call on a device looks up the scratch array's device address
+ * (cudaGetSymbolAddress) and caches it; make that first call before any
+ * stream capture. Every call on a device shares the array and rewrites all
+ * of it that it reads; calls that overlap on the GPU (several streams or host
+ * threads) race on it and must be serialised by the caller.
+ * ---------------------------------------------------------------------- */
+fdl_status fdl_sched_attn_noalloc(const fdl_config* cfg, void* cuda_stream, const void* q,
+                                  const void* k_cache, const void* v_cache, const int* block_table,
+                                  int bt_stride, const int* cu_seqlens_q, const int* kv_len, int B, int R,
+                                  const int* row_kind, const int* search_pos, int search_ld,
+                                  const int* n_search, void* o_out, float* lse_out, float* track_scores,
+                                  int track_ld, unsigned* device_error);
+
 #ifdef __cplusplus
 }
 #endif

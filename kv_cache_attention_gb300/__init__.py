@@ -42,7 +42,7 @@ def FDL_KIND_MASK_VIEW(j: int) -> int:
 EXPORTS = (
     "fdl_create", "fdl_destroy", "fdl_set_stream", "fdl_last_error", "fdl_sync_status",
     "fdl_tile_m", "fdl_worklist_capacity", "fdl_qkv_rope_cache_write", "fdl_sched_attn",
-    "fdl_track_topk", "fdl_unmask_verify",
+    "fdl_track_topk", "fdl_unmask_verify", "fdl_sched_attn_noalloc",
 )
 
 
@@ -109,6 +109,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.fdl_track_topk.restype = i
     L.fdl_unmask_verify.argtypes = [p, ctypes.POINTER(fdl_unmask_args)]
     L.fdl_unmask_verify.restype = i
+    L.fdl_sched_attn_noalloc.argtypes = [ctypes.POINTER(fdl_config), p, p, p, p, p, i, p, p, i, i, p, p, i, p, p,
+                                         p, p, i, p]
+    L.fdl_sched_attn_noalloc.restype = i
     _lib = L
     return L
 
@@ -249,3 +252,23 @@ def fdl_track_topk(ctx: Context, *a, **k) -> None:
 
 def fdl_unmask_verify(ctx: Context, *a, **k) -> None:
     ctx.unmask_verify(*a, **k)
+
+
+def fdl_sched_attn_noalloc(cfg: fdl_config, q, k_cache, v_cache, block_table, cu_seqlens_q, kv_len, row_kind,
+                           o_out, lse_out=None, track_scores=None, search_pos=None, n_search=None,
+                           device_error=None, stream=None) -> None:
+    """Scheduled attention with no device allocation (no context needed).
+
+    For callers that cannot allocate device memory; see include/fdl.h for
+    the static-scratch limits and the serialisation rule.
+    """
+    B = int(kv_len.shape[0])
+    R = int(q.shape[0])
+    search_ld = int(search_pos.shape[-1]) if search_pos is not None else 0
+    track_ld = int(track_scores.shape[-1]) if track_scores is not None else 0
+    st = load_library().fdl_sched_attn_noalloc(
+        ctypes.byref(cfg), _stream_handle(stream), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+        int(block_table.shape[-1]), _ptr(cu_seqlens_q), _ptr(kv_len), B, R, _ptr(row_kind), _ptr(search_pos),
+        search_ld, _ptr(n_search), _ptr(o_out), _ptr(lse_out), _ptr(track_scores), track_ld, _ptr(device_error))
+    if st != FDL_OK:
+        raise FdlError(st, "fdl_sched_attn_noalloc (reason on stderr)")
