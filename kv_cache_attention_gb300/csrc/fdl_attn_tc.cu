@@ -24,9 +24,10 @@
 // The C partial O tiles are summed through distributed shared memory in rank
 // order, so results do not depend on timing.
 //
-// Warp roles (192 threads): warp 0 TMA producer (Q once, then a 3-stage K/V
-// ring), warp 1 TMEM owner and MMA issuer (one lane), warps 2-5 softmax and
-// epilogue, one query row per thread (TMEM lane quadrant = warp % 4).
+// Warp roles (320 threads): warp 0 TMA producer (Q once, then a 3-stage K/V
+// ring), warp 1 TMEM owner and MMA issuer (one lane), warps 2-9 softmax and
+// epilogue: one query row per thread (TMEM lane quadrant = warp % 4) and half
+// of each key tile's columns per warp.
 #include <cudaTypedefs.h>
 #include <math.h>
 
@@ -38,7 +39,7 @@ namespace {
 constexpr int kBM = 128;    // query rows per item
 constexpr int kBN = 64;     // keys per tile
 constexpr int kHD = 128;    // head dim handled here
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr int kStages = 3;
 constexpr int kMaxC = 8;
 
@@ -54,10 +55,10 @@ constexpr int OFF_RING = OFF_Q + Q_BYTES;
 constexpr int OFF_P = OFF_RING + kStages * STAGE_BYTES;
 constexpr int OFF_ML = OFF_P + P_BYTES;
 constexpr int OFF_MISC = OFF_ML + ML_BYTES;
-constexpr int MISC_BYTES = 4096;
+constexpr int MISC_BYTES = 5120;
 constexpr int SMEM_BYTES = 1024 + OFF_MISC + MISC_BYTES;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-static_assert(kStages * STAGE_BYTES >= kBM * kHD * 4, "ring must hold an fp32 O tile for the cluster sum");
+static_assert(kStages * STAGE_BYTES >= kBM * (kHD + 4) * 4, "ring must hold an fp32 O tile for the cluster sum");
 
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -157,13 +158,36 @@ __device__ __forceinline__ bool visible(int kind, int c, int kvl, int m, bool is
   return mask_view ? (j >= k) : (j > k);
 }
 
-// Reduce-scatter of 64 per-lane values over the warp: afterwards lane l holds
-// the warp sums of columns 2l (v[0]) and 2l+1 (v[1]).
-__device__ __forceinline__ void warp_colsum64(float (&v)[64], int lane) {
+// Hardware base-2 exponential (ex2.approx, relative error ~2^-22); ex2(-inf) = 0.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Visibility of keys cb .. cb+31 (cb a multiple of 32) to a row of `kind`,
+// one bit per key. Plain rows only compare against the sequence length; view
+// rows consult the search-position bitmap and the view-key rule.
+__device__ __forceinline__ uint32_t vis_mask(int kind, int cb, int kvl, int m, const uint32_t* bm, int words) {
+  if (kind < 0) return 0u;
+  if (kind < 2) {
+    const int n = kvl - cb;
+    return n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : (1u << n) - 1u);
+  }
+  const uint32_t srch = (cb < kvl && (cb >> 5) < words) ? bm[cb >> 5] : 0u;
+  uint32_t mask = 0u;
+#pragma unroll 4
+  for (int k = 0; k < 32; ++k) mask |= (visible(kind, cb + k, kvl, m, (srch >> k) & 1u) ? 1u : 0u) << k;
+  return mask;
+}
+
+// Reduce-scatter of 32 per-lane values over the warp: afterwards v[0] of
+// lane l holds the warp's sum of column l.
+__device__ __forceinline__ void warp_colsum32(float (&v)[32], int lane) {
 #pragma unroll
   for (int step = 0; step < 5; ++step) {
     const int off = 16 >> step;
-    const int half = 32 >> step;
+    const int half = 16 >> step;
     const bool hi = lane & off;
 #pragma unroll
     for (int k = 0; k < half; ++k) {
@@ -172,15 +196,6 @@ __device__ __forceinline__ void warp_colsum64(float (&v)[64], int lane) {
       v[k] = keep + __shfl_xor_sync(0xffffffffu, send, off);
     }
   }
-}
-
-// 64-bit mask of the search positions in the tile starting at c0.
-__device__ __forceinline__ uint64_t tile_search_bits(const uint32_t* bm, int words, int c0, int kvl) {
-  if (c0 >= kvl) return 0ull;
-  const int w = c0 >> 5;
-  uint64_t lo = w < words ? (uint64_t)bm[w] : 0ull;
-  uint64_t hi = w + 1 < words ? (uint64_t)bm[w + 1] : 0ull;
-  return lo | (hi << 32);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -207,6 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* kinds = reinterpret_cast<int*>(misc + 256);              // [128]
   float* colacc = reinterpret_cast<float*>(misc + 768);         // [64]
   uint32_t* bitmap = reinterpret_cast<uint32_t*>(misc + 1024);  // [bitmap_words] (<= 768)
+  float* halfml = reinterpret_cast<float*>(misc + 4096);        // [2][128][2]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int C = p.C;
@@ -231,9 +247,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(&s_full[s], 1);
-      tc::mbar_init(&s_free[s], 4);
+      tc::mbar_init(&s_free[s], 8);
     }
-    tc::mbar_init(p_full, 4);
+    tc::mbar_init(p_full, 8);
     tc::mbar_init(pv_done, 1);
     tc::mbar_init(ml_ready, 128 * C);
     *abort_flag = 0;
@@ -360,56 +376,77 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ------------------------------------------------------------ softmax warps
+  // Eight warps: warp w in [2, 10) owns TMEM lane quadrant w % 4 (32 query
+  // rows) and key columns [32 ch, 32 ch + 32) of every 64-key tile, with
+  // ch = (w - 2) / 4, so two warps share each sub-partition's issue slots.
   const int qd = warp & 3;
+  const int ch = (warp - 2) >> 2;
   const int row = qd * 32 + lane;
   const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
+  const int t_local = threadIdx.x - 64;  // 0..255 over the softmax warps
   float lse2 = -INFINITY;  // log2-domain log-sum-exp of this row over all splits
   if (warp >= 2) {
     const int kind = kinds[row];
     float mrow = -INFINITY, lrow = 0.f;
     int sc = 0;
-    // ---- pass A
+    // ---- pass A: running max and sum over this warp's columns
     for (int i = 0; i < n_my; ++i, ++sc) {
       const int sb = sc & 1;
       // tcgen05.ld is warp-collective: the whole warp proceeds or none of it
       if (!__all_sync(0xffffffffu, tc::mbar_wait(&s_full[sb], (uint32_t)(sc >> 1) & 1u, abort_flag))) break;
       tc::fence_after_sync();
-      float s[64];
-      {
-        float a[32];
-        tc::tmem_ld_32x32b_x32(tm_s + 64 * sb + lane_off, a);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) s[k] = a[k];
-        tc::tmem_ld_32x32b_x32(tm_s + 64 * sb + 32 + lane_off, a);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) s[32 + k] = a[k];
-      }
+      float x[32];
+      tc::tmem_ld_32x32b_x32(tm_s + 64 * sb + 32 * ch + lane_off, x);
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&s_free[sb]);
-      const int c0 = (t0 + i) * kBN;
-      const uint64_t sbits = tile_search_bits(bitmap, p.bitmap_words, c0, kvl);
-      float tmax = -INFINITY;
+      const uint32_t vm = vis_mask(kind, (t0 + i) * kBN + 32 * ch, kvl, m_search, bitmap, p.bitmap_words);
 #pragma unroll
-      for (int k = 0; k < 64; ++k) {
-        const bool v = visible(kind, c0 + k, kvl, m_search, (sbits >> k) & 1ull);
-        s[k] = v ? s[k] * p.scale_log2 : -INFINITY;
-        tmax = fmaxf(tmax, s[k]);
-      }
+      for (int k = 0; k < 32; ++k) x[k] = ((vm >> k) & 1u) ? x[k] * p.scale_log2 : -INFINITY;
+      float t16[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) t16[k] = fmaxf(x[k], x[k + 16]);
+#pragma unroll
+      for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+        for (int k = 0; k < w; ++k) t16[k] = fmaxf(t16[k], t16[k + w]);
+      const float tmax = t16[0];
       if (tmax == -INFINITY) continue;
       const float mnew = fmaxf(mrow, tmax);
-      float acc = 0.f;
+      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-      for (int k = 0; k < 64; ++k) acc += exp2f(s[k] - mnew);
-      lrow = (mrow == -INFINITY ? 0.f : lrow * exp2f(mrow - mnew)) + acc;
+      for (int k = 0; k < 32; k += 4) {
+        a0 += ex2(x[k] - mnew);
+        a1 += ex2(x[k + 1] - mnew);
+        a2 += ex2(x[k + 2] - mnew);
+        a3 += ex2(x[k + 3] - mnew);
+      }
+      lrow = (mrow == -INFINITY ? 0.f : lrow * ex2(mrow - mnew)) + ((a0 + a1) + (a2 + a3));
       mrow = mnew;
+    }
+    // ---- the two column halves of each row combine their (max, sum)
+    halfml[(ch * kBM + row) * 2] = mrow;
+    halfml[(ch * kBM + row) * 2 + 1] = lrow;
+    tc::named_bar(2, 256);
+    {
+      const float mo = halfml[((1 - ch) * kBM + row) * 2], lo = halfml[((1 - ch) * kBM + row) * 2 + 1];
+      const float mm = fmaxf(mrow, mo);
+      float ll = 0.f;
+      if (mm != -INFINITY) {
+        if (mrow != -INFINITY) ll += lrow * ex2(mrow - mm);
+        if (mo != -INFINITY) ll += lo * ex2(mo - mm);
+      }
+      mrow = mm;
+      lrow = ll;
     }
     // ---- combine (max, sum) over the cluster
     if (C > 1) {
-      // push this row's (max, sum) into every split, then release-arrive there
-      const uint32_t mine = tc::smem_addr(ml + ((size_t)rank * kBM + row) * 2);
-      for (int r = 0; r < C; ++r) st_cluster_v2(tc::map_cluster(mine, (uint32_t)r), mrow, lrow);
-      for (int r = 0; r < C; ++r) mbar_arrive_remote(ml_ready, (uint32_t)r);
+      if (ch == 0) {
+        // push this row's (max, sum) into every split, then release-arrive there
+        const uint32_t mine = tc::smem_addr(ml + ((size_t)rank * kBM + row) * 2);
+        for (int r = 0; r < C; ++r) st_cluster_v2(tc::map_cluster(mine, (uint32_t)r), mrow, lrow);
+        for (int r = 0; r < C; ++r) mbar_arrive_remote(ml_ready, (uint32_t)r);
+      }
       mbar_wait_cluster(ml_ready, 0, abort_flag);
       float mm = -INFINITY;
       for (int r = 0; r < C; ++r) mm = fmaxf(mm, ml[((size_t)r * kBM + row) * 2]);
@@ -417,57 +454,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (mm != -INFINITY)
         for (int r = 0; r < C; ++r) {
           const float mr = ml[((size_t)r * kBM + row) * 2], lr = ml[((size_t)r * kBM + row) * 2 + 1];
-          if (mr != -INFINITY) ll += lr * exp2f(mr - mm);
+          if (mr != -INFINITY) ll += lr * ex2(mr - mm);
         }
       lse2 = ll > 0.f ? mm + log2f(ll) : -INFINITY;
     } else {
       lse2 = lrow > 0.f ? mrow + log2f(lrow) : -INFINITY;
     }
-    if (p.lse && rank == 0 && row < qlen) p.lse[(size_t)(q0 + row) * p.H + h] = lse2 * kLn2;
+    if (p.lse && rank == 0 && ch == 0 && row < qlen) p.lse[(size_t)(q0 + row) * p.H + h] = lse2 * kLn2;
 
-    // ---- pass B
+    // ---- pass B: final probabilities, P V, tracker column sums
     const float wscale = do_track ? 1.f / ((float)p.H * (float)p.n_masked[b]) : 0.f;
     const bool track_row = do_track && kind == FDL_KIND_WINDOW;
-    const int t_local = threadIdx.x - 64;  // 0..127 over the softmax warps
     for (int i = 0; i < n_my; ++i, ++sc) {
       // a wait that gives up (abort) skips the work but never the barriers
       const int sb = sc & 1;
       bool ok = __all_sync(0xffffffffu, tc::mbar_wait(&s_full[sb], (uint32_t)(sc >> 1) & 1u, abort_flag));
-      float pr[64];
+      float pr[32];
       const int c0 = (t0 + i) * kBN;
       if (ok) {
         tc::fence_after_sync();
-        float a[32];
-        tc::tmem_ld_32x32b_x32(tm_s + 64 * sb + lane_off, a);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) pr[k] = a[k];
-        tc::tmem_ld_32x32b_x32(tm_s + 64 * sb + 32 + lane_off, a);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) pr[32 + k] = a[k];
+        tc::tmem_ld_32x32b_x32(tm_s + 64 * sb + 32 * ch + lane_off, pr);
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&s_free[sb]);
-        const uint64_t sbits = tile_search_bits(bitmap, p.bitmap_words, c0, kvl);
+        const uint32_t vm =
+            lse2 != -INFINITY ? vis_mask(kind, c0 + 32 * ch, kvl, m_search, bitmap, p.bitmap_words) : 0u;
 #pragma unroll
-        for (int k = 0; k < 64; ++k) {
-          const bool v = lse2 != -INFINITY && visible(kind, c0 + k, kvl, m_search, (sbits >> k) & 1ull);
-          pr[k] = v ? exp2f(pr[k] * p.scale_log2 - lse2) : 0.f;
-        }
+        for (int k = 0; k < 32; ++k) pr[k] = ((vm >> k) & 1u) ? ex2(pr[k] * p.scale_log2 - lse2) : 0.f;
       } else {
 #pragma unroll
-        for (int k = 0; k < 64; ++k) pr[k] = 0.f;
+        for (int k = 0; k < 32; ++k) pr[k] = 0.f;
       }
       // the previous P V must have consumed the P buffer
       ok = ok && (i == 0 || tc::mbar_wait(pv_done, (uint32_t)(i - 1) & 1u, abort_flag));
       if (ok) {
-        // P in the 128-byte swizzled K-major layout: row r, 16-byte chunk q at q ^ (r & 7)
+        // P in the 128-byte swizzled K-major layout: row r, 16-byte chunk q at q ^ (r & 7);
+        // this warp writes chunks 4 ch .. 4 ch + 3 (its 32 keys)
         uint8_t* prow = sp + row * 128;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
+        for (int qq = 0; qq < 4; ++qq) {
+          const int q = 4 * ch + qq;
           uint32_t w[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(pr[q * 8 + 2 * e], pr[q * 8 + 2 * e + 1]);
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(pr[qq * 8 + 2 * e], pr[qq * 8 + 2 * e + 1]);
             w[e] = *reinterpret_cast<uint32_t*>(&h2);
           }
           *reinterpret_cast<uint4*>(prow + ((q ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -480,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int first = max(0, nkeys - c0);
           for (int e = lane; e < (kBN - first) * 16; e += 32) {
             const int r = first + e / 16, part = e % 16;
-            if ((r & 3) != qd) continue;  // the four warps split the rows
+            if ((r & 7) != warp - 2) continue;  // the eight warps split the rows
             *reinterpret_cast<uint4*>(vt + (part >> 3) * (VT_BYTES / 2) + r * 128 + (part & 7) * 16) =
                 make_uint4(0u, 0u, 0u, 0u);
           }
@@ -492,19 +522,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (do_track) {
         if (!track_row) {
 #pragma unroll
-          for (int k = 0; k < 64; ++k) pr[k] = 0.f;
+          for (int k = 0; k < 32; ++k) pr[k] = 0.f;
         }
-        warp_colsum64(pr, lane);
-        atomicAdd(&colacc[2 * lane], pr[0]);
-        atomicAdd(&colacc[2 * lane + 1], pr[1]);
-        tc::named_bar(1, 128);
+        warp_colsum32(pr, lane);
+        atomicAdd(&colacc[32 * ch + lane], pr[0]);
+        tc::named_bar(1, 256);
         if (t_local < 64) {
           const int c = c0 + t_local;
           const float v = colacc[t_local];
           colacc[t_local] = 0.f;
           if (c < kvl && v != 0.f) atomicAdd(p.track + (size_t)b * p.track_ld + c, v * wscale);
         }
-        tc::named_bar(1, 128);
+        tc::named_bar(1, 256);
       }
     }
     if (n_my > 0) tc::mbar_wait(pv_done, (uint32_t)(n_my - 1) & 1u, abort_flag);
@@ -512,14 +541,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ------------------------------------------------------------ output
+  // Each softmax warp owns O columns [64 ch, 64 ch + 64) of its 32 rows. TMEM
+  // loads are warp-collective: issued by whole warps (n_my is uniform), with
+  // per-row conditions only selecting values and guarding stores.
+  constexpr int kOStride = kHD + 4;  // padded fp32 staging rows: conflict-free float4 access
   if (C == 1) {
-    // TMEM loads are warp-collective: issued by whole warps (n_my is uniform),
-    // per-row conditions only select values and guard the stores
     if (warp >= 2) {
       const bool store = row < qlen && !*abort_flag;
       __nv_bfloat16* orow = p.o + (size_t)(q0 + row) * p.d + h * kHD;
 #pragma unroll
-      for (int c0 = 0; c0 < kHD; c0 += 32) {
+      for (int cc = 0; cc < 64; cc += 32) {
+        const int c0 = 64 * ch + cc;
         float a[32];
         if (n_my > 0) tc::tmem_ld_32x32b_x32(tm_o + c0 + lane_off, a);
 #pragma unroll
@@ -540,38 +572,41 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // every split stages its fp32 partial O (already normalised) in its ring;
     // split r then sums rows [r*128/C, (r+1)*128/C) over all splits in rank order
-    float* ostage = reinterpret_cast<float*>(ring);  // [128][128]
+    float* ostage = reinterpret_cast<float*>(ring);  // [128][kOStride]
     if (warp >= 2) {
 #pragma unroll
-      for (int c0 = 0; c0 < kHD; c0 += 32) {
+      for (int cc = 0; cc < 64; cc += 32) {
+        const int c0 = 64 * ch + cc;
         float a[32];
         if (n_my > 0) tc::tmem_ld_32x32b_x32(tm_o + c0 + lane_off, a);
 #pragma unroll
         for (int e = 0; e < 32; ++e) a[e] = (n_my > 0 && lse2 != -INFINITY) ? a[e] : 0.f;
-        // rotate the 16-byte chunks by row to spread shared-memory banks
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int e0 = 4 * ((q + row) & 7);
-          *reinterpret_cast<float4*>(ostage + row * kHD + c0 + e0) = make_float4(a[e0], a[e0 + 1], a[e0 + 2], a[e0 + 3]);
-        }
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<float4*>(ostage + row * kOStride + c0 + 4 * q) =
+              make_float4(a[4 * q], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
       }
     }
     tc::cluster_sync();
     if (warp >= 2) {
       const int rows_per = kBM / C;
-      const int t_local = threadIdx.x - 64;
       const uint32_t base = tc::smem_addr(ostage);
-      for (int e = t_local; e < rows_per * (kHD / 4); e += 128) {
+      for (int e = t_local; e < rows_per * (kHD / 4); e += 256) {
         const int r = (int)rank * rows_per + e / (kHD / 4);
         const int col = (e % (kHD / 4)) * 4;
+        float4 v[kMaxC];
+#pragma unroll
+        for (int src = 0; src < kMaxC; ++src)
+          if (src < C) v[src] = ld_cluster_v4(tc::map_cluster(base + (uint32_t)(r * kOStride + col) * 4u, (uint32_t)src));
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int src = 0; src < C; ++src) {
-          const float4 v = ld_cluster_v4(tc::map_cluster(base + (uint32_t)(r * kHD + col) * 4u, (uint32_t)src));
-          acc.x += v.x;
-          acc.y += v.y;
-          acc.z += v.z;
-          acc.w += v.w;
-        }
+#pragma unroll
+        for (int src = 0; src < kMaxC; ++src)
+          if (src < C) {
+            acc.x += v[src].x;
+            acc.y += v[src].y;
+            acc.z += v[src].z;
+            acc.w += v[src].w;
+          }
         if (r < qlen && !*abort_flag) {
           __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
           uint2 w = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
