@@ -4,18 +4,20 @@
 // section "Method steps in detail", Algorithm 2 step 4: the k decoded
 // tokens with the largest a_i (Eq. (2)) are refreshed next step.
 //
-// One CTA per sequence. The k-th largest score is found exactly by a 4-pass
-// radix select over the order-preserving 32-bit image of the float; ties at
+// One CTA per sequence. The order-preserving 32-bit images of the eligible
+// scores are staged in shared memory once (sequences up to kStage positions;
+// longer ones re-read global memory); the k-th largest key is found exactly
+// by a 4-pass radix select whose bin search is a warp-parallel scan; ties at
 // that threshold are resolved by lowest position with a block prefix count
 // in position order; the <= k survivors are ranked by (score desc, position
-// asc). Scores are read straight from global memory each pass: a sequence's
-// scores are at most a few KB and stay in L1/L2.
+// asc).
 #include "fdl_internal.cuh"
 
 namespace {
 
 constexpr int kThreads = 512;
 constexpr int kMaxK = 1024;
+constexpr int kStage = 8192;
 
 __global__ void __launch_bounds__(kThreads)
 topk_kernel(const float* __restrict__ scores, const unsigned char* __restrict__ eligible, int ld,
@@ -27,6 +29,7 @@ topk_kernel(const float* __restrict__ scores, const unsigned char* __restrict__ 
   __shared__ unsigned sel_key[kMaxK];
   __shared__ int sel_pos[kMaxK];
   __shared__ unsigned n_sel;
+  __shared__ unsigned skey[kStage];  // order key of eligible positions, 0 = not eligible
 
   const int b = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -37,10 +40,21 @@ topk_kernel(const float* __restrict__ scores, const unsigned char* __restrict__ 
   }
   const float* sc = scores + (size_t)b * ld;
   const unsigned char* el = eligible + (size_t)b * ld;
+  const bool staged = n <= kStage;
+  // order key of position i (0 for an ineligible position; real scores map
+  // to keys >= 1 because NaN is excluded)
+  auto key_of = [&](int i) -> unsigned {
+    if (staged) return skey[i];
+    return el[i] ? fdl::float_order_key(sc[i]) : 0u;
+  };
 
-  // number of eligible positions
+  // stage keys and count eligible positions
   unsigned cnt = 0;
-  for (int i = tid; i < n; i += kThreads) cnt += el[i] ? 1u : 0u;
+  for (int i = tid; i < n; i += kThreads) {
+    const bool e = el[i] != 0;
+    cnt += e ? 1u : 0u;
+    if (staged) skey[i] = e ? fdl::float_order_key(sc[i]) : 0u;
+  }
   for (int off = 16; off; off >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
   if (lane == 0) warp_sum[warp] = cnt;
   __syncthreads();
@@ -65,20 +79,35 @@ topk_kernel(const float* __restrict__ scores, const unsigned char* __restrict__ 
       const unsigned prefix = s_prefix;
       const int shift = 8 * digit;
       for (int i = tid; i < n; i += kThreads) {
-        if (!el[i]) continue;
-        unsigned key = fdl::float_order_key(sc[i]);
-        if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+        const unsigned key = key_of(i);
+        if (key != 0u && (key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
       }
       __syncthreads();
-      if (tid == 0) {
-        unsigned rem = s_remaining, acc = 0u;
-        int bin = 255;
-        for (; bin > 0; --bin) {
-          if (acc + hist[bin] >= rem) break;
-          acc += hist[bin];
+      if (warp == 0) {
+        // lane l owns bins 255-8l down to 248-8l; an exclusive scan from the
+        // top bin finds the bin where the running count reaches `remaining`
+        const unsigned rem = s_remaining;
+        unsigned own = 0u;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) own += hist[255 - 8 * lane - t];
+        unsigned incl = own;
+        for (int off = 1; off < 32; off <<= 1) {
+          const unsigned v = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += v;
         }
-        s_remaining = rem - acc;
-        s_prefix = prefix | ((unsigned)bin << shift);
+        const unsigned before = incl - own;
+        const bool mine = before < rem && rem <= incl;
+        const unsigned who = __ballot_sync(0xffffffffu, mine);
+        if (mine && lane == __ffs(who) - 1) {
+          unsigned acc = before;
+          int bin = 255 - 8 * lane;
+          for (int t = 0; t < 7; ++t, --bin) {
+            if (acc + hist[bin] >= rem) break;
+            acc += hist[bin];
+          }
+          s_remaining = rem - acc;
+          s_prefix = prefix | ((unsigned)bin << shift);
+        }
       }
       mask |= 255u << shift;
       __syncthreads();
@@ -93,7 +122,7 @@ topk_kernel(const float* __restrict__ scores, const unsigned char* __restrict__ 
   unsigned ties = 0;
   if (!take_all)
     for (int i = lo; i < hi; ++i)
-      if (el[i] && fdl::float_order_key(sc[i]) == T) ++ties;
+      if (key_of(i) == T) ++ties;
   // exclusive scan of ties over threads
   unsigned incl = ties;
   for (int off = 1; off < 32; off <<= 1) {
@@ -115,8 +144,8 @@ topk_kernel(const float* __restrict__ scores, const unsigned char* __restrict__ 
   __syncthreads();
   unsigned tie_rank = warp_sum[warp] + incl - ties;
   for (int i = lo; i < hi; ++i) {
-    if (!el[i]) continue;
-    unsigned key = fdl::float_order_key(sc[i]);
+    const unsigned key = key_of(i);
+    if (key == 0u) continue;
     bool take;
     if (take_all) take = true;
     else if (key > T) take = true;

@@ -8,18 +8,21 @@
 // stop at the first failure). Fast-dLLM news piece, "confidence-aware
 // parallel decoding": commit the most confident token when none passes.
 //
-// Both phases are HBM-bound reductions over vocab-wide logits rows. Each row
-// is split across the CTAs of one thread-block cluster; every CTA streams its
-// slice with 128-bit loads and keeps a running (max, sum exp, argmax); warps
-// merge with shuffles, CTAs through distributed shared memory. The last
-// cluster to finish (a ticket counter that it resets) takes the per-sequence
-// decisions, so one launch covers one phase.
+// Both phases are HBM-bound reductions over vocab-wide logits rows. A row is
+// split across independent CTAs; every CTA streams its slice with 128-bit
+// loads, keeps (max, sum exp, argmax) per thread over register blocks (tree
+// max, then the sum of exponentials with four accumulators), and merges with
+// warp shuffles. Split CTAs publish their partial to a workspace slot and the
+// row's last CTA to arrive (a ticket it resets) merges the partials in split
+// order, so the result does not depend on timing. The last row to finish (a
+// second ticket) takes the per-sequence decisions: one launch per phase, and
+// nothing ever waits on another CTA.
 #include "fdl_internal.cuh"
 
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kMaxSplit = 8;
+constexpr int kMaxSplit = 16;
 
 struct Stat {
   float m;  // running max
@@ -90,75 +93,81 @@ __device__ __forceinline__ float to_f<float>(float x) { return x; }
 template <>
 __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
 
-// Reduces elements [lo, hi) of one row (this CTA's slice).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Reduces elements [lo, hi) of one row (this CTA's slice). Each thread takes
+// blocks of kVB 128-bit vectors: the block maximum (first index on ties) is
+// found before any exponential, then the block's exp(x - max) are summed with
+// four accumulators; blocks merge into the running statistic.
 template <typename T>
 __device__ Stat slice_stat(const T* row, int lo, int hi, bool vec_ok) {
   constexpr int N = 16 / sizeof(T);
+  constexpr int kVB = 4;
   Stat st{-INFINITY, 0.f, 0x7fffffff};
   const int tid = threadIdx.x;
   int i = lo;
   if (vec_ok) {
-    // lo is a multiple of N; stream full vectors, 4 in flight per thread.
+    // lo is a multiple of N
     const int n_vec = (hi - lo) / N;
     const int4* vp = reinterpret_cast<const int4*>(row + lo);
-    int v = tid;
-    for (; v + 3 * kThreads < n_vec; v += 4 * kThreads) {
-      int4 q0 = __ldcs(vp + v), q1 = __ldcs(vp + v + kThreads);
-      int4 q2 = __ldcs(vp + v + 2 * kThreads), q3 = __ldcs(vp + v + 3 * kThreads);
-      float f[N];
-      unpack(q0, f); fold(st, f, lo + v * N);
-      unpack(q1, f); fold(st, f, lo + (v + kThreads) * N);
-      unpack(q2, f); fold(st, f, lo + (v + 2 * kThreads) * N);
-      unpack(q3, f); fold(st, f, lo + (v + 3 * kThreads) * N);
-    }
-    for (; v < n_vec; v += kThreads) {
-      float f[N];
-      unpack(__ldcs(vp + v), f);
-      fold(st, f, lo + v * N);
+    for (int v0 = 0; v0 < n_vec; v0 += kVB * kThreads) {
+      float f[kVB][N];
+      bool have[kVB];
+#pragma unroll
+      for (int u = 0; u < kVB; ++u) {
+        const int idx = v0 + u * kThreads + tid;
+        have[u] = idx < n_vec;
+        const int4 q = have[u] ? __ldcs(vp + idx) : make_int4(0, 0, 0, 0);
+        unpack(q, f[u]);
+      }
+      float bm = -INFINITY;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int u = 0; u < kVB; ++u)
+#pragma unroll
+        for (int t = 0; t < N; ++t)
+          if (have[u] && f[u][t] > bm) {
+            bm = f[u][t];
+            bi = lo + (v0 + u * kThreads + tid) * N + t;
+          }
+      if (bm == -INFINITY) continue;
+      if (bm > st.m) {
+        st.s = (st.s == 0.f) ? 0.f : st.s * ex2((st.m - bm) * kLog2e);
+        st.m = bm;
+        st.i = bi;
+      }
+      const float mb = st.m * kLog2e;
+      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+      for (int u = 0; u < kVB; ++u)
+#pragma unroll
+        for (int t = 0; t < N; t += 4) {
+          if (!have[u]) continue;
+          a0 += ex2(fmaf(f[u][t], kLog2e, -mb));
+          a1 += ex2(fmaf(f[u][t + 1], kLog2e, -mb));
+          a2 += ex2(fmaf(f[u][t + 2], kLog2e, -mb));
+          a3 += ex2(fmaf(f[u][t + 3], kLog2e, -mb));
+        }
+      st.s += (a0 + a1) + (a2 + a3);
     }
     i = lo + n_vec * N;
   }
   for (int j = i + tid; j < hi; j += kThreads) {
     float x = to_f<T>(row[j]);
     if (x > st.m) {
-      st.s = (st.s == 0.f) ? 0.f : st.s * __expf(st.m - x);
+      st.s = (st.s == 0.f) ? 0.f : st.s * ex2((st.m - x) * kLog2e);
       st.m = x;
       st.i = j;
     }
-    st.s += __expf(x - st.m);
+    st.s += ex2((x - st.m) * kLog2e);
   }
   return st;
-}
-
-__device__ __forceinline__ unsigned smem_u32(const void* p) {
-  return (unsigned)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n"
-               "barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
-}
-
-__device__ __forceinline__ unsigned cluster_rank() {
-  unsigned r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ float ld_dsmem_f32(unsigned addr, unsigned rank) {
-  unsigned remote;
-  float v;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(addr), "r"(rank));
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ int ld_dsmem_s32(unsigned addr, unsigned rank) {
-  unsigned remote;
-  int v;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(addr), "r"(rank));
-  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
-  return v;
 }
 
 struct RowParams {
@@ -173,6 +182,8 @@ struct RowParams {
   int max_search;
   float* out_conf;
   int* out_arg;
+  float* part;                 // [n_rows * split][3] split partials (max, sum, argmax bits)
+  unsigned* row_ticket;        // [n_rows] per-row arrival counters, zero between calls
   unsigned* ticket;
   unsigned* err;
   // unmask decisions
@@ -192,37 +203,52 @@ struct RowParams {
   int* n_accept;
 };
 
-// Per-sequence decisions of the unmask phase; one warp per sequence.
+// Per-sequence decisions of the unmask phase; one warp per sequence. The
+// rows' confidences, positions and sequence ids are first staged in shared
+// memory (up to kStageRows rows) so the ranking loops never wait on L2.
+constexpr int kStageRows = 2048;
+
 __device__ void decide_unmask(const RowParams& p) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const int R = p.n_rows;
-  // row_seq must be non-decreasing and inside [0, B)
+  __shared__ float s_conf[kStageRows];
+  __shared__ int s_pos[kStageRows];
+  __shared__ int s_seq[kStageRows];
   __shared__ int bad;
+  const bool staged = R <= kStageRows;
   if (threadIdx.x == 0) bad = 0;
   __syncthreads();
   for (int r = threadIdx.x; r < R; r += blockDim.x) {
-    int s = p.row_seq[r];
-    if (s < 0 || s >= p.B || (r + 1 < R && p.row_seq[r + 1] < s)) bad = 1;
+    const int sq = p.row_seq[r];
+    if (sq < 0 || sq >= p.B || (r + 1 < R && p.row_seq[r + 1] < sq)) bad = 1;
+    if (staged) {
+      s_conf[r] = __ldcg(p.out_conf + r);
+      s_pos[r] = p.row_pos[r];
+      s_seq[r] = sq;
+    }
   }
   __syncthreads();
   if (bad) {
     if (threadIdx.x == 0) fdl::raise_error(p.err, FDL_DEVERR_SHAPE);
     return;
   }
+  auto conf = [&](int r) { return staged ? s_conf[r] : __ldcg(p.out_conf + r); };
+  auto pos = [&](int r) { return staged ? s_pos[r] : p.row_pos[r]; };
+  auto seq = [&](int r) { return staged ? s_seq[r] : p.row_seq[r]; };
   for (int b = warp; b < p.B; b += nw) {
     // rows of b: [lo, hi) by binary search on the sorted row_seq
     int lo = 0, hi = R;
     {
       int a = 0, z = R;
-      while (a < z) { int m = (a + z) >> 1; if (p.row_seq[m] < b) a = m + 1; else z = m; }
+      while (a < z) { int m = (a + z) >> 1; if (seq(m) < b) a = m + 1; else z = m; }
       lo = a;
       z = R;
-      while (a < z) { int m = (a + z) >> 1; if (p.row_seq[m] <= b) a = m + 1; else z = m; }
+      while (a < z) { int m = (a + z) >> 1; if (seq(m) <= b) a = m + 1; else z = m; }
       hi = a;
     }
     // eps rule
     bool any = false;
-    for (int r = lo + lane; r < hi; r += 32) any |= __ldcg(p.out_conf + r) >= p.eps;
+    for (int r = lo + lane; r < hi; r += 32) any |= conf(r) >= p.eps;
     any = __any_sync(0xffffffffu, any);
     int forced = -1;
     if (p.force_progress && !any && hi > lo) {
@@ -230,8 +256,8 @@ __device__ void decide_unmask(const RowParams& p) {
       float bc = -1.f;
       int bp = 0x7fffffff, br = -1;
       for (int r = lo + lane; r < hi; r += 32) {
-        float c = __ldcg(p.out_conf + r);
-        int ps = p.row_pos[r];
+        const float c = conf(r);
+        const int ps = pos(r);
         if (c > bc || (c == bc && ps < bp)) { bc = c; bp = ps; br = r; }
       }
       for (int off = 16; off; off >>= 1) {
@@ -242,27 +268,26 @@ __device__ void decide_unmask(const RowParams& p) {
       }
       forced = br;
     }
-    for (int r = lo + lane; r < hi; r += 32)
-      p.commit[r] = (__ldcg(p.out_conf + r) >= p.eps || r == forced) ? 1 : 0;
+    for (int r = lo + lane; r < hi; r += 32) p.commit[r] = (conf(r) >= p.eps || r == forced) ? 1 : 0;
     // rank the uncommitted rows by (conf desc, pos asc)
     int n_unc = 0;
     for (int r = lo + lane; r < hi; r += 32) {
-      float c = __ldcg(p.out_conf + r);
-      bool unc = !(c >= p.eps) && r != forced;
+      const float c = conf(r);
+      const bool unc = !(c >= p.eps) && r != forced;
       n_unc += unc ? 1 : 0;
       if (!unc) continue;
-      int ps = p.row_pos[r];
+      const int ps = pos(r);
       int rank = 0;
       for (int o = lo; o < hi; ++o) {
-        float co = __ldcg(p.out_conf + o);
+        const float co = conf(o);
         if (co >= p.eps || o == forced) continue;
-        int po = p.row_pos[o];
+        const int po = pos(o);
         rank += (co > c || (co == c && po < ps)) ? 1 : 0;
       }
       if (rank < p.max_search) p.search_rows[b * p.max_search + rank] = r;
     }
     for (int off = 16; off; off >>= 1) n_unc += __shfl_xor_sync(0xffffffffu, n_unc, off);
-    int ns = min(n_unc, p.max_search);
+    const int ns = min(n_unc, p.max_search);
     for (int j = ns + lane; j < p.max_search; j += 32) p.search_rows[b * p.max_search + j] = -1;
     if (lane == 0) p.n_search_out[b] = ns;
   }
@@ -296,59 +321,61 @@ __device__ void decide_verify(const RowParams& p) {
 template <typename T>
 __global__ void __launch_bounds__(kThreads) row_reduce_kernel(RowParams p) {
   __shared__ Stat warp_stat[kThreads / 32];
-  __shared__ float cta_m, cta_s;
-  __shared__ int cta_i;
-  __shared__ unsigned last;
+  __shared__ unsigned go;
   const int row = blockIdx.x / p.split;
-  const unsigned rank = p.split > 1 ? cluster_rank() : 0u;
+  const int sp = blockIdx.x % p.split;
   bool valid = row < p.n_rows;
   if (valid && p.phase == 1) {
     int b = row / p.max_search, j = row % p.max_search;
     valid = j < p.n_search[b];
   }
+  if (!valid && sp != 0) return;  // an idle row takes one global ticket, from split 0
   Stat st{-INFINITY, 0.f, 0x7fffffff};
   if (valid) {
     const T* base = reinterpret_cast<const T*>(p.logits) + (size_t)row * p.vocab;
-    int lo = (int)rank * p.chunk;
-    int hi = min(p.vocab, lo + p.chunk);
+    const int lo = sp * p.chunk;
+    const int hi = min(p.vocab, lo + p.chunk);
     if (lo < hi) st = slice_stat<T>(base, lo, hi, p.vec_ok);
   }
   for (int off = 16; off; off >>= 1) st = shfl_merge(st, off);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (lane == 0) warp_stat[warp] = st;
   __syncthreads();
-  if (warp == 0) {
-    st = lane < kThreads / 32 ? warp_stat[lane] : Stat{-INFINITY, 0.f, 0x7fffffff};
-    for (int off = 16; off; off >>= 1) st = shfl_merge(st, off);
-    if (lane == 0) { cta_m = st.m; cta_s = st.s; cta_i = st.i; }
-  }
-  if (p.split > 1) {
-    cluster_sync_all();  // every slice result is in its CTA's shared memory
-    if (rank == 0 && threadIdx.x == 0) {
-      Stat acc{cta_m, cta_s, cta_i};
-      for (int r = 1; r < p.split; ++r) {
-        Stat o{ld_dsmem_f32(smem_u32(&cta_m), r), ld_dsmem_f32(smem_u32(&cta_s), r),
-               ld_dsmem_s32(smem_u32(&cta_i), r)};
-        acc = merge(acc, o);
-      }
-      cta_m = acc.m; cta_s = acc.s; cta_i = acc.i;
-    }
-    cluster_sync_all();  // peers stay resident until rank 0 has read them
-  } else {
-    __syncthreads();
-  }
-  if (rank != 0) return;
   if (threadIdx.x == 0) {
-    if (valid) {
-      p.out_conf[row] = 1.f / cta_s;  // cta_s = sum exp(x - max) >= 1
-      p.out_arg[row] = cta_i;
+    Stat acc = warp_stat[0];
+    for (int w = 1; w < kThreads / 32; ++w) acc = merge(acc, warp_stat[w]);
+    unsigned proceed = 1u;
+    if (valid && p.split > 1) {
+      float* slot = p.part + ((size_t)row * p.split + sp) * 3;
+      __stcg(slot, acc.m);
+      __stcg(slot + 1, acc.s);
+      __stcg(slot + 2, __int_as_float(acc.i));
+      __threadfence();
+      const unsigned t = atomicAdd(p.row_ticket + row, 1u);
+      proceed = t == (unsigned)(p.split - 1) ? 1u : 0u;
+      if (proceed) {
+        p.row_ticket[row] = 0u;  // all splits arrived: ready for the next call
+        __threadfence();
+        acc = Stat{-INFINITY, 0.f, 0x7fffffff};
+        for (int k = 0; k < p.split; ++k) {  // split order, independent of arrival order
+          const float* o = p.part + ((size_t)row * p.split + k) * 3;
+          acc = merge(acc, Stat{__ldcg(o), __ldcg(o + 1), __float_as_int(__ldcg(o + 2))});
+        }
+      }
     }
-    __threadfence();
-    unsigned t = atomicAdd(p.ticket, 1u);
-    last = (t == (unsigned)p.n_rows - 1u) ? 1u : 0u;
+    if (proceed) {
+      if (valid) {
+        p.out_conf[row] = 1.f / acc.s;  // acc.s = sum exp(x - max) >= 1
+        p.out_arg[row] = acc.i;
+      }
+      __threadfence();
+      const unsigned t = atomicAdd(p.ticket, 1u);
+      proceed = (t == (unsigned)p.n_rows - 1u) ? 2u : 0u;
+    }
+    go = proceed;
   }
   __syncthreads();
-  if (!last) return;
+  if (go != 2u) return;
   __threadfence();
   if (p.phase == 0) decide_unmask(p);
   else decide_verify(p);
@@ -359,27 +386,21 @@ template <typename T>
 cudaError_t launch_phase(fdl_ctx* ctx, RowParams p) {
   if (p.n_rows == 0) return cudaSuccess;
   const int V = p.vocab;
-  int split = (2 * ctx->num_sms + p.n_rows - 1) / p.n_rows;
+  // about four CTAs per SM in total; slices of at least 2048 elements
+  int split = (4 * ctx->num_sms + p.n_rows - 1) / p.n_rows;
   split = max(1, min(split, kMaxSplit));
-  split = min(split, max(1, V / 4096));
+  split = min(split, max(1, V / 2048));
+  if ((size_t)p.n_rows * split > (size_t)ctx->row_slots) split = 1;
   int chunk = (V + split - 1) / split;
   chunk = (chunk + 7) / 8 * 8;
   split = (V + chunk - 1) / chunk;
   p.split = split;
   p.chunk = chunk;
+  p.part = ctx->row_part;
+  p.row_ticket = ctx->row_tickets;
   p.vec_ok = ((reinterpret_cast<uintptr_t>(p.logits) & 15) == 0) && ((size_t)V * sizeof(T)) % 16 == 0;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(p.n_rows * split), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.stream = ctx->stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = split;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = split > 1 ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, row_reduce_kernel<T>, p);
+  row_reduce_kernel<T><<<(unsigned)(p.n_rows * split), kThreads, 0, ctx->stream>>>(p);
+  return cudaGetLastError();
 }
 
 }  // namespace
