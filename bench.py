@@ -42,6 +42,32 @@ METRIC = "layer-step query-tokens/s at LLaDA-8B shapes; % of bf16 TC peak / HBM 
 WORKLOAD = "llada8b_layer_bf16_b1_p512_g256_w32_t32"
 
 
+# DRAM traffic of one launch of the projection kernel on this workload
+# (dram__bytes_read.sum + dram__bytes_write.sum), from the ncu capture
+# summarised in profiles/qkv_tc_kernel_llada8b_layer.txt. It is reported only
+# while the sources it was taken from hash to the recorded value; after any
+# change to them the figure is stale and the line carries null.
+QKV_TRAFFIC = {"sources_sha256": "89ca5f1ae9f17fff14066c74f98f2d5671aaa073500fc7570e9f3fbfbea9a552",
+               "bytes": 102026240 + 3668224}
+QKV_SOURCES = ("kv_cache_attention_gb300/csrc/fdl_qkv_tc.cu", "kv_cache_attention_gb300/csrc/fdl_qkv.cu",
+               "kv_cache_attention_gb300/csrc/tc_ptx.cuh", "kv_cache_attention_gb300/csrc/fdl_internal.cuh")
+
+
+def sources_sha256(paths) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in paths:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def qkv_traffic():
+    if QKV_TRAFFIC["sources_sha256"] and QKV_TRAFFIC["sources_sha256"] == sources_sha256(QKV_SOURCES):
+        return QKV_TRAFFIC["bytes"]
+    return None
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -117,13 +143,22 @@ def barrier(world):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """The largest of the ranks' x (every rank gets it): the job's time is
+    the slowest replica's."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_rate(rows_per_rank_step: int, steps: int, ms_max: float, world: int) -> float:
+    """Rows of all ranks' steps over the slowest rank's time (rows/s); every
+    rank runs the same replica workload."""
+    return world * rows_per_rank_step * steps / (ms_max * 1e-3)
 
 
 # ---------------------------------------------------------------------------
@@ -246,37 +281,59 @@ def run_gpu(args, world, rank, local):
     nsr = torch.empty((1,), dtype=torch.int32, device="cuda")
     launches_per_step = 5  # qkv, work-list build, attention, top-k, unmask (our kernels)
 
-    def step(c, X=None, L=None):
+    def qkv_part(c, X=None):
         X = Xs[c] if X is None else X
+        ctx.qkv_rope_cache_write(X, Ws[c], row_seq, row_rope, row_cache, bt, KC[c], VC[c], q)
+
+    def rest_part(c, L=None):
         L = Ls[c] if L is None else L
         track.zero_()
-        ctx.qkv_rope_cache_write(X, Ws[c], row_seq, row_rope, row_cache, bt, KC[c], VC[c], q)
         ctx.sched_attn(q, KC[c], VC[c], bt, cu, kv_len, row_kind, o, lse_out=lse, track_scores=track)
         ctx.track_topk(track, elig, seq_len, k, idx, cnt)
         ctx.unmask_verify(1, ms, logits=L, row_seq=win_seq, row_pos=win_pos, eps=e["eps"], force_progress=False,
                           conf=conf, argmax=arg, commit=com, search_rows=srows, n_search=nsr)
 
-    def qkv_only(c):
-        ctx.qkv_rope_cache_write(Xs[c], Ws[c], row_seq, row_rope, row_cache, bt, KC[c], VC[c], q)
+    def step(c, X=None, L=None):
+        qkv_part(c, X)
+        rest_part(c, L)
 
     for i in range(args.warmup):
         step(i % n_copies)
     ctx.sync_status()
-    # The device-resident step is replayed from CUDA graphs (one per rotating
-    # input copy) so host launch cost does not stand in for GPU time; the
-    # graphs hold exactly the kernels a direct call launches.
+    # The device-resident step is replayed from CUDA graphs so host launch
+    # cost does not stand in for GPU time; the graphs hold exactly the kernels
+    # a direct call launches. Each graph also holds an event-record node on
+    # either side of the projection, so the dominant kernel is timed inside
+    # the timed steps themselves. A graph's events are overwritten when it is
+    # replayed again, so the steps cycle over n_graphs graphs and the
+    # projection's duration is averaged over the last n_graphs timed steps.
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+        in_graph_events = True
+    except TypeError:
+        in_graph_events = False
+    n_graphs = 4 * n_copies
+    qa = [torch.cuda.Event(enable_timing=True, external=in_graph_events) for _ in range(n_graphs)]
+    qb = [torch.cuda.Event(enable_timing=True, external=in_graph_events) for _ in range(n_graphs)]
     step_graphs, qkv_graphs = [], []
-    for c in range(n_copies):
-        g_step, g_qkv = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    for j in range(n_graphs):
+        c = j % n_copies
+        g_step = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g_step, stream=stream):
-            step(c)
-        with torch.cuda.graph(g_qkv, stream=stream):
-            qkv_only(c)
+            if in_graph_events:
+                qa[j].record(stream)
+            qkv_part(c)
+            if in_graph_events:
+                qb[j].record(stream)
+            rest_part(c)
         step_graphs.append(g_step)
-        qkv_graphs.append(g_qkv)
-    for i in range(args.warmup):
-        step_graphs[i % n_copies].replay()
-        qkv_graphs[i % n_copies].replay()
+        if not in_graph_events and j < n_copies:
+            g_qkv = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_qkv, stream=stream):
+                qkv_part(c)
+            qkv_graphs.append(g_qkv)
+    for i in range(max(args.warmup, n_graphs)):
+        step_graphs[i % n_graphs].replay()
     ctx.sync_status()
     K = args.steps
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -285,7 +342,7 @@ def run_gpu(args, world, rank, local):
     with Clocks(local) as clk:
         t0.record(stream)
         for i in range(K):
-            step_graphs[i % n_copies].replay()
+            step_graphs[i % n_graphs].replay()
         t1.record(stream)
         torch.cuda.synchronize()
     barrier(world)
@@ -293,15 +350,20 @@ def run_gpu(args, world, rank, local):
     ms_total = t0.elapsed_time(t1)
     ms_total = max_over_ranks(ms_total, world)
     ms_step = ms_total / K
-    value = world * R * K / (ms_total * 1e-3)
-    # dominant kernel alone, back to back over the same rotating copies
-    q0e, q1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    q0e.record(stream)
-    for i in range(K):
-        qkv_graphs[i % n_copies].replay()
-    q1e.record(stream)
-    torch.cuda.synchronize()
-    qkv_ms = [q0e.elapsed_time(q1e) / K]
+    value = whole_job_rate(R, K, ms_total, world)
+    if in_graph_events:
+        last = [(K - 1 - t) % n_graphs for t in range(min(K, n_graphs))]
+        qkv_ms = [qa[j].elapsed_time(qb[j]) for j in last]
+        qkv_timing = f"CUDA event nodes around the projection inside the step graph; last {len(last)} timed steps"
+    else:
+        q0e, q1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        q0e.record(stream)
+        for i in range(K):
+            qkv_graphs[i % n_copies].replay()
+        q1e.record(stream)
+        torch.cuda.synchronize()
+        qkv_ms = [q0e.elapsed_time(q1e) / K]
+        qkv_timing = "CUDA events over back-to-back replays of the projection alone, after the timed steps"
 
     # end to end: pinned host inputs in, step results out, every step
     x_pin = x_host.pin_memory()
@@ -330,7 +392,7 @@ def run_gpu(args, world, rank, local):
     b.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(a.elapsed_time(b), world)
-    e2e_value = world * R * K_e2e / (e2e_ms * 1e-3)
+    e2e_value = whole_job_rate(R, K_e2e, e2e_ms, world)
 
     if rank != 0:
         return
@@ -343,15 +405,15 @@ def run_gpu(args, world, rank, local):
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "global_batch": world, "seq_len": N, "rows_per_step": R,
-                   "parallelism": f"replicas{world}", "launch": "CUDA graph replay per step",
+                   "parallelism": f"replicas{world}", "launch": "one CUDA graph replay per step",
                    "l2_hygiene": f"{n_copies} rotating copies of W/X/cache/logits "
                    f"({per_copy * n_copies / 1e9:.2f} GB > 4x L2 {l2 / 1e6:.0f} MB)"},
         "e2e": {"value": e2e_value, "unit": "query-rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * K,
         "roofline": {"kernel": "qkv_rope_cache_write", "bound": "hbm", "achieved": achieved, "peak": hbm,
-                     "unit": "GB/s", "frac": achieved / hbm, "traffic": None, "peak_source": src,
+                     "unit": "GB/s", "frac": achieved / hbm, "traffic": qkv_traffic(), "peak_source": src,
                      "algorithmic_bytes": qkv_bytes, "avg_launch_us": qkv_avg * 1e3,
-                     "timing": "CUDA events over back-to-back graph replays of the projection alone"},
+                     "timing": qkv_timing},
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline:

@@ -11,7 +11,9 @@ tracked sets feeding the next step are identical on both sides.
 test_chain_full_size: the full 32 layers x 16 steps on the GPU alone, checked
 by properties that hold at any size: every sequence's scores sum to the
 number of layers, top-32 equals a full sort of the scores the kernel got,
-sampled projection rows match the oracle, and a re-run is bit-identical."""
+sampled projection rows match the oracle, and a teacher-forced re-run gives
+the same scores to within fp32 reassociation and the same tracked sets
+wherever their cut is not a near-tie."""
 import numpy as np
 import pytest
 
@@ -117,7 +119,7 @@ def test_chain_full_size():
     k = e["topk"]
     sample_layers = (0, 15, 31)
 
-    def run(check):
+    def run(check, forced=None):
         caches = [(torch.zeros((n_slots, d), dtype=torch.bfloat16, device="cuda"),
                    torch.zeros((n_slots, d), dtype=torch.bfloat16, device="cuda")) for _ in range(L)]
         tracked, hist = None, []
@@ -155,12 +157,21 @@ def test_chain_full_size():
                     order = pos[np.lexsort((pos, -sc[b, pos].astype(np.float64)))]
                     assert ih[b].tolist() == order[:k].tolist()
             hist.append((sc, ih))
-            tracked = [ih[b] for b in range(B)]
+            src = ih if forced is None else forced[step][1]
+            tracked = [src[b] for b in range(B)]
         return hist
 
+    # The tracker adds each head's column sums into the scores with fp32
+    # atomics, whose order varies between runs, so a re-run reproduces the
+    # scores to within that reassociation error rather than bit for bit. The
+    # re-run is fed the first run's tracked sets (so a near-tie cannot fork
+    # the chain) and must give the same sets wherever the k-th and (k+1)-th
+    # scores are further apart than that error.
     first = run(True)
-    second = run(False)
+    second = run(False, forced=first)
     for (s1, i1), (s2, i2) in zip(first, second):
-        assert np.array_equal(i1, i2)
         np.testing.assert_allclose(s1, s2, rtol=0, atol=1e-6)
+        for b in range(B):
+            if H.topk_margin_ok(s1[b], e["eligible"][b], N, k, 4e-6):
+                assert i1[b].tolist() == i2[b].tolist()
     ctx.close()
