@@ -11,9 +11,11 @@ the launching stream, bracketed by a barrier and torch.cuda.synchronize().
 Weights, caches, hidden rows and logits rotate over enough copies that the
 step's working set is several times the L2 size, so no step reads a
 previous step's data out of L2. The dominant kernel (the QKV projection,
-which streams the 100.7 MB weight) is bracketed by its own events every
-step for the roofline figure. SM clocks and throttle reasons are sampled
-with nvidia-smi during the timed region.
+which streams the 100.7 MB weight) is timed for the roofline figure by CUDA
+events around back-to-back graph launches of it alone, right after the
+timed steps (events inside the step graph would slow the step itself). SM
+clocks and throttle reasons are sampled with nvidia-smi during the timed
+region.
 
 --impl reference times the float64 CPU oracle (the reference arm of this
 build; there is no upstream implementation to install) on bounded samples
@@ -300,40 +302,27 @@ def run_gpu(args, world, rank, local):
     for i in range(args.warmup):
         step(i % n_copies)
     ctx.sync_status()
-    # The device-resident step is replayed from CUDA graphs so host launch
-    # cost does not stand in for GPU time; the graphs hold exactly the kernels
-    # a direct call launches. Each graph also holds an event-record node on
-    # either side of the projection, so the dominant kernel is timed inside
-    # the timed steps themselves. A graph's events are overwritten when it is
-    # replayed again, so the steps cycle over n_graphs graphs and the
-    # projection's duration is averaged over the last n_graphs timed steps.
-    try:
-        torch.cuda.Event(enable_timing=True, external=True)
-        in_graph_events = True
-    except TypeError:
-        in_graph_events = False
-    n_graphs = 4 * n_copies
-    qa = [torch.cuda.Event(enable_timing=True, external=in_graph_events) for _ in range(n_graphs)]
-    qb = [torch.cuda.Event(enable_timing=True, external=in_graph_events) for _ in range(n_graphs)]
-    step_graphs, qkv_graphs = [], []
-    for j in range(n_graphs):
-        c = j % n_copies
+    # The device-resident step is replayed from CUDA graphs (one per rotating
+    # input copy) so host launch cost does not stand in for GPU time; the
+    # graphs hold exactly the kernels a direct call launches. Nothing else is
+    # put inside the step graph: event-record nodes between its kernels were
+    # measured to add about 9 us per step.
+    step_graphs = []
+    for c in range(n_copies):
         g_step = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g_step, stream=stream):
-            if in_graph_events:
-                qa[j].record(stream)
-            qkv_part(c)
-            if in_graph_events:
-                qb[j].record(stream)
-            rest_part(c)
+            step(c)
         step_graphs.append(g_step)
-        if not in_graph_events and j < n_copies:
-            g_qkv = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g_qkv, stream=stream):
-                qkv_part(c)
-            qkv_graphs.append(g_qkv)
-    for i in range(max(args.warmup, n_graphs)):
-        step_graphs[i % n_graphs].replay()
+    # The dominant kernel's launch duration: one graph holding the projection
+    # once per rotating copy, replayed back to back right after the timed
+    # steps, between CUDA events on the same stream.
+    qkv_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(qkv_graph, stream=stream):
+        for c in range(n_copies):
+            qkv_part(c)
+    for i in range(args.warmup):
+        step_graphs[i % n_copies].replay()
+    qkv_graph.replay()
     ctx.sync_status()
     K = args.steps
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -342,7 +331,7 @@ def run_gpu(args, world, rank, local):
     with Clocks(local) as clk:
         t0.record(stream)
         for i in range(K):
-            step_graphs[i % n_graphs].replay()
+            step_graphs[i % n_copies].replay()
         t1.record(stream)
         torch.cuda.synchronize()
     barrier(world)
@@ -351,19 +340,16 @@ def run_gpu(args, world, rank, local):
     ms_total = max_over_ranks(ms_total, world)
     ms_step = ms_total / K
     value = whole_job_rate(R, K, ms_total, world)
-    if in_graph_events:
-        last = [(K - 1 - t) % n_graphs for t in range(min(K, n_graphs))]
-        qkv_ms = [qa[j].elapsed_time(qb[j]) for j in last]
-        qkv_timing = f"CUDA event nodes around the projection inside the step graph; last {len(last)} timed steps"
-    else:
-        q0e, q1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        q0e.record(stream)
-        for i in range(K):
-            qkv_graphs[i % n_copies].replay()
-        q1e.record(stream)
-        torch.cuda.synchronize()
-        qkv_ms = [q0e.elapsed_time(q1e) / K]
-        qkv_timing = "CUDA events over back-to-back replays of the projection alone, after the timed steps"
+    n_qkv = max(1, K // n_copies)
+    q0e, q1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    q0e.record(stream)
+    for i in range(n_qkv):
+        qkv_graph.replay()
+    q1e.record(stream)
+    torch.cuda.synchronize()
+    qkv_ms = [q0e.elapsed_time(q1e) / (n_qkv * n_copies)]
+    qkv_timing = (f"CUDA events over {n_qkv * n_copies} back-to-back graph launches of the projection "
+                  f"(rotating copies), right after the timed steps")
 
     # end to end: pinned host inputs in, step results out, every step
     x_pin = x_host.pin_memory()

@@ -227,9 +227,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int C = p.C;
   const uint32_t rank = C > 1 ? tc::cluster_ctarank() : 0u;
-  const int item = blockIdx.x / C;
+  const int item = blockIdx.z;
   const int h = blockIdx.y;
-  if (item >= p.wl[0]) return;  // uniform over the cluster
+  if (item >= p.wl[0]) return;  // uniform over the cluster (a cluster spans x only)
   const int* it = p.wl + 1 + 4 * item;
   const int b = it[0], q0 = it[1], qlen = it[2], nkeys = it[3];
   const int kvl = min(p.kv_len[b], nkeys);
@@ -706,7 +706,10 @@ cudaError_t fdl_launch_attn_tc(fdl_ctx* ctx, const void* q, const void* k_cache,
   while (C < kMaxC && est_items * c.n_heads * (2 * C) <= ctx->num_sms) C *= 2;
   p.C = C;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(cap * C), (unsigned)c.n_heads, 1);
+  // grid (split, head, item): items vary slowest, so the CTAs of real items
+  // are scheduled before the idle tail of the capacity bound
+  if (cap > 65535) return cudaErrorInvalidConfiguration;
+  cfg.gridDim = dim3((unsigned)C, (unsigned)c.n_heads, (unsigned)cap);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = ctx->stream;

@@ -13,8 +13,9 @@
 // loads, keeps (max, sum exp, argmax) per thread over register blocks (tree
 // max, then the sum of exponentials with four accumulators), and merges with
 // warp shuffles. Split CTAs publish their partial to a workspace slot and the
-// row's last CTA to arrive (a ticket it resets) merges the partials in split
-// order, so the result does not depend on timing. The last row to finish (a
+// row's last CTA to arrive (a ticket it resets) loads all partials at once
+// and merges them by a fixed xor tree, so the result does not depend on
+// timing. The last row to finish (a
 // second ticket) takes the per-sequence decisions: one launch per phase, and
 // nothing ever waits on another CTA.
 #include "fdl_internal.cuh"
@@ -341,38 +342,50 @@ __global__ void __launch_bounds__(kThreads) row_reduce_kernel(RowParams p) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (lane == 0) warp_stat[warp] = st;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    Stat acc = warp_stat[0];
-    for (int w = 1; w < kThreads / 32; ++w) acc = merge(acc, warp_stat[w]);
+  if (warp == 0) {
+    // block statistic: lanes 0..7 hold the warps' statistics, merged by a
+    // fixed xor tree (lane 0 ends with the result)
+    const Stat none{-INFINITY, 0.f, 0x7fffffff};
+    Stat acc = lane < kThreads / 32 ? warp_stat[lane] : none;
+    for (int off = kThreads / 64; off; off >>= 1) acc = shfl_merge(acc, off);
     unsigned proceed = 1u;
     if (valid && p.split > 1) {
-      float* slot = p.part + ((size_t)row * p.split + sp) * 3;
-      __stcg(slot, acc.m);
-      __stcg(slot + 1, acc.s);
-      __stcg(slot + 2, __int_as_float(acc.i));
-      __threadfence();
-      const unsigned t = atomicAdd(p.row_ticket + row, 1u);
-      proceed = t == (unsigned)(p.split - 1) ? 1u : 0u;
-      if (proceed) {
-        p.row_ticket[row] = 0u;  // all splits arrived: ready for the next call
+      if (lane == 0) {
+        float* slot = p.part + ((size_t)row * p.split + sp) * 3;
+        __stcg(slot, acc.m);
+        __stcg(slot + 1, acc.s);
+        __stcg(slot + 2, __int_as_float(acc.i));
         __threadfence();
-        acc = Stat{-INFINITY, 0.f, 0x7fffffff};
-        for (int k = 0; k < p.split; ++k) {  // split order, independent of arrival order
-          const float* o = p.part + ((size_t)row * p.split + k) * 3;
-          acc = merge(acc, Stat{__ldcg(o), __ldcg(o + 1), __float_as_int(__ldcg(o + 2))});
+        const unsigned t = atomicAdd(p.row_ticket + row, 1u);
+        proceed = t == (unsigned)(p.split - 1) ? 1u : 0u;
+        if (proceed) p.row_ticket[row] = 0u;  // all splits arrived: ready for the next call
+      }
+      proceed = __shfl_sync(0xffffffffu, proceed, 0);
+      if (proceed) {
+        // the row's last CTA: lane k loads split k's partial (all loads in
+        // flight at once) and a fixed xor tree merges them, so the result
+        // does not depend on the order in which the splits arrived
+        __threadfence();
+        acc = none;
+        if (lane < p.split) {
+          const float* o = p.part + ((size_t)row * p.split + lane) * 3;
+          acc = Stat{__ldcg(o), __ldcg(o + 1), __float_as_int(__ldcg(o + 2))};
         }
+        for (int off = kMaxSplit / 2; off; off >>= 1) acc = shfl_merge(acc, off);
       }
     }
-    if (proceed) {
-      if (valid) {
-        p.out_conf[row] = 1.f / acc.s;  // acc.s = sum exp(x - max) >= 1
-        p.out_arg[row] = acc.i;
+    if (lane == 0) {
+      if (proceed) {
+        if (valid) {
+          p.out_conf[row] = 1.f / acc.s;  // acc.s = sum exp(x - max) >= 1
+          p.out_arg[row] = acc.i;
+        }
+        __threadfence();
+        const unsigned t = atomicAdd(p.ticket, 1u);
+        proceed = (t == (unsigned)p.n_rows - 1u) ? 2u : 0u;
       }
-      __threadfence();
-      const unsigned t = atomicAdd(p.ticket, 1u);
-      proceed = (t == (unsigned)p.n_rows - 1u) ? 2u : 0u;
+      go = proceed;
     }
-    go = proceed;
   }
   __syncthreads();
   if (go != 2u) return;

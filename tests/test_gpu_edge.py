@@ -138,6 +138,35 @@ def test_topk_ties_signed_zero_and_short_sequences():
     ctx.close()
 
 
+def test_topk_every_selection_path():
+    """Rows that take each way through the selection: spread scores (the
+    threshold bin is found within one digit), dense ties at the full key with
+    at most 1024 candidates, more than 1024 keys tied at the threshold (cut
+    by position), all keys equal, and rows longer than the shared-memory
+    stage (read from global memory)."""
+    import torch
+    rng = np.random.default_rng(11)
+    for ld in (4000, 9000):
+        ctx = _tiny_ctx(max_batch=5)
+        sc = np.zeros((5, ld), np.float32)
+        sc[0] = (32 * np.exp(1.5 * rng.standard_normal(ld)) / ld).astype(np.float32)
+        sc[1] = rng.integers(0, 40, ld).astype(np.float32) / 8            # ~100 copies of each value
+        sc[2] = np.where(rng.random(ld) < 0.6, 1.0, rng.random(ld)).astype(np.float32)  # >1024 tied at the top
+        sc[3] = 0.25
+        sc[4] = rng.standard_normal(ld).astype(np.float32)
+        el = (rng.random((5, ld)) < 0.8).astype(np.uint8)
+        seq_len = np.array([ld, ld - 7, ld, ld - 100, ld // 3], np.int32)
+        for k in (32, 1024):
+            idx = torch.empty((5, k), dtype=torch.int32, device="cuda")
+            cnt = torch.empty((5,), dtype=torch.int32, device="cuda")
+            ctx.track_topk(H.dev(sc), H.u8(el), H.ints(seq_len), k, idx, cnt)
+            ctx.sync_status()
+            want, wc = oracle.track_topk(sc, el, seq_len, k)
+            assert H.host(idx).tolist() == want.tolist(), (ld, k)
+            assert H.host(cnt).tolist() == wc.tolist()
+        ctx.close()
+
+
 def test_unmask_ties_and_forced_progress_per_sequence():
     import torch
     ctx = _tiny_ctx(max_batch=4, vocab=64)
