@@ -120,6 +120,8 @@ __device__ __forceinline__ float4 ld_cluster_v4(uint32_t caddr) {
   return v;
 }
 
+__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -198,6 +200,47 @@ __device__ __forceinline__ void warp_colsum32(float (&v)[32], int lane) {
   }
 }
 
+// Split `rank` of a C-CTA cluster sums rows [rank * 128 / C, (rank + 1) *
+// 128 / C) of the C staged fp32 O tiles in rank order and stores them as
+// bf16; every thread's remote loads are issued together.
+template <int CC>
+__device__ __forceinline__ void merge_o(const TcAttnParams& p, uint32_t base, uint32_t rank, int t_local, int q0,
+                                        int qlen, int h, bool aborted) {
+  constexpr int kOStride = kHD + 4;
+  constexpr int rows_per = kBM / CC;
+  constexpr int per_thr = rows_per * (kHD / 4) / 256;
+  static_assert(per_thr * 256 == rows_per * (kHD / 4), "whole float4 columns per thread");
+  float4 v[per_thr][CC];
+#pragma unroll
+  for (int u = 0; u < per_thr; ++u) {
+    const int e = t_local + 256 * u;
+    const int r = (int)rank * rows_per + e / (kHD / 4);
+    const int col = (e % (kHD / 4)) * 4;
+#pragma unroll
+    for (int src = 0; src < CC; ++src)
+      v[u][src] = ld_cluster_v4(tc::map_cluster(base + (uint32_t)(r * kOStride + col) * 4u, (uint32_t)src));
+  }
+#pragma unroll
+  for (int u = 0; u < per_thr; ++u) {
+    const int e = t_local + 256 * u;
+    const int r = (int)rank * rows_per + e / (kHD / 4);
+    const int col = (e % (kHD / 4)) * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int src = 0; src < CC; ++src) {
+      acc.x += v[u][src].x;
+      acc.y += v[u][src].y;
+      acc.z += v[u][src].z;
+      acc.w += v[u][src].w;
+    }
+    if (r < qlen && !aborted) {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+      uint2 w = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+      *reinterpret_cast<uint2*>(p.o + (size_t)(q0 + r) * p.d + h * kHD + col) = w;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const TcAttnParams p) {
@@ -238,7 +281,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int t0 = (int)(rank * n_tiles / C), t1 = (int)((rank + 1) * n_tiles / C);
   const int n_my = t1 - t0;
 
+  // slot of key tile j's first key; an unmapped page points past the cache
+  // so the TMA zero-fills the tile (and the error word says so)
+  auto tile_slot = [&](int j, bool report) -> int {
+    const int c0 = j * kBN;
+    const int pi = c0 / p.page_size;
+    const int page = pi < p.bt_stride ? p.block_table[(size_t)b * p.bt_stride + pi] : -1;
+    if (page >= 0 && page < p.n_pages) return page * p.page_size + c0 % p.page_size;
+    if (report) fdl::raise_error(p.err, FDL_DEVERR_INDEX);
+    return p.n_slots;
+  };
+
   // ---------------------------------------------------------------- setup
+  const int pre = min(n_my, kStages);  // pass-A key tiles issued before the CTA barrier
   if (threadIdx.x == 0) {
     tc::mbar_init(q_full, 1);
     for (int s = 0; s < kStages; ++s) {
@@ -251,36 +306,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc::mbar_init(p_full, 8);
     tc::mbar_init(pv_done, 1);
-    tc::mbar_init(ml_ready, 128 * C);
+    tc::mbar_init(ml_ready, 4 * C);  // the four column-half-0 warps of every split
     *abort_flag = 0;
     tc::fence_mbar_init();
+    // Q and the first ring of key tiles need no free slot: the producer (this
+    // thread) issues them now, so the loads overlap the rest of the setup
+    if (n_my > 0) {
+      tc::prefetch_tensormap(&tm_q);
+      tc::prefetch_tensormap(&tm_k);
+      tc::prefetch_tensormap(&tm_v);
+      tc::mbar_arrive_expect_tx(q_full, Q_BYTES);
+      tc::tma_load_2d(sq, &tm_q, h * kHD, q0, q_full);
+      tc::tma_load_2d(sq + Q_BYTES / 2, &tm_q, h * kHD + 64, q0, q_full);
+      for (int lc = 0; lc < pre; ++lc) {
+        const int slot = tile_slot(t0 + lc, true);
+        uint8_t* st = ring + lc * STAGE_BYTES;
+        tc::mbar_arrive_expect_tx(&kv_full[lc], KT_BYTES);
+        tc::tma_load_2d(st, &tm_k, h * kHD, slot, &kv_full[lc]);
+        tc::tma_load_2d(st + KT_BYTES / 2, &tm_k, h * kHD + 64, slot, &kv_full[lc]);
+      }
+    }
   }
   if (warp == 1) {
     tc::tmem_alloc(tmem_slot, 256);
     tc::tmem_relinquish();
   }
-  for (int r = threadIdx.x; r < kBM; r += kThreads) {
-    int k = -1;
-    if (r < qlen) {
-      k = p.row_kind[q0 + r];
-      if (k >= 2 && ((k - 2) >> 1) >= m_search) {
-        fdl::raise_error(p.err, FDL_DEVERR_SHAPE);
-        k = -1;
-      }
-    }
-    kinds[r] = k;
-  }
-  for (int w = threadIdx.x; w < p.bitmap_words; w += kThreads) bitmap[w] = 0u;
-  if (threadIdx.x < 64) colacc[threadIdx.x] = 0.f;
-  __syncthreads();
-  for (int j = threadIdx.x; j < m_search; j += kThreads) {
-    const int s = p.search_pos[(size_t)b * p.search_ld + j];
-    if (s >= 0 && s < kvl && (s >> 5) < p.bitmap_words) atomicOr(&bitmap[s >> 5], 1u << (s & 31));
-  }
   tc::fence_before_sync();
   __syncthreads();
-  if (C > 1) tc::cluster_sync();  // peers' barriers and buffers exist before any remote access
   tc::fence_after_sync();
+  // peers' barriers and buffers must exist before any remote access: every
+  // thread arrives now and waits just before its first remote access
+  if (C > 1) tc::cluster_arrive();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tm_o = tmem;            // columns [0, 128)
   const uint32_t tm_s = tmem + 128;      // two 64-column S buffers
@@ -289,26 +345,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && n_my > 0) {
-      tc::prefetch_tensormap(&tm_q);
-      tc::prefetch_tensormap(&tm_k);
-      tc::prefetch_tensormap(&tm_v);
-      tc::mbar_arrive_expect_tx(q_full, Q_BYTES);
-      tc::tma_load_2d(sq, &tm_q, h * kHD, q0, q_full);
-      tc::tma_load_2d(sq + Q_BYTES / 2, &tm_q, h * kHD + 64, q0, q_full);
-      int lc = 0;
+      int lc = pre;
       for (int pass = 0; pass < 2; ++pass) {
-        for (int j = t0; j < t1; ++j, ++lc) {
+        for (int j = pass == 0 ? t0 + pre : t0; j < t1; ++j, ++lc) {
           const int s = lc % kStages;
           const uint32_t ph = (uint32_t)(lc / kStages) & 1u;
           if (!tc::mbar_wait(&kv_empty[s], ph ^ 1u, abort_flag)) break;
-          // slot of the tile's first key; an unmapped page points past the
-          // cache so the TMA zero-fills the tile (and the error word says so)
-          const int c0 = j * kBN;
-          const int pi = c0 / p.page_size;
-          const int page = pi < p.bt_stride ? p.block_table[(size_t)b * p.bt_stride + pi] : -1;
-          int slot = p.n_slots;
-          if (page >= 0 && page < p.n_pages) slot = page * p.page_size + c0 % p.page_size;
-          else if (pass == 0) fdl::raise_error(p.err, FDL_DEVERR_INDEX);
+          const int slot = tile_slot(j, pass == 0);
           uint8_t* st = ring + s * STAGE_BYTES;
           tc::mbar_arrive_expect_tx(&kv_full[s], pass == 0 ? KT_BYTES : STAGE_BYTES);
           tc::tma_load_2d(st, &tm_k, h * kHD, slot, &kv_full[s]);
@@ -322,6 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
+    if (C > 1) tc::cluster_wait();  // matches the setup arrive
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n_my > 0) {
@@ -373,6 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
+    if (C > 1) tc::cluster_wait();  // matches the setup arrive
   }
 
   // ------------------------------------------------------------ softmax warps
@@ -386,6 +431,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int t_local = threadIdx.x - 64;  // 0..255 over the softmax warps
   float lse2 = -INFINITY;  // log2-domain log-sum-exp of this row over all splits
   if (warp >= 2) {
+    // row kinds and the search-position bitmap, read only by these warps
+    for (int r = t_local; r < kBM; r += 256) {
+      int k = -1;
+      if (r < qlen) {
+        k = p.row_kind[q0 + r];
+        if (k >= 2 && ((k - 2) >> 1) >= m_search) {
+          fdl::raise_error(p.err, FDL_DEVERR_SHAPE);
+          k = -1;
+        }
+      }
+      kinds[r] = k;
+    }
+    for (int w = t_local; w < p.bitmap_words; w += 256) bitmap[w] = 0u;
+    if (t_local < 64) colacc[t_local] = 0.f;
+    tc::named_bar(3, 256);
+    for (int j = t_local; j < m_search; j += 256) {
+      const int s = p.search_pos[(size_t)b * p.search_ld + j];
+      if (s >= 0 && s < kvl && (s >> 5) < p.bitmap_words) atomicOr(&bitmap[s >> 5], 1u << (s & 31));
+    }
+    tc::named_bar(3, 256);
     const int kind = kinds[row];
     float mrow = -INFINITY, lrow = 0.f;
     int sc = 0;
@@ -441,11 +506,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // ---- combine (max, sum) over the cluster
     if (C > 1) {
+      tc::cluster_wait();  // peers have initialised their barriers (setup arrive)
       if (ch == 0) {
         // push this row's (max, sum) into every split, then release-arrive there
         const uint32_t mine = tc::smem_addr(ml + ((size_t)rank * kBM + row) * 2);
         for (int r = 0; r < C; ++r) st_cluster_v2(tc::map_cluster(mine, (uint32_t)r), mrow, lrow);
-        for (int r = 0; r < C; ++r) mbar_arrive_remote(ml_ready, (uint32_t)r);
+        // one release-arrive per warp and destination: every lane's remote
+        // stores are ordered before lane 0's arrive by its cluster-scope
+        // fence and the warp barrier
+        fence_acq_rel_cluster();
+        __syncwarp();
+        if (lane == 0)
+          for (int r = 0; r < C; ++r) mbar_arrive_remote(ml_ready, (uint32_t)r);
       }
       mbar_wait_cluster(ml_ready, 0, abort_flag);
       float mm = -INFINITY;
@@ -589,30 +661,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc::cluster_sync();
     if (warp >= 2) {
-      const int rows_per = kBM / C;
       const uint32_t base = tc::smem_addr(ostage);
-      for (int e = t_local; e < rows_per * (kHD / 4); e += 256) {
-        const int r = (int)rank * rows_per + e / (kHD / 4);
-        const int col = (e % (kHD / 4)) * 4;
-        float4 v[kMaxC];
-#pragma unroll
-        for (int src = 0; src < kMaxC; ++src)
-          if (src < C) v[src] = ld_cluster_v4(tc::map_cluster(base + (uint32_t)(r * kOStride + col) * 4u, (uint32_t)src));
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int src = 0; src < kMaxC; ++src)
-          if (src < C) {
-            acc.x += v[src].x;
-            acc.y += v[src].y;
-            acc.z += v[src].z;
-            acc.w += v[src].w;
-          }
-        if (r < qlen && !*abort_flag) {
-          __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
-          uint2 w = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
-          *reinterpret_cast<uint2*>(p.o + (size_t)(q0 + r) * p.d + h * kHD + col) = w;
-        }
-      }
+      const bool ab = *abort_flag != 0;
+      if (C == 2) merge_o<2>(p, base, rank, t_local, q0, qlen, h, ab);
+      else if (C == 4) merge_o<4>(p, base, rank, t_local, q0, qlen, h, ab);
+      else merge_o<8>(p, base, rank, t_local, q0, qlen, h, ab);
     }
     tc::cluster_sync();  // peers finished reading this CTA's staged O
   }

@@ -100,8 +100,6 @@ fdl_status fdl_create(const fdl_config* cfg, void* cuda_stream, fdl_ctx** out) {
   e = e ? e : cudaMalloc(&ctx->tickets, 8 * sizeof(unsigned));
   ctx->row_slots = 8192;
   e = e ? e : cudaMalloc(&ctx->row_part, (size_t)ctx->row_slots * 3 * sizeof(float));
-  e = e ? e : cudaMalloc(&ctx->row_tickets, (size_t)ctx->row_slots * sizeof(unsigned));
-  e = e ? e : cudaMemset(ctx->row_tickets, 0, (size_t)ctx->row_slots * sizeof(unsigned));
   if (cfg->dtype == FDL_BF16) {
     ctx->qkv_partial_floats = fdl_qkv_partial_floats(ctx->num_sms);
     ctx->qkv_tickets = 4 * ctx->num_sms;
@@ -130,7 +128,6 @@ void fdl_destroy(fdl_ctx* ctx) {
   cudaFree(ctx->n_masked);
   cudaFree(ctx->tickets);
   cudaFree(ctx->row_part);
-  cudaFree(ctx->row_tickets);
   cudaFree(ctx->qkv_partials);
   cudaFree(ctx->qkv_ticket_buf);
   free(ctx);

@@ -97,6 +97,7 @@ __global__ void __launch_bounds__(kThreads, BN == 64 ? 2 : 1)
   const int section = f0 / p.d;  // 0 = Q, 1 = K, 2 = V (tiles never straddle)
   const int kb0 = (int)(rank * p.nkb / ks), kb1 = (int)((rank + 1) * p.nkb / ks);
 
+  const int pre = min(kb1 - kb0, C::STAGES);  // loads issued before the CTA barrier
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       tc::mbar_init(&full[s], 1);
@@ -106,36 +107,21 @@ __global__ void __launch_bounds__(kThreads, BN == 64 ? 2 : 1)
     *abort_flag = 0;
     *is_last = ks == 1;
     tc::fence_mbar_init();
+    // The first ring of loads needs no free slot: the producer (this thread)
+    // issues it before the CTA barrier, so the weight stream starts while
+    // the other warps are still setting up.
+    tc::prefetch_tensormap(&tmap_w);
+    tc::prefetch_tensormap(&tmap_x);
+    for (int it = 0; it < pre; ++it) {
+      uint8_t* a = pipe + it * C::STAGE_BYTES;
+      tc::mbar_arrive_expect_tx(&full[it], C::STAGE_BYTES);
+      tc::tma_load_2d(a, &tmap_w, (kb0 + it) * kBK, f0, &full[it]);
+      tc::tma_load_2d(a + C::A_BYTES, &tmap_x, (kb0 + it) * kBK, tile_r * BN, &full[it]);
+    }
   }
   if (warp == 1) {
     tc::tmem_alloc(tmem_slot, BN);
     tc::tmem_relinquish();
-  }
-  if (warp >= 2) {
-    // per-column (query row) destination and RoPE position
-    for (int c = threadIdx.x - 64; c < BN; c += kEpiThreads) {
-      const int r = tile_r * BN + c;
-      int pos = -1;
-      long long dst = -1;
-      if (r < p.R) {
-        pos = p.row_rope_pos[r];
-        if (pos < 0 || pos >= p.rope_positions) {
-          fdl::raise_error(p.err, FDL_DEVERR_INDEX);
-          pos = -1;
-        } else if (section == 0) {
-          dst = (long long)r * p.d + f0;
-        } else {
-          const int cp = p.row_cache_pos[r];
-          if (cp >= 0) {
-            long long slot = fdl::cache_slot(p.block_table, p.bt_stride, p.page_size, p.n_pages, p.row_seq[r], cp,
-                                             p.err);
-            if (slot >= 0) dst = slot * p.d + (f0 - section * p.d);
-          }
-        }
-      }
-      col_pos[c] = pos;
-      col_dst[c] = pos >= 0 ? dst : -1;
-    }
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -144,10 +130,8 @@ __global__ void __launch_bounds__(kThreads, BN == 64 ? 2 : 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      tc::prefetch_tensormap(&tmap_w);
-      tc::prefetch_tensormap(&tmap_x);
-      int it = 0;
-      for (int kb = kb0; kb < kb1; ++kb, ++it) {
+      int it = pre;
+      for (int kb = kb0 + pre; kb < kb1; ++kb, ++it) {
         const int s = it % C::STAGES;
         const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
         if (!tc::mbar_wait(&empty[s], ph ^ 1u, abort_flag)) break;
@@ -188,6 +172,32 @@ __global__ void __launch_bounds__(kThreads, BN == 64 ? 2 : 1)
     }
     __syncwarp();
   } else {
+    // per-column (query row) destination and RoPE position, computed while
+    // the main loop streams (only the epilogue warps read them)
+    for (int c = threadIdx.x - 64; c < BN; c += kEpiThreads) {
+      const int r = tile_r * BN + c;
+      int pos = -1;
+      long long dst = -1;
+      if (r < p.R) {
+        pos = p.row_rope_pos[r];
+        if (pos < 0 || pos >= p.rope_positions) {
+          fdl::raise_error(p.err, FDL_DEVERR_INDEX);
+          pos = -1;
+        } else if (section == 0) {
+          dst = (long long)r * p.d + f0;
+        } else {
+          const int cp = p.row_cache_pos[r];
+          if (cp >= 0) {
+            long long slot = fdl::cache_slot(p.block_table, p.bt_stride, p.page_size, p.n_pages, p.row_seq[r], cp,
+                                             p.err);
+            if (slot >= 0) dst = slot * p.d + (f0 - section * p.d);
+          }
+        }
+      }
+      col_pos[c] = pos;
+      col_dst[c] = pos >= 0 ? dst : -1;
+    }
+    tc::named_bar(1, kEpiThreads);
     tc::mbar_wait(tmem_full, 0, abort_flag);
     tc::fence_after_sync();
   }
@@ -197,41 +207,23 @@ __global__ void __launch_bounds__(kThreads, BN == 64 ? 2 : 1)
   const uint32_t t_lane = tmem + ((uint32_t)(q * 32) << 16);
   const bool epi = warp >= 2 && !*abort_flag;
 
-  if (ks > 1 && epi) {
-    // publish this split's partial tile, then take a ticket
-    float* mine = p.partials + ((size_t)tile_lin * ks + rank) * BN * kBM;
-    for (int c0 = 0; c0 < BN; c0 += 32) {
-      float v[32];
-      tc::tmem_ld_32x32b_x32(t_lane + c0, v);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) __stcg(mine + (c0 + j) * kBM + t, v[j]);
-    }
-    __threadfence();
-    tc::named_bar(1, kEpiThreads);
-    if (t == 0) {
-      const unsigned prev = atomicAdd(p.tickets + tile_lin, 1u);
-      *is_last = prev == (unsigned)(ks - 1);
-      if (*is_last) p.tickets[tile_lin] = 0u;  // every split has arrived: reset for the next launch
-    }
-    tc::named_bar(1, kEpiThreads);
-    if (*is_last) __threadfence();
-  }
-
-  if (epi && *is_last) {
+  if (epi) {
     const int half = p.hd / 2;
     const int i = (f0 + t) % p.hd;
     const int jj = i % half;
     const bool low = i < half;
     const int partner = t ^ half;
     __nv_bfloat16* out = section == 0 ? p.q_out : (section == 1 ? p.k_cache : p.v_cache);
-    __nv_bfloat16* obuf = reinterpret_cast<__nv_bfloat16*>(xbuf);  // [16][128] bf16, aliases xbuf
-    const float* parts = p.partials + (size_t)tile_lin * ks * BN * kBM;
-    constexpr int CH = 16;  // columns per epilogue chunk
-    for (int c0 = 0; c0 < BN; c0 += CH) {
-      // issue this chunk's RoPE table loads first so their latency overlaps
-      // the TMEM and partial-sum loads (one round trip per chunk)
+    __nv_bfloat16* obuf = reinterpret_cast<__nv_bfloat16*>(xbuf);  // [32][128] bf16, aliases xbuf
+    constexpr int CH = 16;  // columns per TMEM chunk
+
+    // Columns c0..c0+CH-1 of this thread's output feature from TMEM, with
+    // RoPE applied (each pair's partner is exchanged through shared memory).
+    // RoPE is linear, so a K split may rotate its own partial sum.
+    auto load_rotated = [&](int c0, float (&v)[CH]) {
       float cs[CH], sn[CH];
       if (section < 2) {
+        // table loads first, so their latency overlaps the TMEM load
 #pragma unroll
         for (int j = 0; j < CH; ++j) {
           const int pos = max(col_pos[c0 + j], 0);
@@ -239,27 +231,8 @@ __global__ void __launch_bounds__(kThreads, BN == 64 ? 2 : 1)
           sn[j] = __ldg(p.rope_sin + (size_t)pos * half + jj);
         }
       }
-      float v[CH];
       tc::tmem_ld_32x32b_x16(t_lane + c0, v);
-      if (ks > 1) {
-        // fixed split order: sum = p_0 + p_1 + ... (own split from TMEM)
-        float acc[CH];
-#pragma unroll
-        for (int j = 0; j < CH; ++j) acc[j] = 0.f;
-        for (int sp = 0; sp < ks; ++sp) {
-          if (sp == (int)rank) {
-#pragma unroll
-            for (int j = 0; j < CH; ++j) acc[j] += v[j];
-          } else {
-            const float* ps = parts + (size_t)sp * BN * kBM;
-#pragma unroll
-            for (int j = 0; j < CH; ++j) acc[j] += __ldcg(ps + (c0 + j) * kBM + t);
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < CH; ++j) v[j] = acc[j];
-      }
-      tc::named_bar(1, kEpiThreads);  // previous chunk's readers of xbuf/obuf are done
+      tc::named_bar(1, kEpiThreads);  // earlier readers of xbuf / obuf are done
       if (section < 2) {
 #pragma unroll
         for (int j = 0; j < CH; ++j) xbuf[t * kXStride + j] = v[j];
@@ -269,19 +242,73 @@ __global__ void __launch_bounds__(kThreads, BN == 64 ? 2 : 1)
           const float other = xbuf[partner * kXStride + j];
           v[j] = low ? (v[j] * cs[j] - other * sn[j]) : (other * sn[j] + v[j] * cs[j]);
         }
-        tc::named_bar(1, kEpiThreads);  // exchange reads done before obuf overwrites xbuf
+        tc::named_bar(1, kEpiThreads);  // exchange reads done before xbuf is reused
       }
-#pragma unroll
-      for (int j = 0; j < CH; ++j) obuf[j * kBM + t] = __float2bfloat16_rn(v[j]);
-      tc::named_bar(1, kEpiThreads);
-      // CH rows x 256 bytes: 16-byte chunks, consecutive threads on consecutive chunks
-#pragma unroll
-      for (int u = 0; u < CH * 16 / kEpiThreads; ++u) {
-        const int id = t + kEpiThreads * u;
+    };
+    // nrows query rows x 256 bytes from obuf: 16-byte chunks, consecutive
+    // threads on consecutive chunks
+    auto store_rows = [&](int c0, int nrows) {
+      for (int id = t; id < nrows * 16; id += kEpiThreads) {
         const int j = id >> 4, part = id & 15;
         const long long dst = col_dst[c0 + j];
         if (dst >= 0)
           *reinterpret_cast<int4*>(out + dst + part * 8) = *reinterpret_cast<const int4*>(obuf + j * kBM + part * 8);
+      }
+    };
+
+    if (ks == 1) {
+      for (int c0 = 0; c0 < BN; c0 += CH) {
+        float v[CH];
+        load_rotated(c0, v);
+#pragma unroll
+        for (int j = 0; j < CH; ++j) obuf[j * kBM + t] = __float2bfloat16_rn(v[j]);
+        tc::named_bar(1, kEpiThreads);
+        store_rows(c0, CH);
+      }
+    } else {
+      // publish this split's rotated partial tile, then take a ticket
+      float* mine = p.partials + ((size_t)tile_lin * ks + rank) * BN * kBM;
+      for (int c0 = 0; c0 < BN; c0 += CH) {
+        float v[CH];
+        load_rotated(c0, v);
+#pragma unroll
+        for (int j = 0; j < CH; ++j) __stcg(mine + (c0 + j) * kBM + t, v[j]);
+      }
+      __threadfence();
+      tc::named_bar(1, kEpiThreads);
+      if (t == 0) {
+        const unsigned prev = atomicAdd(p.tickets + tile_lin, 1u);
+        *is_last = prev == (unsigned)(ks - 1);
+        if (*is_last) p.tickets[tile_lin] = 0u;  // every split has arrived: reset for the next launch
+      }
+      tc::named_bar(1, kEpiThreads);
+      if (*is_last) {
+        // sum the ks rotated partials in split order (all loads of a chunk
+        // in flight together), round to bf16 and store
+        __threadfence();
+        const float* parts = p.partials + (size_t)tile_lin * ks * BN * kBM;
+        constexpr int CHM = 32;
+        const size_t split_stride = (size_t)BN * kBM;
+        for (int c0 = 0; c0 < BN; c0 += CHM) {
+          float a0[CHM], a1[CHM], a2[CHM];
+#pragma unroll
+          for (int j = 0; j < CHM; ++j) a0[j] = __ldcg(parts + (c0 + j) * kBM + t);
+#pragma unroll
+          for (int j = 0; j < CHM; ++j) a1[j] = __ldcg(parts + split_stride + (c0 + j) * kBM + t);
+#pragma unroll
+          for (int j = 0; j < CHM; ++j) a2[j] = ks > 2 ? __ldcg(parts + 2 * split_stride + (c0 + j) * kBM + t) : 0.f;
+#pragma unroll
+          for (int j = 0; j < CHM; ++j) a0[j] = (a0[j] + a1[j]) + a2[j];
+          for (int sp = 3; sp < ks; ++sp) {
+#pragma unroll
+            for (int j = 0; j < CHM; ++j) a0[j] += __ldcg(parts + sp * split_stride + (c0 + j) * kBM + t);
+          }
+          tc::named_bar(1, kEpiThreads);  // earlier readers of xbuf / obuf are done
+#pragma unroll
+          for (int j = 0; j < CHM; ++j) obuf[j * kBM + t] = __float2bfloat16_rn(a0[j]);
+          tc::named_bar(1, kEpiThreads);
+          store_rows(c0, CHM);
+        }
       }
     }
   }

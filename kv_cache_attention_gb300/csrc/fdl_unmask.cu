@@ -12,12 +12,12 @@
 // split across independent CTAs; every CTA streams its slice with 128-bit
 // loads, keeps (max, sum exp, argmax) per thread over register blocks (tree
 // max, then the sum of exponentials with four accumulators), and merges with
-// warp shuffles. Split CTAs publish their partial to a workspace slot and the
-// row's last CTA to arrive (a ticket it resets) loads all partials at once
-// and merges them by a fixed xor tree, so the result does not depend on
-// timing. The last row to finish (a
-// second ticket) takes the per-sequence decisions: one launch per phase, and
-// nothing ever waits on another CTA.
+// warp shuffles. Each CTA publishes its slice partial to a workspace slot (a
+// row in one slice writes its confidence directly) and takes one ticket for
+// the whole grid; the last CTA to arrive merges every row's partials by a
+// fixed xor tree, so the result does not depend on timing, and takes the
+// per-sequence decisions: one launch per phase, and nothing ever waits on
+// another CTA.
 #include "fdl_internal.cuh"
 
 namespace {
@@ -184,8 +184,7 @@ struct RowParams {
   float* out_conf;
   int* out_arg;
   float* part;                 // [n_rows * split][3] split partials (max, sum, argmax bits)
-  unsigned* row_ticket;        // [n_rows] per-row arrival counters, zero between calls
-  unsigned* ticket;
+  unsigned* ticket;            // arrival counter of the whole grid, zero between calls
   unsigned* err;
   // unmask decisions
   int phase;         // 0 = unmask, 1 = verify
@@ -205,27 +204,38 @@ struct RowParams {
 };
 
 // Per-sequence decisions of the unmask phase; one warp per sequence. The
-// rows' confidences, positions and sequence ids are first staged in shared
-// memory (up to kStageRows rows) so the ranking loops never wait on L2.
+// rows' confidences and positions are first staged in shared memory (up to
+// kStageRows rows), together with each sequence's row range (up to
+// kStageSeqs sequences), so no step waits on a chain of memory loads: the
+// ranking compares a sequence's rows in registers through warp shuffles.
 constexpr int kStageRows = 2048;
+constexpr int kStageSeqs = 1024;
 
 __device__ void decide_unmask(const RowParams& p) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const int R = p.n_rows;
   __shared__ float s_conf[kStageRows];
   __shared__ int s_pos[kStageRows];
-  __shared__ int s_seq[kStageRows];
+  __shared__ int s_lo[kStageSeqs], s_hi[kStageSeqs];
   __shared__ int bad;
   const bool staged = R <= kStageRows;
+  const bool ranged = staged && p.B <= kStageSeqs;
   if (threadIdx.x == 0) bad = 0;
+  if (ranged)
+    for (int b = threadIdx.x; b < p.B; b += blockDim.x) s_lo[b] = s_hi[b] = 0;
   __syncthreads();
   for (int r = threadIdx.x; r < R; r += blockDim.x) {
     const int sq = p.row_seq[r];
-    if (sq < 0 || sq >= p.B || (r + 1 < R && p.row_seq[r + 1] < sq)) bad = 1;
+    const int prev = r > 0 ? p.row_seq[r - 1] : -1;
+    const int next = r + 1 < R ? p.row_seq[r + 1] : p.B;
+    if (sq < 0 || sq >= p.B || next < sq) bad = 1;
     if (staged) {
       s_conf[r] = __ldcg(p.out_conf + r);
       s_pos[r] = p.row_pos[r];
-      s_seq[r] = sq;
+    }
+    if (ranged && sq >= 0 && sq < p.B) {  // rows are sorted by sequence (checked)
+      if (prev != sq) s_lo[sq] = r;
+      if (next != sq) s_hi[sq] = r + 1;
     }
   }
   __syncthreads();
@@ -235,16 +245,17 @@ __device__ void decide_unmask(const RowParams& p) {
   }
   auto conf = [&](int r) { return staged ? s_conf[r] : __ldcg(p.out_conf + r); };
   auto pos = [&](int r) { return staged ? s_pos[r] : p.row_pos[r]; };
-  auto seq = [&](int r) { return staged ? s_seq[r] : p.row_seq[r]; };
   for (int b = warp; b < p.B; b += nw) {
-    // rows of b: [lo, hi) by binary search on the sorted row_seq
-    int lo = 0, hi = R;
-    {
+    int lo, hi;
+    if (ranged) {
+      lo = s_lo[b];
+      hi = s_hi[b];
+    } else {  // rows of b: [lo, hi) by binary search on the sorted row_seq
       int a = 0, z = R;
-      while (a < z) { int m = (a + z) >> 1; if (seq(m) < b) a = m + 1; else z = m; }
+      while (a < z) { int m = (a + z) >> 1; if (p.row_seq[m] < b) a = m + 1; else z = m; }
       lo = a;
       z = R;
-      while (a < z) { int m = (a + z) >> 1; if (seq(m) <= b) a = m + 1; else z = m; }
+      while (a < z) { int m = (a + z) >> 1; if (p.row_seq[m] <= b) a = m + 1; else z = m; }
       hi = a;
     }
     // eps rule
@@ -270,22 +281,33 @@ __device__ void decide_unmask(const RowParams& p) {
       forced = br;
     }
     for (int r = lo + lane; r < hi; r += 32) p.commit[r] = (conf(r) >= p.eps || r == forced) ? 1 : 0;
-    // rank the uncommitted rows by (conf desc, pos asc)
+    // rank the uncommitted rows by (conf desc, pos asc): lane l holds row
+    // a0 + l and compares it with every row of the sequence, 32 at a time,
+    // through shuffles
     int n_unc = 0;
-    for (int r = lo + lane; r < hi; r += 32) {
-      const float c = conf(r);
-      const bool unc = !(c >= p.eps) && r != forced;
-      n_unc += unc ? 1 : 0;
-      if (!unc) continue;
-      const int ps = pos(r);
+    for (int a0 = lo; a0 < hi; a0 += 32) {
+      const int ra = a0 + lane;
+      const bool va = ra < hi;
+      const float ca = va ? conf(ra) : 0.f;
+      const int pa = va ? pos(ra) : 0;
+      const bool ua = va && !(ca >= p.eps) && ra != forced;
       int rank = 0;
-      for (int o = lo; o < hi; ++o) {
-        const float co = conf(o);
-        if (co >= p.eps || o == forced) continue;
-        const int po = pos(o);
-        rank += (co > c || (co == c && po < ps)) ? 1 : 0;
+      for (int b0 = lo; b0 < hi; b0 += 32) {
+        const int rb = b0 + lane;
+        const bool vb = rb < hi;
+        const float cb = vb ? conf(rb) : 0.f;
+        const int pb = vb ? pos(rb) : 0;
+        const int ub = (vb && !(cb >= p.eps) && rb != forced) ? 1 : 0;
+#pragma unroll 8
+        for (int k = 0; k < 32; ++k) {
+          const float co = __shfl_sync(0xffffffffu, cb, k);
+          const int po = __shfl_sync(0xffffffffu, pb, k);
+          const int uo = __shfl_sync(0xffffffffu, ub, k);
+          rank += (uo && (co > ca || (co == ca && po < pa))) ? 1 : 0;
+        }
       }
-      if (rank < p.max_search) p.search_rows[b * p.max_search + rank] = r;
+      n_unc += ua ? 1 : 0;
+      if (ua && rank < p.max_search) p.search_rows[b * p.max_search + rank] = ra;
     }
     for (int off = 16; off; off >>= 1) n_unc += __shfl_xor_sync(0xffffffffu, n_unc, off);
     const int ns = min(n_unc, p.max_search);
@@ -325,13 +347,16 @@ __global__ void __launch_bounds__(kThreads) row_reduce_kernel(RowParams p) {
   __shared__ unsigned go;
   const int row = blockIdx.x / p.split;
   const int sp = blockIdx.x % p.split;
-  bool valid = row < p.n_rows;
-  if (valid && p.phase == 1) {
-    int b = row / p.max_search, j = row % p.max_search;
-    valid = j < p.n_search[b];
-  }
-  if (!valid && sp != 0) return;  // an idle row takes one global ticket, from split 0
-  Stat st{-INFINITY, 0.f, 0x7fffffff};
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // verify phase: row r = b*max_search + j is valid only when j < n_search[b]
+  auto row_valid = [&](int r) {
+    if (r >= p.n_rows) return false;
+    if (p.phase == 1) return r % p.max_search < p.n_search[r / p.max_search];
+    return true;
+  };
+  const bool valid = row_valid(row);
+  const Stat none{-INFINITY, 0.f, 0x7fffffff};
+  Stat st = none;
   if (valid) {
     const T* base = reinterpret_cast<const T*>(p.logits) + (size_t)row * p.vocab;
     const int lo = sp * p.chunk;
@@ -339,57 +364,62 @@ __global__ void __launch_bounds__(kThreads) row_reduce_kernel(RowParams p) {
     if (lo < hi) st = slice_stat<T>(base, lo, hi, p.vec_ok);
   }
   for (int off = 16; off; off >>= 1) st = shfl_merge(st, off);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (lane == 0) warp_stat[warp] = st;
   __syncthreads();
   if (warp == 0) {
     // block statistic: lanes 0..7 hold the warps' statistics, merged by a
     // fixed xor tree (lane 0 ends with the result)
-    const Stat none{-INFINITY, 0.f, 0x7fffffff};
     Stat acc = lane < kThreads / 32 ? warp_stat[lane] : none;
     for (int off = kThreads / 64; off; off >>= 1) acc = shfl_merge(acc, off);
-    unsigned proceed = 1u;
-    if (valid && p.split > 1) {
-      if (lane == 0) {
-        float* slot = p.part + ((size_t)row * p.split + sp) * 3;
-        __stcg(slot, acc.m);
-        __stcg(slot + 1, acc.s);
-        __stcg(slot + 2, __int_as_float(acc.i));
-        __threadfence();
-        const unsigned t = atomicAdd(p.row_ticket + row, 1u);
-        proceed = t == (unsigned)(p.split - 1) ? 1u : 0u;
-        if (proceed) p.row_ticket[row] = 0u;  // all splits arrived: ready for the next call
-      }
-      proceed = __shfl_sync(0xffffffffu, proceed, 0);
-      if (proceed) {
-        // the row's last CTA: lane k loads split k's partial (all loads in
-        // flight at once) and a fixed xor tree merges them, so the result
-        // does not depend on the order in which the splits arrived
-        __threadfence();
-        acc = none;
-        if (lane < p.split) {
-          const float* o = p.part + ((size_t)row * p.split + lane) * 3;
-          acc = Stat{__ldcg(o), __ldcg(o + 1), __float_as_int(__ldcg(o + 2))};
-        }
-        for (int off = kMaxSplit / 2; off; off >>= 1) acc = shfl_merge(acc, off);
-      }
-    }
     if (lane == 0) {
-      if (proceed) {
-        if (valid) {
+      if (valid) {
+        if (p.split > 1) {
+          float* slot = p.part + ((size_t)row * p.split + sp) * 3;
+          __stcg(slot, acc.m);
+          __stcg(slot + 1, acc.s);
+          __stcg(slot + 2, __int_as_float(acc.i));
+        } else {
           p.out_conf[row] = 1.f / acc.s;  // acc.s = sum exp(x - max) >= 1
           p.out_arg[row] = acc.i;
         }
-        __threadfence();
-        const unsigned t = atomicAdd(p.ticket, 1u);
-        proceed = (t == (unsigned)p.n_rows - 1u) ? 2u : 0u;
       }
-      go = proceed;
+      // one ticket for the whole grid: the last CTA finishes every row
+      __threadfence();
+      const unsigned t = atomicAdd(p.ticket, 1u);
+      go = t == gridDim.x - 1u ? 1u : 0u;
     }
   }
   __syncthreads();
-  if (go != 2u) return;
+  if (!go) return;
   __threadfence();
+  if (p.split > 1) {
+    // merge each valid row's slice partials: a warp takes 4 rows per round
+    // with all their loads in flight, lane k holding slice k; a fixed xor
+    // tree merges them, so the result does not depend on arrival order
+    constexpr int kRowsPerWarp = 4;
+    for (int r0 = warp * kRowsPerWarp; r0 < p.n_rows; r0 += (kThreads / 32) * kRowsPerWarp) {
+      Stat a[kRowsPerWarp];
+      bool v[kRowsPerWarp];
+#pragma unroll
+      for (int u = 0; u < kRowsPerWarp; ++u) {
+        v[u] = row_valid(r0 + u);
+        a[u] = none;
+        if (v[u] && lane < p.split) {
+          const float* o = p.part + ((size_t)(r0 + u) * p.split + lane) * 3;
+          a[u] = Stat{__ldcg(o), __ldcg(o + 1), __float_as_int(__ldcg(o + 2))};
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kRowsPerWarp; ++u) {
+        for (int off = kMaxSplit / 2; off; off >>= 1) a[u] = shfl_merge(a[u], off);
+        if (v[u] && lane == 0) {
+          p.out_conf[r0 + u] = 1.f / a[u].s;
+          p.out_arg[r0 + u] = a[u].i;
+        }
+      }
+    }
+    __syncthreads();  // this CTA's confidences are written before the decisions read them
+  }
   if (p.phase == 0) decide_unmask(p);
   else decide_verify(p);
   if (threadIdx.x == 0) *p.ticket = 0u;  // ready for the next call
@@ -410,7 +440,6 @@ cudaError_t launch_phase(fdl_ctx* ctx, RowParams p) {
   p.split = split;
   p.chunk = chunk;
   p.part = ctx->row_part;
-  p.row_ticket = ctx->row_tickets;
   p.vec_ok = ((reinterpret_cast<uintptr_t>(p.logits) & 15) == 0) && ((size_t)V * sizeof(T)) % 16 == 0;
   row_reduce_kernel<T><<<(unsigned)(p.n_rows * split), kThreads, 0, ctx->stream>>>(p);
   return cudaGetLastError();

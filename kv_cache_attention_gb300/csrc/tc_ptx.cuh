@@ -175,6 +175,16 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
   return r;
 }
 
+// split cluster barrier: every thread arrives (releasing its prior writes,
+// e.g. mbarrier initialisation) and later waits (acquiring the peers')
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }

@@ -165,13 +165,17 @@ def test_chain_full_size():
     # atomics, whose order varies between runs, so a re-run reproduces the
     # scores to within that reassociation error rather than bit for bit. The
     # re-run is fed the first run's tracked sets (so a near-tie cannot fork
-    # the chain) and must give the same sets wherever the k-th and (k+1)-th
-    # scores are further apart than that error.
+    # the chain). Its top-k must hold the same positions wherever the k-th
+    # and (k+1)-th scores are further apart than that error, and rank j must
+    # hold a score within that error of the first run's rank j (near-equal
+    # scores may trade places).
+    tol = 4e-6
     first = run(True)
     second = run(False, forced=first)
     for (s1, i1), (s2, i2) in zip(first, second):
         np.testing.assert_allclose(s1, s2, rtol=0, atol=1e-6)
         for b in range(B):
-            if H.topk_margin_ok(s1[b], e["eligible"][b], N, k, 4e-6):
-                assert i1[b].tolist() == i2[b].tolist()
+            if H.topk_margin_ok(s1[b], e["eligible"][b], N, k, tol):
+                assert sorted(i1[b].tolist()) == sorted(i2[b].tolist())
+            np.testing.assert_allclose(s1[b][i1[b]], s1[b][i2[b]], rtol=0, atol=tol)
     ctx.close()
