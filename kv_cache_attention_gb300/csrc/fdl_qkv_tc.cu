@@ -279,13 +279,15 @@ __global__ void __launch_bounds__(kThreads, BN == 64 ? 2 : 1)
       if (t == 0) {
         const unsigned prev = atomicAdd(p.tickets + tile_lin, 1u);
         *is_last = prev == (unsigned)(ks - 1);
-        if (*is_last) p.tickets[tile_lin] = 0u;  // every split has arrived: reset for the next launch
+        if (*is_last) {
+          p.tickets[tile_lin] = 0u;  // every split has arrived: reset for the next launch
+          __threadfence();           // acquire: the other splits' partials, for every thread after the barrier
+        }
       }
       tc::named_bar(1, kEpiThreads);
       if (*is_last) {
         // sum the ks rotated partials in split order (all loads of a chunk
         // in flight together), round to bf16 and store
-        __threadfence();
         const float* parts = p.partials + (size_t)tile_lin * ks * BN * kBM;
         constexpr int CHM = 32;
         const size_t split_stride = (size_t)BN * kBM;

@@ -213,27 +213,35 @@ constexpr int kStageSeqs = 1024;
 
 __device__ void decide_unmask(const RowParams& p) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const int R = p.n_rows;
+  // parameters used inside loops, read once into registers
+  const int R = p.n_rows, B = p.B, max_search = p.max_search;
+  const float eps = p.eps;
+  const bool force_progress = p.force_progress != 0;
+  const int* __restrict__ row_seq = p.row_seq;
+  const int* __restrict__ row_pos = p.row_pos;
+  const float* out_conf = p.out_conf;
+  unsigned char* __restrict__ commit = p.commit;
+  int* __restrict__ search_rows = p.search_rows;
   __shared__ float s_conf[kStageRows];
   __shared__ int s_pos[kStageRows];
   __shared__ int s_lo[kStageSeqs], s_hi[kStageSeqs];
   __shared__ int bad;
   const bool staged = R <= kStageRows;
-  const bool ranged = staged && p.B <= kStageSeqs;
+  const bool ranged = staged && B <= kStageSeqs;
   if (threadIdx.x == 0) bad = 0;
   if (ranged)
-    for (int b = threadIdx.x; b < p.B; b += blockDim.x) s_lo[b] = s_hi[b] = 0;
+    for (int b = threadIdx.x; b < B; b += blockDim.x) s_lo[b] = s_hi[b] = 0;
   __syncthreads();
   for (int r = threadIdx.x; r < R; r += blockDim.x) {
-    const int sq = p.row_seq[r];
-    const int prev = r > 0 ? p.row_seq[r - 1] : -1;
-    const int next = r + 1 < R ? p.row_seq[r + 1] : p.B;
-    if (sq < 0 || sq >= p.B || next < sq) bad = 1;
+    const int sq = row_seq[r];
+    const int prev = r > 0 ? row_seq[r - 1] : -1;
+    const int next = r + 1 < R ? row_seq[r + 1] : B;
+    if (sq < 0 || sq >= B || next < sq) bad = 1;
     if (staged) {
-      s_conf[r] = __ldcg(p.out_conf + r);
-      s_pos[r] = p.row_pos[r];
+      s_conf[r] = __ldcg(out_conf + r);
+      s_pos[r] = row_pos[r];
     }
-    if (ranged && sq >= 0 && sq < p.B) {  // rows are sorted by sequence (checked)
+    if (ranged && sq >= 0 && sq < B) {  // rows are sorted by sequence (checked)
       if (prev != sq) s_lo[sq] = r;
       if (next != sq) s_hi[sq] = r + 1;
     }
@@ -243,27 +251,27 @@ __device__ void decide_unmask(const RowParams& p) {
     if (threadIdx.x == 0) fdl::raise_error(p.err, FDL_DEVERR_SHAPE);
     return;
   }
-  auto conf = [&](int r) { return staged ? s_conf[r] : __ldcg(p.out_conf + r); };
-  auto pos = [&](int r) { return staged ? s_pos[r] : p.row_pos[r]; };
-  for (int b = warp; b < p.B; b += nw) {
+  auto conf = [&](int r) { return staged ? s_conf[r] : __ldcg(out_conf + r); };
+  auto pos = [&](int r) { return staged ? s_pos[r] : row_pos[r]; };
+  for (int b = warp; b < B; b += nw) {
     int lo, hi;
     if (ranged) {
       lo = s_lo[b];
       hi = s_hi[b];
     } else {  // rows of b: [lo, hi) by binary search on the sorted row_seq
       int a = 0, z = R;
-      while (a < z) { int m = (a + z) >> 1; if (p.row_seq[m] < b) a = m + 1; else z = m; }
+      while (a < z) { int m = (a + z) >> 1; if (row_seq[m] < b) a = m + 1; else z = m; }
       lo = a;
       z = R;
-      while (a < z) { int m = (a + z) >> 1; if (p.row_seq[m] <= b) a = m + 1; else z = m; }
+      while (a < z) { int m = (a + z) >> 1; if (row_seq[m] <= b) a = m + 1; else z = m; }
       hi = a;
     }
     // eps rule
     bool any = false;
-    for (int r = lo + lane; r < hi; r += 32) any |= conf(r) >= p.eps;
+    for (int r = lo + lane; r < hi; r += 32) any |= conf(r) >= eps;
     any = __any_sync(0xffffffffu, any);
     int forced = -1;
-    if (p.force_progress && !any && hi > lo) {
+    if (force_progress && !any && hi > lo) {
       // most confident row, lowest position on ties
       float bc = -1.f;
       int bp = 0x7fffffff, br = -1;
@@ -280,7 +288,7 @@ __device__ void decide_unmask(const RowParams& p) {
       }
       forced = br;
     }
-    for (int r = lo + lane; r < hi; r += 32) p.commit[r] = (conf(r) >= p.eps || r == forced) ? 1 : 0;
+    for (int r = lo + lane; r < hi; r += 32) commit[r] = (conf(r) >= eps || r == forced) ? 1 : 0;
     // rank the uncommitted rows by (conf desc, pos asc): lane l holds row
     // a0 + l and compares it with every row of the sequence, 32 at a time,
     // through shuffles
@@ -290,28 +298,37 @@ __device__ void decide_unmask(const RowParams& p) {
       const bool va = ra < hi;
       const float ca = va ? conf(ra) : 0.f;
       const int pa = va ? pos(ra) : 0;
-      const bool ua = va && !(ca >= p.eps) && ra != forced;
+      const bool ua = va && !(ca >= eps) && ra != forced;
       int rank = 0;
       for (int b0 = lo; b0 < hi; b0 += 32) {
         const int rb = b0 + lane;
         const bool vb = rb < hi;
         const float cb = vb ? conf(rb) : 0.f;
         const int pb = vb ? pos(rb) : 0;
-        const int ub = (vb && !(cb >= p.eps) && rb != forced) ? 1 : 0;
-#pragma unroll 8
-        for (int k = 0; k < 32; ++k) {
-          const float co = __shfl_sync(0xffffffffu, cb, k);
-          const int po = __shfl_sync(0xffffffffu, pb, k);
-          const int uo = __shfl_sync(0xffffffffu, ub, k);
-          rank += (uo && (co > ca || (co == ca && po < pa))) ? 1 : 0;
+        // an uncommitted row's key for the comparison; committed and absent
+        // rows take -1 (below every confidence) so they never outrank
+        const float kb = (vb && !(cb >= eps) && rb != forced) ? cb : -1.f;
+        // eight (key, position) pairs per round: their shuffles issue back to
+        // back, and the rolled loop keeps this one-off code small
+#pragma unroll 1
+        for (int k0 = 0; k0 < 32; k0 += 8) {
+          float co[8];
+          int po[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            co[k] = __shfl_sync(0xffffffffu, kb, k0 + k);
+            po[k] = __shfl_sync(0xffffffffu, pb, k0 + k);
+          }
+#pragma unroll
+          for (int k = 0; k < 8; ++k) rank += (co[k] > ca || (co[k] == ca && po[k] < pa)) ? 1 : 0;
         }
       }
       n_unc += ua ? 1 : 0;
-      if (ua && rank < p.max_search) p.search_rows[b * p.max_search + rank] = ra;
+      if (ua && rank < max_search) search_rows[b * max_search + rank] = ra;
     }
     for (int off = 16; off; off >>= 1) n_unc += __shfl_xor_sync(0xffffffffu, n_unc, off);
-    const int ns = min(n_unc, p.max_search);
-    for (int j = ns + lane; j < p.max_search; j += 32) p.search_rows[b * p.max_search + j] = -1;
+    const int ns = min(n_unc, max_search);
+    for (int j = ns + lane; j < max_search; j += 32) search_rows[b * max_search + j] = -1;
     if (lane == 0) p.n_search_out[b] = ns;
   }
 }
@@ -319,25 +336,34 @@ __device__ void decide_unmask(const RowParams& p) {
 // Per-sequence prefix walk of the verify phase; one warp per sequence.
 __device__ void decide_verify(const RowParams& p) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  for (int b = warp; b < p.B; b += nw) {
-    int n = p.n_search[b];
-    if (n < 0 || n > p.max_search) {
+  // parameters used inside loops, read once into registers
+  const int B = p.B, max_search = p.max_search;
+  const float gamma = p.gamma;
+  const int* __restrict__ n_search = p.n_search;
+  const int* __restrict__ draft_tok = p.draft_tok;
+  const int* out_arg = p.out_arg;
+  const float* out_conf = p.out_conf;
+  unsigned char* __restrict__ accept = p.accept;
+  int* __restrict__ n_accept = p.n_accept;
+  for (int b = warp; b < B; b += nw) {
+    int n = n_search[b];
+    if (n < 0 || n > max_search) {
       if (lane == 0) fdl::raise_error(p.err, FDL_DEVERR_SHAPE);
-      n = max(0, min(n, p.max_search));
+      n = max(0, min(n, max_search));
     }
     int stop = n;
     for (int j0 = 0; j0 < n && stop == n; j0 += 32) {
       int j = j0 + lane;
       bool ok = true;
       if (j < n) {
-        int r = b * p.max_search + j;
-        ok = (p.draft_tok[r] == __ldcg(p.out_arg + r)) && (__ldcg(p.out_conf + r) >= p.gamma);
+        int r = b * max_search + j;
+        ok = (draft_tok[r] == __ldcg(out_arg + r)) && (__ldcg(out_conf + r) >= gamma);
       }
       unsigned fails = __ballot_sync(0xffffffffu, !ok);
       if (fails) stop = j0 + __ffs(fails) - 1;
     }
-    for (int j = lane; j < p.max_search; j += 32) p.accept[b * p.max_search + j] = (j < stop) ? 1 : 0;
-    if (lane == 0) p.n_accept[b] = stop;
+    for (int j = lane; j < max_search; j += 32) accept[b * max_search + j] = (j < stop) ? 1 : 0;
+    if (lane == 0) n_accept[b] = stop;
   }
 }
 
@@ -349,9 +375,11 @@ __global__ void __launch_bounds__(kThreads) row_reduce_kernel(RowParams p) {
   const int sp = blockIdx.x % p.split;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   // verify phase: row r = b*max_search + j is valid only when j < n_search[b]
-  auto row_valid = [&](int r) {
-    if (r >= p.n_rows) return false;
-    if (p.phase == 1) return r % p.max_search < p.n_search[r / p.max_search];
+  const int n_rows_all = p.n_rows, phase = p.phase, ms_all = p.max_search;
+  const int* n_search_in = p.n_search;
+  auto row_valid = [=](int r) {
+    if (r >= n_rows_all) return false;
+    if (phase == 1) return r % ms_all < n_search_in[r / ms_all];
     return true;
   };
   const bool valid = row_valid(row);
@@ -387,34 +415,43 @@ __global__ void __launch_bounds__(kThreads) row_reduce_kernel(RowParams p) {
       __threadfence();
       const unsigned t = atomicAdd(p.ticket, 1u);
       go = t == gridDim.x - 1u ? 1u : 0u;
+      if (go) __threadfence();  // acquire: every CTA's results, for all threads after the barrier
     }
   }
   __syncthreads();
   if (!go) return;
-  __threadfence();
   if (p.split > 1) {
+    const int n_rows = p.n_rows, split = p.split;
+    const float* part = p.part;
+    float* out_conf = p.out_conf;
+    int* out_arg = p.out_arg;
     // merge each valid row's slice partials: a warp takes 4 rows per round
     // with all their loads in flight, lane k holding slice k; a fixed xor
     // tree merges them, so the result does not depend on arrival order
     constexpr int kRowsPerWarp = 4;
-    for (int r0 = warp * kRowsPerWarp; r0 < p.n_rows; r0 += (kThreads / 32) * kRowsPerWarp) {
+    for (int r0 = warp * kRowsPerWarp; r0 < n_rows; r0 += (kThreads / 32) * kRowsPerWarp) {
       Stat a[kRowsPerWarp];
       bool v[kRowsPerWarp];
 #pragma unroll
       for (int u = 0; u < kRowsPerWarp; ++u) {
         v[u] = row_valid(r0 + u);
         a[u] = none;
-        if (v[u] && lane < p.split) {
-          const float* o = p.part + ((size_t)(r0 + u) * p.split + lane) * 3;
+        if (v[u] && lane < split) {
+          const float* o = part + ((size_t)(r0 + u) * split + lane) * 3;
           a[u] = Stat{__ldcg(o), __ldcg(o + 1), __float_as_int(__ldcg(o + 2))};
         }
       }
+      // level by level over the rows, so the rows' shuffles overlap (the
+      // level loop stays rolled: this code runs once per launch)
+#pragma unroll 1
+      for (int off = kMaxSplit / 2; off; off >>= 1)
+#pragma unroll
+        for (int u = 0; u < kRowsPerWarp; ++u) a[u] = shfl_merge(a[u], off);
 #pragma unroll
       for (int u = 0; u < kRowsPerWarp; ++u) {
-        for (int off = kMaxSplit / 2; off; off >>= 1) a[u] = shfl_merge(a[u], off);
         if (v[u] && lane == 0) {
-          p.out_conf[r0 + u] = 1.f / a[u].s;
-          p.out_arg[r0 + u] = a[u].i;
+          out_conf[r0 + u] = 1.f / a[u].s;
+          out_arg[r0 + u] = a[u].i;
         }
       }
     }
