@@ -411,6 +411,171 @@ def run_gpu(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# Per-configuration kernel measurements (--configs)
+# ---------------------------------------------------------------------------
+def run_configs(args):
+    """Times each kernel of the path on the ragged batch, one layer of the
+    32-layer chain and the Flash-Verify stress workload: CUDA-graph replays
+    of one call, µs per call, and algorithmic TFLOP/s or GB/s against the
+    measured peaks. Prints one JSON line per configuration."""
+    import torch
+
+    import kv_cache_attention_gb300 as fdl
+    import synth
+    from kv_cache_attention_gb300 import build as fdl_build
+
+    fdl_build.build()
+    hbm, tc, src = peaks()
+    stream = torch.cuda.Stream()
+    torch.cuda.set_stream(stream)
+
+    def bf(t):
+        return torch.from_numpy(np.ascontiguousarray(t.data).view(np.int16)).view(torch.bfloat16).cuda()
+
+    def i32(a):
+        return torch.as_tensor(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+
+    def timed(fns, reps):
+        """Average µs of one call; fns rotate over input copies, one per graph."""
+        graphs = []
+        for fn in fns:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+            graphs.append(g)
+        for i in range(3 * len(graphs)):
+            graphs[i % len(graphs)].replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(reps):
+            graphs[i % len(graphs)].replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps * 1e3
+
+    def entry(us, flops=None, nbytes=None):
+        e = {"us": round(us, 2)}
+        if flops:
+            e["tflops"] = round(flops / us * 1e-6, 1)
+            e["frac_bf16_peak"] = round(flops / us * 1e-6 / tc, 3)
+        if nbytes:
+            e["gbs"] = round(nbytes / us * 1e-3, 1)
+            e["frac_hbm"] = round(nbytes / us * 1e-3 / hbm, 3)
+        return e
+
+    def layer_kernels(name, wl, rows, x, w_copies, kc, vc, ctx, track_rows=True, search=None, reps=50):
+        s, g = wl.shape, wl.geom
+        d, Hh, hd = s.d_model, s.n_heads, s.head_dim
+        R = rows.n_rows
+        q = torch.empty((R, Hh, hd), dtype=torch.bfloat16, device="cuda")
+        o = torch.empty_like(q)
+        lse = torch.empty((R, Hh), dtype=torch.float32, device="cuda")
+        track = torch.zeros((wl.batch, wl.max_seq), dtype=torch.float32, device="cuda") if track_rows else None
+        rs, rp, rc, rk, cu = (i32(rows.row_seq), i32(rows.row_rope_pos), i32(rows.row_cache_pos),
+                              i32(rows.row_kind), i32(rows.cu_seqlens))
+        bt, kvl = i32(g.block_table), i32(wl.seq_len)
+        out = {"rows": R}
+        qkv_fns = [lambda W=W: ctx.qkv_rope_cache_write(x, W, rs, rp, rc, bt, kc, vc, q) for W in w_copies]
+        qkv_fl = 2.0 * R * 3 * d * d
+        qkv_by = 2.0 * (3 * d * d + R * d + 3 * R * d)
+        out["qkv_rope_cache_write"] = entry(timed(qkv_fns, reps), qkv_fl, qkv_by)
+        kw = {}
+        n_keys = wl.seq_len.astype(np.int64).copy()
+        if search is not None:
+            kw = {"search_pos": i32(search[0]), "n_search": i32(search[1])}
+            n_keys = n_keys + 2 * np.asarray(search[1], np.int64)
+        rows_b = np.diff(rows.cu_seqlens).astype(np.int64)
+        att_fl = 4.0 * d * float((rows_b * n_keys).sum())
+        att_by = 2.0 * (2 * d * float(wl.seq_len.astype(np.int64).sum()) + 2 * R * d)
+        att_fn = lambda: ctx.sched_attn(q, kc, vc, bt, cu, kvl, rk, o, lse_out=lse, track_scores=track, **kw)
+        out["sched_attn"] = entry(timed([att_fn], reps), att_fl, att_by)
+        return out
+
+    results = []
+    # ragged batch of 16 (paged cache, half full refresh)
+    wl = synth.ragged_batch()
+    e, s, g = wl.extra, wl.shape, wl.geom
+    rows = e["rows"]
+    ctx = fdl.fdl_create(s.d_model, s.n_heads, s.head_dim, s.rope_theta, wl.batch, wl.max_seq, 0, g.page_size,
+                         g.n_pages, rows.n_rows, 16, "bf16", stream=stream)
+    Ws = [bf(e["w"]), bf(e["w"])]
+    res = layer_kernels("ragged_batch", wl, rows, bf(e["x"]), Ws, bf(e["k_cache"]), bf(e["v_cache"]), ctx, reps=20)
+    results.append({"config": "ragged_batch_b16_p64", **res})
+    ctx.close()
+    del Ws
+
+    # one layer of the 32-layer chain: 8 sequences x (32 window + 32 tracked)
+    wl = synth.layer_chain()
+    e, s, g = wl.extra, wl.shape, wl.geom
+    d = s.d_model
+    rng = np.random.default_rng(7)
+    per_seq = [synth.draft_rows(e["window_pos"], np.sort(rng.choice(e["prompt"], 32, replace=False)))
+               for _ in range(wl.batch)]
+    rows = synth.build_rows(per_seq)
+    ctx = fdl.fdl_create(d, s.n_heads, s.head_dim, s.rope_theta, wl.batch, wl.max_seq, 0, g.page_size,
+                         g.n_pages, rows.n_rows, 16, "bf16", stream=stream)
+    n_slots = g.n_pages * g.page_size
+    kc = torch.randn((n_slots, d), device="cuda").mul_(0.02 * d ** 0.5).bfloat16()
+    vc = torch.randn((n_slots, d), device="cuda").mul_(0.02 * d ** 0.5).bfloat16()
+    Ws = [bf(synth.chain_weight(e["seed"], l, d)) for l in range(2)]
+    x = bf(synth.chain_hidden(e["seed"], 1, 0, rows.n_rows, d))
+    res = layer_kernels("layer_chain", wl, rows, x, Ws, kc, vc, ctx)
+    results.append({"config": "layer_chain_b8_one_layer", **res})
+    ctx.close()
+    del Ws, kc, vc
+
+    # Flash-Verify stress: draft forward, eps unmasking, verify acceptance, top-k
+    wl = synth.flash_verify()
+    e, s, g = wl.extra, wl.shape, wl.geom
+    rows = e["rows"]
+    B, ms, V = wl.batch, e["max_search"], e["vocab"]
+    ctx = fdl.fdl_create(s.d_model, s.n_heads, s.head_dim, s.rope_theta, B, wl.max_seq, wl.max_views,
+                         g.page_size, g.n_pages, rows.n_rows, V, "bf16", stream=stream)
+    Ws = [bf(e["w"]), bf(e["w"])]
+    res = layer_kernels("flash_verify", wl, rows, bf(e["x"]), Ws, bf(e["k_cache"]), bf(e["v_cache"]), ctx)
+    del Ws
+    logits = bf(e["logits"])
+    Rw = logits.shape[0]
+    wseq, wpos = i32(e["window_row_seq"]), i32(e["window_row_pos"])
+    conf = torch.empty(Rw, dtype=torch.float32, device="cuda")
+    arg = torch.empty(Rw, dtype=torch.int32, device="cuda")
+    com = torch.empty(Rw, dtype=torch.uint8, device="cuda")
+    srows = torch.empty((B, ms), dtype=torch.int32, device="cuda")
+    nsr = torch.empty((B,), dtype=torch.int32, device="cuda")
+    um = lambda: ctx.unmask_verify(B, ms, logits=logits, row_seq=wseq, row_pos=wpos, eps=e["eps"],
+                                   force_progress=False, conf=conf, argmax=arg, commit=com, search_rows=srows,
+                                   n_search=nsr)
+    res["unmask (eps rule)"] = entry(timed([um], 50), None, 2.0 * Rw * V)
+    um()
+    torch.cuda.synchronize()
+    ns_host = nsr.cpu().numpy()
+    mask_logits = torch.empty((B * ms, V), dtype=torch.bfloat16, device="cuda")
+    mask_logits.copy_(logits[: B * ms])
+    draft = arg[: B * ms].clone()
+    acc = torch.empty(B * ms, dtype=torch.uint8, device="cuda")
+    nacc = torch.empty(B, dtype=torch.int32, device="cuda")
+    mconf = torch.empty(B * ms, dtype=torch.float32, device="cuda")
+    marg = torch.empty(B * ms, dtype=torch.int32, device="cuda")
+    vf = lambda: ctx.unmask_verify(B, ms, mask_logits=mask_logits, draft_tok=draft, gamma=e["gamma"], n_search=nsr,
+                                   accept=acc, n_accept=nacc, mask_conf=mconf, mask_argmax=marg)
+    res["verify (acceptance)"] = entry(timed([vf], 50), None, 2.0 * float(ns_host.sum()) * V)
+    res["verify (acceptance)"]["valid_rows"] = int(ns_host.sum())
+    track = torch.rand((B, wl.max_seq), device="cuda")
+    elig, sl = torch.as_tensor(e["eligible"]).cuda(), i32(wl.seq_len)
+    idx = torch.empty((B, 32), dtype=torch.int32, device="cuda")
+    cnt = torch.empty((B,), dtype=torch.int32, device="cuda")
+    res["track_topk"] = entry(timed([lambda: ctx.track_topk(track, elig, sl, 32, idx, cnt)], 200))
+    ctx.sync_status()
+    results.append({"config": "flash_verify_b32", **res})
+    ctx.close()
+    for r in results:
+        r.update({"peaks": {"hbm_gbs": hbm, "bf16_tflops": tc, "source": src},
+                  "timing": "CUDA-graph replays of one call on the dedicated stream; algorithmic work"})
+        print(json.dumps(r), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -419,8 +584,13 @@ def main():
     ap.add_argument("--impl", default="fdl", choices=["fdl", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--configs", action="store_true",
+                    help="time each kernel on the ragged-batch, 32-layer-chain and Flash-Verify workloads")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.configs:
+        run_configs(args)
+        return
     world, rank, local = dist_init()
     if args.impl == "reference":
         run_reference(args, world, rank)

@@ -55,7 +55,11 @@ constexpr int OFF_RING = OFF_Q + Q_BYTES;
 constexpr int OFF_P = OFF_RING + kStages * STAGE_BYTES;
 constexpr int OFF_ML = OFF_P + P_BYTES;
 constexpr int OFF_MISC = OFF_ML + ML_BYTES;
-constexpr int MISC_BYTES = 5120;
+// misc: barriers [0, 256), row kinds [256, 768), column sums [768, 1024),
+// search bitmap [1024, 4096) (<= 768 words), half-row (max, sum) pairs
+// [4096, 6144), flags [6144, 6160)
+constexpr int MISC_BYTES = 6400;
+static_assert(4096 + 2 * kBM * 2 * 4 + 16 <= MISC_BYTES, "misc layout fits");
 constexpr int SMEM_BYTES = 1024 + OFF_MISC + MISC_BYTES;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 static_assert(kStages * STAGE_BYTES >= kBM * (kHD + 4) * 4, "ring must hold an fp32 O tile for the cluster sum");
@@ -266,6 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* colacc = reinterpret_cast<float*>(misc + 768);         // [64]
   uint32_t* bitmap = reinterpret_cast<uint32_t*>(misc + 1024);  // [bitmap_words] (<= 768)
   float* halfml = reinterpret_cast<float*>(misc + 4096);        // [2][128][2]
+  volatile int* any_window = reinterpret_cast<volatile int*>(misc + 4096 + 2 * kBM * 2 * 4);  // item has WINDOW rows
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int C = p.C;
@@ -308,6 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::mbar_init(pv_done, 1);
     tc::mbar_init(ml_ready, 4 * C);  // the four column-half-0 warps of every split
     *abort_flag = 0;
+    *any_window = 0;
     tc::fence_mbar_init();
     // Q and the first ring of key tiles need no free slot: the producer (this
     // thread) issues them now, so the loads overlap the rest of the setup
@@ -442,6 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       kinds[r] = k;
+      if (k == FDL_KIND_WINDOW) *any_window = 1;
     }
     for (int w = t_local; w < p.bitmap_words; w += 256) bitmap[w] = 0u;
     if (t_local < 64) colacc[t_local] = 0.f;
@@ -537,6 +544,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- pass B: final probabilities, P V, tracker column sums
     const float wscale = do_track ? 1.f / ((float)p.H * (float)p.n_masked[b]) : 0.f;
     const bool track_row = do_track && kind == FDL_KIND_WINDOW;
+    // the tracker work (and its barriers) only for items holding WINDOW rows;
+    // the flag is the same for every softmax warp (set before barrier 3)
+    const bool track_item = do_track && *any_window != 0;
+    const bool track_warp = __any_sync(0xffffffffu, track_row);
     for (int i = 0; i < n_my; ++i, ++sc) {
       // a wait that gives up (abort) skips the work but never the barriers
       const int sb = sc & 1;
@@ -591,13 +602,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       if (ok && lane == 0) tc::mbar_arrive(p_full);
-      if (do_track) {
-        if (!track_row) {
+      if (track_item) {
+        if (track_warp) {  // a warp without WINDOW rows adds nothing
+          if (!track_row) {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) pr[k] = 0.f;
+            for (int k = 0; k < 32; ++k) pr[k] = 0.f;
+          }
+          warp_colsum32(pr, lane);
+          atomicAdd(&colacc[32 * ch + lane], pr[0]);
         }
-        warp_colsum32(pr, lane);
-        atomicAdd(&colacc[32 * ch + lane], pr[0]);
         tc::named_bar(1, 256);
         if (t_local < 64) {
           const int c = c0 + t_local;

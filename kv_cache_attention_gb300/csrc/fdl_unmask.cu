@@ -425,33 +425,52 @@ __global__ void __launch_bounds__(kThreads) row_reduce_kernel(RowParams p) {
     const float* part = p.part;
     float* out_conf = p.out_conf;
     int* out_arg = p.out_arg;
-    // merge each valid row's slice partials: a warp takes 4 rows per round
-    // with all their loads in flight, lane k holding slice k; a fixed xor
-    // tree merges them, so the result does not depend on arrival order
-    constexpr int kRowsPerWarp = 4;
-    for (int r0 = warp * kRowsPerWarp; r0 < n_rows; r0 += (kThreads / 32) * kRowsPerWarp) {
-      Stat a[kRowsPerWarp];
-      bool v[kRowsPerWarp];
+    if (split <= 4) {
+      // many rows, few slices: one thread per row, its slices' loads in
+      // flight together, merged in slice order
+      for (int r = threadIdx.x; r < n_rows; r += kThreads) {
+        if (!row_valid(r)) continue;
+        Stat a[4];
 #pragma unroll
-      for (int u = 0; u < kRowsPerWarp; ++u) {
-        v[u] = row_valid(r0 + u);
-        a[u] = none;
-        if (v[u] && lane < split) {
-          const float* o = part + ((size_t)(r0 + u) * split + lane) * 3;
-          a[u] = Stat{__ldcg(o), __ldcg(o + 1), __float_as_int(__ldcg(o + 2))};
+        for (int k = 0; k < 4; ++k) {
+          a[k] = none;
+          if (k < split) {
+            const float* o = part + ((size_t)r * split + k) * 3;
+            a[k] = Stat{__ldcg(o), __ldcg(o + 1), __float_as_int(__ldcg(o + 2))};
+          }
         }
+        const Stat m = merge(merge(a[0], a[1]), merge(a[2], a[3]));
+        out_conf[r] = 1.f / m.s;
+        out_arg[r] = m.i;
       }
-      // level by level over the rows, so the rows' shuffles overlap (the
-      // level loop stays rolled: this code runs once per launch)
+    } else {
+      // few rows, many slices: a warp takes 4 rows per round with all their
+      // loads in flight, lane k holding slice k; a fixed xor tree merges them
+      constexpr int kRowsPerWarp = 4;
+      for (int r0 = warp * kRowsPerWarp; r0 < n_rows; r0 += (kThreads / 32) * kRowsPerWarp) {
+        Stat a[kRowsPerWarp];
+        bool v[kRowsPerWarp];
+#pragma unroll
+        for (int u = 0; u < kRowsPerWarp; ++u) {
+          v[u] = row_valid(r0 + u);
+          a[u] = none;
+          if (v[u] && lane < split) {
+            const float* o = part + ((size_t)(r0 + u) * split + lane) * 3;
+            a[u] = Stat{__ldcg(o), __ldcg(o + 1), __float_as_int(__ldcg(o + 2))};
+          }
+        }
+        // level by level over the rows, so the rows' shuffles overlap (the
+        // level loop stays rolled: this code runs once per launch)
 #pragma unroll 1
-      for (int off = kMaxSplit / 2; off; off >>= 1)
+        for (int off = kMaxSplit / 2; off; off >>= 1)
 #pragma unroll
-        for (int u = 0; u < kRowsPerWarp; ++u) a[u] = shfl_merge(a[u], off);
+          for (int u = 0; u < kRowsPerWarp; ++u) a[u] = shfl_merge(a[u], off);
 #pragma unroll
-      for (int u = 0; u < kRowsPerWarp; ++u) {
-        if (v[u] && lane == 0) {
-          out_conf[r0 + u] = 1.f / a[u].s;
-          out_arg[r0 + u] = a[u].i;
+        for (int u = 0; u < kRowsPerWarp; ++u) {
+          if (v[u] && lane == 0) {
+            out_conf[r0 + u] = 1.f / a[u].s;
+            out_arg[r0 + u] = a[u].i;
+          }
         }
       }
     }
