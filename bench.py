@@ -289,13 +289,15 @@ def run_gpu(args, world, rank, local):
 
     def rest_part(c, L=None):
         L = Ls[c] if L is None else L
-        track.zero_()
         ctx.sched_attn(q, KC[c], VC[c], bt, cu, kv_len, row_kind, o, lse_out=lse, track_scores=track)
         ctx.track_topk(track, elig, seq_len, k, idx, cnt)
         ctx.unmask_verify(1, ms, logits=L, row_seq=win_seq, row_pos=win_pos, eps=e["eps"], force_progress=False,
                           conf=conf, argmax=arg, commit=com, search_rows=srows, n_search=nsr)
 
     def step(c, X=None, L=None):
+        # the tracker accumulates over a step's layers: zeroed once per step,
+        # before its first layer
+        track.zero_()
         qkv_part(c, X)
         rest_part(c, L)
 

@@ -36,6 +36,8 @@ build_worklist_kernel(const int* __restrict__ cu, const int* __restrict__ kv_len
   extern __shared__ int offs[];  // [B + 1]
   __shared__ int ok;
   const int tid = threadIdx.x;
+  fdl::grid_dep_wait();
+  fdl::grid_dep_launch();
   if (tid == 0) {
     int good = (cu[0] == 0) && (cu[B] == R);
     int acc = 0;
@@ -144,6 +146,8 @@ __global__ void __launch_bounds__(kWarps * 32) attn_simt_kernel(AttnParams p) {
   __shared__ float colacc[kKT];
 
   const int item = blockIdx.x;
+  fdl::grid_dep_wait();
+  fdl::grid_dep_launch();
   if (item >= p.wl[0]) return;
   const int h = blockIdx.y;
   const int* it = p.wl + 1 + 4 * item;
@@ -295,10 +299,10 @@ cudaError_t fdl_launch_attn(fdl_ctx* ctx, const void* q, const void* k_cache, co
   const int tile = ctx->attn_tile_m;
   const int cap = (R + tile - 1) / tile + B;
   const int max_search_tokens = min(c.max_views / 2, search_pos ? search_ld : 0);
-  build_worklist_kernel<<<1, kBuildThreads, (B + 1) * sizeof(int), ctx->stream>>>(
-      cu_seqlens_q, kv_len, search_pos ? n_search : nullptr, B, R, tile, row_kind, c.max_seq,
-      max_search_tokens, ctx->worklist, ctx->worklist_items, ctx->n_masked, ctx->err_word);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = fdl_launch_pdl(build_worklist_kernel, dim3(1), dim3(kBuildThreads), (B + 1) * sizeof(int),
+                                 ctx->stream, 1, cu_seqlens_q, kv_len, search_pos ? n_search : nullptr, B, R,
+                                 tile, row_kind, c.max_seq, max_search_tokens, ctx->worklist,
+                                 ctx->worklist_items, ctx->n_masked, ctx->err_word);
   if (e != cudaSuccess) return e;
   if (worklist_out) {
     e = cudaMemcpyAsync(worklist_out, ctx->worklist, (1 + 4 * (size_t)cap) * sizeof(int),
@@ -332,13 +336,11 @@ cudaError_t fdl_launch_attn(fdl_ctx* ctx, const void* q, const void* k_cache, co
   p.d = c.d_model;
   p.scale = (float)(1.0 / sqrt((double)c.head_dim));
   p.err = ctx->err_word;
-  dim3 grid(cap, c.n_heads);
+  const dim3 grid(cap, c.n_heads), block(kWarps * 32);
   if (c.dtype == FDL_BF16) {
-    if (c.head_dim == 128) attn_simt_kernel<__nv_bfloat16, 128><<<grid, kWarps * 32, 0, ctx->stream>>>(p);
-    else attn_simt_kernel<__nv_bfloat16, 64><<<grid, kWarps * 32, 0, ctx->stream>>>(p);
-  } else {
-    if (c.head_dim == 128) attn_simt_kernel<float, 128><<<grid, kWarps * 32, 0, ctx->stream>>>(p);
-    else attn_simt_kernel<float, 64><<<grid, kWarps * 32, 0, ctx->stream>>>(p);
+    if (c.head_dim == 128) return fdl_launch_pdl(attn_simt_kernel<__nv_bfloat16, 128>, grid, block, 0, ctx->stream, 1, p);
+    return fdl_launch_pdl(attn_simt_kernel<__nv_bfloat16, 64>, grid, block, 0, ctx->stream, 1, p);
   }
-  return cudaGetLastError();
+  if (c.head_dim == 128) return fdl_launch_pdl(attn_simt_kernel<float, 128>, grid, block, 0, ctx->stream, 1, p);
+  return fdl_launch_pdl(attn_simt_kernel<float, 64>, grid, block, 0, ctx->stream, 1, p);
 }

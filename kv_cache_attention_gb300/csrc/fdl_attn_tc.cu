@@ -21,13 +21,25 @@
 //           -> bf16 P staged in shared memory -> O += P V (tcgen05); the
 //           tracker column sums of the masked-window rows come from the same
 //           P. K is read twice (the second time mostly from L2); V once.
+// An unsplit item (C = 1) without masked-window rows needs no final
+// probabilities: its pass A takes only the row maximum m (no exponentials),
+// pass B stages P = exp(S - m) and sums it per row, and the epilogue divides
+// O by that sum. The two P tiles alternate, so the softmax of key tile i+1
+// overlaps the P V product of tile i.
 // The C partial O tiles are summed through distributed shared memory in rank
 // order, so results do not depend on timing.
 //
-// Warp roles (320 threads): warp 0 TMA producer (Q once, then a 3-stage K/V
-// ring), warp 1 TMEM owner and MMA issuer (one lane), warps 2-9 softmax and
+// Pass B issues the S product of tile i + 3 before the P V product of tile i
+// (four S buffers in TMEM), so a tile's scores are ready before its softmax
+// turn comes and the tensor pipe never waits behind a P V product for them.
+//
+// Warp roles (352 threads): warp 0 TMA producer of Q and of a 4-stage K
+// ring (each K stage is released as soon as its S product finishes), warp 10
+// TMA producer of a 4-stage V ring (the first V tiles land during pass A),
+// warp 1 TMEM owner and MMA issuer (one lane), warps 2-9 softmax and
 // epilogue: one query row per thread (TMEM lane quadrant = warp % 4) and half
-// of each key tile's columns per warp.
+// of each key tile's columns per warp. The cache slot of every key tile of
+// the CTA is looked up once, before the main loops, into shared memory.
 #include <cudaTypedefs.h>
 #include <math.h>
 
@@ -39,30 +51,40 @@ namespace {
 constexpr int kBM = 128;    // query rows per item
 constexpr int kBN = 64;     // keys per tile
 constexpr int kHD = 128;    // head dim handled here
-constexpr int kThreads = 320;
-constexpr int kStages = 3;
+constexpr int kThreads = 352;
+constexpr int kVWarp = 10;  // V producer
+constexpr int kKS = 4;      // K ring stages
+constexpr int kVS = 4;      // V ring stages
+constexpr int kSB = 4;      // S buffers in TMEM (64 columns each)
+constexpr int kLook = 3;    // pass B issues S of tile i + kLook before P V of tile i
+constexpr int kTmemCols = 512;  // O (128 columns) + kSB S buffers, rounded to a power of two
 constexpr int kMaxC = 8;
+constexpr int kMaxTiles = 384;  // key tiles of one item: (max_seq + max_views) / 64
 
 constexpr int Q_BYTES = kBM * kHD * 2;          // two 64-column halves of 16 KB
 constexpr int KT_BYTES = kBN * kHD * 2;         // K tile: two halves of 8 KB
 constexpr int VT_BYTES = kBN * kHD * 2;         // V tile: two halves of 8 KB
-constexpr int STAGE_BYTES = KT_BYTES + VT_BYTES;
-constexpr int P_BYTES = kBM * kBN * 2;          // bf16 P tile, 128 B rows
+constexpr int P_BYTES = kBM * kBN * 2;          // bf16 P tile, 128 B rows (two alternate)
 constexpr int ML_BYTES = kMaxC * kBM * 2 * 4;   // (max, sum) from every split
 
 constexpr int OFF_Q = 0;
-constexpr int OFF_RING = OFF_Q + Q_BYTES;
-constexpr int OFF_P = OFF_RING + kStages * STAGE_BYTES;
-constexpr int OFF_ML = OFF_P + P_BYTES;
+constexpr int OFF_KRING = OFF_Q + Q_BYTES;
+constexpr int OFF_VRING = OFF_KRING + kKS * KT_BYTES;  // directly after the K ring
+constexpr int OFF_P = OFF_VRING + kVS * VT_BYTES;
+constexpr int OFF_ML = OFF_P + 2 * P_BYTES;
 constexpr int OFF_MISC = OFF_ML + ML_BYTES;
 // misc: barriers [0, 256), row kinds [256, 768), column sums [768, 1024),
 // search bitmap [1024, 4096) (<= 768 words), half-row (max, sum) pairs
-// [4096, 6144), flags [6144, 6160)
-constexpr int MISC_BYTES = 6400;
-static_assert(4096 + 2 * kBM * 2 * 4 + 16 <= MISC_BYTES, "misc layout fits");
+// [4096, 6144), flags [6144, 6160), key-tile slots [6400, 6400 + 4 kMaxTiles)
+constexpr int OFF_SLOTS = 6400;
+constexpr int MISC_BYTES = OFF_SLOTS + 4 * kMaxTiles;
+static_assert(4096 + 2 * kBM * 2 * 4 + 16 <= OFF_SLOTS, "misc layout fits");
+static_assert(8 * (1 + 2 * kKS + 2 * kVS + 2 * kSB + 5) + 8 <= 256, "barriers fit");
+static_assert(128 + 64 * kSB <= kTmemCols && kLook < kSB, "TMEM columns and S lookahead");
 constexpr int SMEM_BYTES = 1024 + OFF_MISC + MISC_BYTES;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-static_assert(kStages * STAGE_BYTES >= kBM * (kHD + 4) * 4, "ring must hold an fp32 O tile for the cluster sum");
+static_assert(kKS * KT_BYTES + kVS * VT_BYTES >= kBM * (kHD + 4) * 4,
+              "the two rings must hold an fp32 O tile for the cluster sum");
 
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -204,40 +226,42 @@ __device__ __forceinline__ void warp_colsum32(float (&v)[32], int lane) {
   }
 }
 
-// Split `rank` of a C-CTA cluster sums rows [rank * 128 / C, (rank + 1) *
-// 128 / C) of the C staged fp32 O tiles in rank order and stores them as
-// bf16; every thread's remote loads are issued together.
+// Split `rank` of a C-CTA cluster sums its share of the item's qlen valid
+// rows, [rank * qlen / C, (rank + 1) * qlen / C), over the C staged fp32 O
+// tiles in rank order and stores them as bf16; each thread keeps the remote
+// loads of two float4 columns (from every split) in flight together.
 template <int CC>
 __device__ __forceinline__ void merge_o(const TcAttnParams& p, uint32_t base, uint32_t rank, int t_local, int q0,
                                         int qlen, int h, bool aborted) {
   constexpr int kOStride = kHD + 4;
-  constexpr int rows_per = kBM / CC;
-  constexpr int per_thr = rows_per * (kHD / 4) / 256;
-  static_assert(per_thr * 256 == rows_per * (kHD / 4), "whole float4 columns per thread");
-  float4 v[per_thr][CC];
+  constexpr int kVec = kHD / 4;  // float4 columns per row
+  const int r0 = (int)rank * qlen / CC, r1 = ((int)rank + 1) * qlen / CC;
+  const int n = (r1 - r0) * kVec;
+  for (int e0 = t_local; e0 < n; e0 += 2 * 256) {
+    float4 v[2][CC];
 #pragma unroll
-  for (int u = 0; u < per_thr; ++u) {
-    const int e = t_local + 256 * u;
-    const int r = (int)rank * rows_per + e / (kHD / 4);
-    const int col = (e % (kHD / 4)) * 4;
+    for (int u = 0; u < 2; ++u) {
+      const int e = e0 + 256 * u;
+      if (e < n) {
+        const int r = r0 + e / kVec, col = (e % kVec) * 4;
 #pragma unroll
-    for (int src = 0; src < CC; ++src)
-      v[u][src] = ld_cluster_v4(tc::map_cluster(base + (uint32_t)(r * kOStride + col) * 4u, (uint32_t)src));
-  }
-#pragma unroll
-  for (int u = 0; u < per_thr; ++u) {
-    const int e = t_local + 256 * u;
-    const int r = (int)rank * rows_per + e / (kHD / 4);
-    const int col = (e % (kHD / 4)) * 4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int src = 0; src < CC; ++src) {
-      acc.x += v[u][src].x;
-      acc.y += v[u][src].y;
-      acc.z += v[u][src].z;
-      acc.w += v[u][src].w;
+        for (int src = 0; src < CC; ++src)
+          v[u][src] = ld_cluster_v4(tc::map_cluster(base + (uint32_t)(r * kOStride + col) * 4u, (uint32_t)src));
+      }
     }
-    if (r < qlen && !aborted) {
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int e = e0 + 256 * u;
+      if (e >= n || aborted) continue;
+      const int r = r0 + e / kVec, col = (e % kVec) * 4;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int src = 0; src < CC; ++src) {
+        acc.x += v[u][src].x;
+        acc.y += v[u][src].y;
+        acc.z += v[u][src].z;
+        acc.w += v[u][src].w;
+      }
       __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
       uint2 w = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
       *reinterpret_cast<uint2*>(p.o + (size_t)(q0 + r) * p.d + h * kHD + col) = w;
@@ -251,38 +275,89 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sq = smem + OFF_Q;
-  uint8_t* ring = smem + OFF_RING;
+  uint8_t* kring = smem + OFF_KRING;
+  uint8_t* vring = smem + OFF_VRING;
   uint8_t* sp = smem + OFF_P;
   float* ml = reinterpret_cast<float*>(smem + OFF_ML);  // [C][128][2]
   uint8_t* misc = smem + OFF_MISC;
   uint64_t* bars = reinterpret_cast<uint64_t*>(misc);
   uint64_t* q_full = bars + 0;
-  uint64_t* kv_full = bars + 1;                 // [kStages]
-  uint64_t* kv_empty = bars + 1 + kStages;      // [kStages]
-  uint64_t* s_full = bars + 1 + 2 * kStages;    // [2]
-  uint64_t* s_free = bars + 3 + 2 * kStages;    // [2]
-  uint64_t* p_full = bars + 5 + 2 * kStages;
-  uint64_t* pv_done = bars + 6 + 2 * kStages;
-  uint64_t* ml_ready = bars + 7 + 2 * kStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8 + 2 * kStages);
+  uint64_t* k_full = bars + 1;                   // [kKS]
+  uint64_t* k_empty = k_full + kKS;              // [kKS]
+  uint64_t* v_full = k_empty + kKS;              // [kVS]
+  uint64_t* v_empty = v_full + kVS;              // [kVS]
+  uint64_t* s_full = v_empty + kVS;              // [kSB]
+  uint64_t* s_free = s_full + kSB;               // [kSB]
+  uint64_t* p_full = s_free + kSB;               // [2], one per P tile
+  uint64_t* pv_done = p_full + 2;                // [2], one per P tile
+  uint64_t* ml_ready = pv_done + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ml_ready + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* kinds = reinterpret_cast<int*>(misc + 256);              // [128]
   float* colacc = reinterpret_cast<float*>(misc + 768);         // [64]
   uint32_t* bitmap = reinterpret_cast<uint32_t*>(misc + 1024);  // [bitmap_words] (<= 768)
   float* halfml = reinterpret_cast<float*>(misc + 4096);        // [2][128][2]
   volatile int* any_window = reinterpret_cast<volatile int*>(misc + 4096 + 2 * kBM * 2 * 4);  // item has WINDOW rows
+  int* slots = reinterpret_cast<int*>(misc + OFF_SLOTS);        // [n_my] cache slot of each key tile
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int C = p.C;
   const uint32_t rank = C > 1 ? tc::cluster_ctarank() : 0u;
   const int item = blockIdx.z;
   const int h = blockIdx.y;
-  if (item >= p.wl[0]) return;  // uniform over the cluster (a cluster spans x only)
+
+  // ---------------------------------------------------------------- setup
+  // Barriers, TMEM and the tensor-map prefetch touch no global memory, so
+  // they overlap the end of the previous kernel in the stream; the work list,
+  // Q and the cache are read only after the dependency wait.
+  if (threadIdx.x == 0) {
+    tc::mbar_init(q_full, 1);
+    for (int s = 0; s < kKS; ++s) {
+      tc::mbar_init(&k_full[s], 1);
+      tc::mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < kVS; ++s) {
+      tc::mbar_init(&v_full[s], 1);
+      tc::mbar_init(&v_empty[s], 1);
+    }
+    for (int s = 0; s < kSB; ++s) {
+      tc::mbar_init(&s_full[s], 1);
+      tc::mbar_init(&s_free[s], 8);
+    }
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(&p_full[s], 8);
+      tc::mbar_init(&pv_done[s], 1);
+    }
+    tc::mbar_init(ml_ready, 4 * C);  // the four column-half-0 warps of every split
+    *abort_flag = 0;
+    *any_window = 0;
+    tc::fence_mbar_init();
+    tc::prefetch_tensormap(&tm_q);
+    tc::prefetch_tensormap(&tm_k);
+    tc::prefetch_tensormap(&tm_v);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_slot, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  fdl::grid_dep_wait();
+  fdl::grid_dep_launch();
+  if (item >= p.wl[0]) {  // uniform over the cluster (a cluster spans x only)
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (warp == 1) tc::tmem_dealloc(*tmem_slot, kTmemCols);
+    return;
+  }
   const int* it = p.wl + 1 + 4 * item;
   const int b = it[0], q0 = it[1], qlen = it[2], nkeys = it[3];
   const int kvl = min(p.kv_len[b], nkeys);
   const int m_search = p.search_pos ? (nkeys - kvl) / 2 : 0;
-  const int n_tiles = (nkeys + kBN - 1) / kBN;
+  int n_tiles = (nkeys + kBN - 1) / kBN;
+  if (n_tiles > kMaxTiles) {  // the launcher's limits rule this out; never index past the slot table
+    if (threadIdx.x == 0) fdl::raise_error(p.err, FDL_DEVERR_SHAPE);
+    n_tiles = kMaxTiles;
+  }
   const int t0 = (int)(rank * n_tiles / C), t1 = (int)((rank + 1) * n_tiles / C);
   const int n_my = t1 - t0;
 
@@ -297,45 +372,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     return p.n_slots;
   };
 
-  // ---------------------------------------------------------------- setup
-  const int pre = min(n_my, kStages);  // pass-A key tiles issued before the CTA barrier
-  if (threadIdx.x == 0) {
-    tc::mbar_init(q_full, 1);
-    for (int s = 0; s < kStages; ++s) {
-      tc::mbar_init(&kv_full[s], 1);
-      tc::mbar_init(&kv_empty[s], 1);
-    }
-    for (int s = 0; s < 2; ++s) {
-      tc::mbar_init(&s_full[s], 1);
-      tc::mbar_init(&s_free[s], 8);
-    }
-    tc::mbar_init(p_full, 8);
-    tc::mbar_init(pv_done, 1);
-    tc::mbar_init(ml_ready, 4 * C);  // the four column-half-0 warps of every split
-    *abort_flag = 0;
-    *any_window = 0;
-    tc::fence_mbar_init();
-    // Q and the first ring of key tiles need no free slot: the producer (this
-    // thread) issues them now, so the loads overlap the rest of the setup
-    if (n_my > 0) {
-      tc::prefetch_tensormap(&tm_q);
-      tc::prefetch_tensormap(&tm_k);
-      tc::prefetch_tensormap(&tm_v);
+  const int pre = min(n_my, kKS);  // pass-A key tiles issued before the CTA barrier
+  if (warp == 0) {
+    // every key tile's slot, looked up once by the whole warp
+    for (int i = lane; i < n_my; i += 32) slots[i] = tile_slot(t0 + i, true);
+    __syncwarp();
+    if (lane == 0 && n_my > 0) {
+      // Q and the first ring of key tiles need no free slot: the producer
+      // (this thread) issues them now, so the loads overlap the rest of the setup
       tc::mbar_arrive_expect_tx(q_full, Q_BYTES);
       tc::tma_load_2d(sq, &tm_q, h * kHD, q0, q_full);
       tc::tma_load_2d(sq + Q_BYTES / 2, &tm_q, h * kHD + 64, q0, q_full);
       for (int lc = 0; lc < pre; ++lc) {
-        const int slot = tile_slot(t0 + lc, true);
-        uint8_t* st = ring + lc * STAGE_BYTES;
-        tc::mbar_arrive_expect_tx(&kv_full[lc], KT_BYTES);
-        tc::tma_load_2d(st, &tm_k, h * kHD, slot, &kv_full[lc]);
-        tc::tma_load_2d(st + KT_BYTES / 2, &tm_k, h * kHD + 64, slot, &kv_full[lc]);
+        uint8_t* st = kring + lc * KT_BYTES;
+        tc::mbar_arrive_expect_tx(&k_full[lc], KT_BYTES);
+        tc::tma_load_2d(st, &tm_k, h * kHD, slots[lc], &k_full[lc]);
+        tc::tma_load_2d(st + KT_BYTES / 2, &tm_k, h * kHD + 64, slots[lc], &k_full[lc]);
       }
     }
-  }
-  if (warp == 1) {
-    tc::tmem_alloc(tmem_slot, 256);
-    tc::tmem_relinquish();
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -345,29 +399,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (C > 1) tc::cluster_arrive();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tm_o = tmem;            // columns [0, 128)
-  const uint32_t tm_s = tmem + 128;      // two 64-column S buffers
+  const uint32_t tm_s = tmem + 128;      // kSB 64-column S buffers
   const bool do_track = p.track != nullptr && p.n_masked[b] > 0;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ K producer
+    // K load lc = 0 .. 2 n_my - 1: key tile lc % n_my, for pass A then pass B
     if (lane == 0 && n_my > 0) {
-      int lc = pre;
-      for (int pass = 0; pass < 2; ++pass) {
-        for (int j = pass == 0 ? t0 + pre : t0; j < t1; ++j, ++lc) {
-          const int s = lc % kStages;
-          const uint32_t ph = (uint32_t)(lc / kStages) & 1u;
-          if (!tc::mbar_wait(&kv_empty[s], ph ^ 1u, abort_flag)) break;
-          const int slot = tile_slot(j, pass == 0);
-          uint8_t* st = ring + s * STAGE_BYTES;
-          tc::mbar_arrive_expect_tx(&kv_full[s], pass == 0 ? KT_BYTES : STAGE_BYTES);
-          tc::tma_load_2d(st, &tm_k, h * kHD, slot, &kv_full[s]);
-          tc::tma_load_2d(st + KT_BYTES / 2, &tm_k, h * kHD + 64, slot, &kv_full[s]);
-          if (pass == 1) {
-            tc::tma_load_2d(st + KT_BYTES, &tm_v, h * kHD, slot, &kv_full[s]);
-            tc::tma_load_2d(st + KT_BYTES + VT_BYTES / 2, &tm_v, h * kHD + 64, slot, &kv_full[s]);
-          }
-        }
-        if (*abort_flag) break;
+      for (int lc = pre; lc < 2 * n_my; ++lc) {
+        const int s = lc % kKS;
+        if (!tc::mbar_wait(&k_empty[s], ((uint32_t)(lc / kKS) & 1u) ^ 1u, abort_flag)) break;
+        const int slot = slots[lc % n_my];
+        uint8_t* st = kring + s * KT_BYTES;
+        tc::mbar_arrive_expect_tx(&k_full[s], KT_BYTES);
+        tc::tma_load_2d(st, &tm_k, h * kHD, slot, &k_full[s]);
+        tc::tma_load_2d(st + KT_BYTES / 2, &tm_k, h * kHD + 64, slot, &k_full[s]);
+      }
+    }
+    __syncwarp();
+    if (C > 1) tc::cluster_wait();  // matches the setup arrive
+  } else if (warp == kVWarp) {
+    // ------------------------------------------------------------ V producer
+    if (lane == 0 && n_my > 0) {
+      for (int i = 0; i < n_my; ++i) {
+        const int s = i % kVS;
+        if (!tc::mbar_wait(&v_empty[s], ((uint32_t)(i / kVS) & 1u) ^ 1u, abort_flag)) break;
+        const int slot = slots[i];
+        uint8_t* st = vring + s * VT_BYTES;
+        tc::mbar_arrive_expect_tx(&v_full[s], VT_BYTES);
+        tc::tma_load_2d(st, &tm_v, h * kHD, slot, &v_full[s]);
+        tc::tma_load_2d(st + VT_BYTES / 2, &tm_v, h * kHD + 64, slot, &v_full[s]);
       }
     }
     __syncwarp();
@@ -381,14 +442,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t ap = tc::smem_addr(sp);
       bool ok = tc::mbar_wait(q_full, 0, abort_flag);
       int sc = 0;
-      // S #sc = Q K(load_idx)^T into TMEM buffer sc & 1
+      // S #sc = Q K(load_idx)^T into TMEM buffer sc % kSB; the K stage is
+      // released as soon as the product finishes
       auto issue_s = [&](int load_idx) -> bool {
-        const int s = load_idx % kStages;
-        if (!tc::mbar_wait(&kv_full[s], (uint32_t)(load_idx / kStages) & 1u, abort_flag)) return false;
-        const int sb = sc & 1;
-        if (sc >= 2 && !tc::mbar_wait(&s_free[sb], (uint32_t)((sc - 2) >> 1) & 1u, abort_flag)) return false;
+        const int s = load_idx % kKS;
+        if (!tc::mbar_wait(&k_full[s], (uint32_t)(load_idx / kKS) & 1u, abort_flag)) return false;
+        const int sb = sc % kSB;
+        if (sc >= kSB && !tc::mbar_wait(&s_free[sb], (uint32_t)((sc - kSB) / kSB) & 1u, abort_flag)) return false;
         tc::fence_after_sync();
-        const uint32_t ak = tc::smem_addr(ring + s * STAGE_BYTES);
+        const uint32_t ak = tc::smem_addr(kring + s * KT_BYTES);
 #pragma unroll
         for (int k = 0; k < kHD / 16; ++k) {
           const uint32_t half = (uint32_t)(k >> 2), kk = (uint32_t)(k & 3) * 32u;
@@ -396,30 +458,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                           tc::desc_kmajor_sw128(ak + half * (KT_BYTES / 2) + kk), id_s, k > 0 ? 1u : 0u);
         }
         tc::mma_commit(&s_full[sb]);
+        tc::mma_commit(&k_empty[s]);
         ++sc;
         return true;
       };
-      // pass A: scores only; each stage is released once its S MMAs finish
-      for (int i = 0; ok && i < n_my; ++i) {
-        ok = issue_s(i);
-        if (ok) tc::mma_commit(&kv_empty[i % kStages]);
-      }
+      // pass A: scores only
+      for (int i = 0; ok && i < n_my; ++i) ok = issue_s(i);
       // pass B: S(i+1) is issued before O += P(i) V(i) so the softmax overlaps
       const int lb = n_my;
-      if (ok) ok = issue_s(lb);
+      for (int i = 0; ok && i < min(kLook, n_my); ++i) ok = issue_s(lb + i);
       for (int i = 0; ok && i < n_my; ++i) {
-        if (i + 1 < n_my) ok = issue_s(lb + i + 1);
+        if (i + kLook < n_my) ok = issue_s(lb + i + kLook);
         if (!ok) break;
-        if (!tc::mbar_wait(p_full, (uint32_t)i & 1u, abort_flag)) break;
+        const int pb = i & 1;
+        if (!tc::mbar_wait(&p_full[pb], (uint32_t)(i >> 1) & 1u, abort_flag)) break;
+        const int s = i % kVS;
+        if (!tc::mbar_wait(&v_full[s], (uint32_t)(i / kVS) & 1u, abort_flag)) break;
         tc::fence_after_sync();
-        const int s = (lb + i) % kStages;
-        const uint32_t av = tc::smem_addr(ring + s * STAGE_BYTES + KT_BYTES);
+        const uint32_t av = tc::smem_addr(vring + s * VT_BYTES);
+        const uint32_t apb = ap + (uint32_t)(pb * P_BYTES);
 #pragma unroll
         for (int k = 0; k < kBN / 16; ++k)
-          tc::mma_bf16_ss(tm_o, tc::desc_kmajor_sw128(ap + k * 32), desc_mnmajor_sw128(av + k * 2048, VT_BYTES / 2),
+          tc::mma_bf16_ss(tm_o, tc::desc_kmajor_sw128(apb + k * 32), desc_mnmajor_sw128(av + k * 2048, VT_BYTES / 2),
                           id_pv, (i > 0 || k > 0) ? 1u : 0u);
-        tc::mma_commit(pv_done);
-        tc::mma_commit(&kv_empty[s]);
+        tc::mma_commit(&pv_done[pb]);
+        tc::mma_commit(&v_empty[s]);
       }
     }
     __syncwarp();
@@ -435,8 +498,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int row = qd * 32 + lane;
   const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
   const int t_local = threadIdx.x - 64;  // 0..255 over the softmax warps
+  const bool softmax_warp = warp >= 2 && warp < 10;
   float lse2 = -INFINITY;  // log2-domain log-sum-exp of this row over all splits
-  if (warp >= 2) {
+  float inv_l = 1.f;       // scale of the accumulated O (1 unless P was relative to the max)
+  if (softmax_warp) {
     // row kinds and the search-position bitmap, read only by these warps
     for (int r = t_local; r < kBM; r += 256) {
       int k = -1;
@@ -459,13 +524,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc::named_bar(3, 256);
     const int kind = kinds[row];
+    // items with masked-window rows feed the tracker and need the final
+    // probabilities in pass B; so do split items (their O partials are
+    // summed over the cluster). The flag is the same for every softmax warp
+    // (any_window was set before barrier 3).
+    const bool track_item = do_track && *any_window != 0;
+    const bool max_only = C == 1 && !track_item;
     float mrow = -INFINITY, lrow = 0.f;
     int sc = 0;
-    // ---- pass A: running max and sum over this warp's columns
+    // ---- pass A: running max (and, unless max_only, sum) over this warp's columns
     for (int i = 0; i < n_my; ++i, ++sc) {
-      const int sb = sc & 1;
+      const int sb = sc % kSB;
       // tcgen05.ld is warp-collective: the whole warp proceeds or none of it
-      if (!__all_sync(0xffffffffu, tc::mbar_wait(&s_full[sb], (uint32_t)(sc >> 1) & 1u, abort_flag))) break;
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&s_full[sb], (uint32_t)(sc / kSB) & 1u, abort_flag))) break;
       tc::fence_after_sync();
       float x[32];
       tc::tmem_ld_32x32b_x32(tm_s + 64 * sb + 32 * ch + lane_off, x);
@@ -485,6 +556,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float tmax = t16[0];
       if (tmax == -INFINITY) continue;
       const float mnew = fmaxf(mrow, tmax);
+      if (max_only) {
+        mrow = mnew;
+        continue;
+      }
       float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
       for (int k = 0; k < 32; k += 4) {
@@ -496,11 +571,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       lrow = (mrow == -INFINITY ? 0.f : lrow * ex2(mrow - mnew)) + ((a0 + a1) + (a2 + a3));
       mrow = mnew;
     }
-    // ---- the two column halves of each row combine their (max, sum)
+    // ---- the two column halves of each row combine their (max, sum); a
+    // max_only pass A publishes only the max (slot 0), and its pass B the
+    // sum (slot 1), so the partner's slot-0 read never races a slot-1 write
     halfml[(ch * kBM + row) * 2] = mrow;
-    halfml[(ch * kBM + row) * 2 + 1] = lrow;
+    if (!max_only) halfml[(ch * kBM + row) * 2 + 1] = lrow;
     tc::named_bar(2, 256);
-    {
+    if (max_only) {
+      mrow = fmaxf(mrow, halfml[((1 - ch) * kBM + row) * 2]);
+    } else {
       const float mo = halfml[((1 - ch) * kBM + row) * 2], lo = halfml[((1 - ch) * kBM + row) * 2 + 1];
       const float mm = fmaxf(mrow, mo);
       float ll = 0.f;
@@ -536,22 +615,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (mr != -INFINITY) ll += lr * ex2(mr - mm);
         }
       lse2 = ll > 0.f ? mm + log2f(ll) : -INFINITY;
-    } else {
+    } else if (!max_only) {
       lse2 = lrow > 0.f ? mrow + log2f(lrow) : -INFINITY;
     }
-    if (p.lse && rank == 0 && ch == 0 && row < qlen) p.lse[(size_t)(q0 + row) * p.H + h] = lse2 * kLn2;
+    if (p.lse && !max_only && rank == 0 && ch == 0 && row < qlen) p.lse[(size_t)(q0 + row) * p.H + h] = lse2 * kLn2;
 
-    // ---- pass B: final probabilities, P V, tracker column sums
+    // ---- pass B: probabilities (final, or relative to the row max when
+    // max_only), P V, tracker column sums
+    const float sub = max_only ? mrow : lse2;  // exponent offset of P
+    float ps0 = 0.f, ps1 = 0.f, ps2 = 0.f, ps3 = 0.f;  // max_only: row sums of P
     const float wscale = do_track ? 1.f / ((float)p.H * (float)p.n_masked[b]) : 0.f;
     const bool track_row = do_track && kind == FDL_KIND_WINDOW;
-    // the tracker work (and its barriers) only for items holding WINDOW rows;
-    // the flag is the same for every softmax warp (set before barrier 3)
-    const bool track_item = do_track && *any_window != 0;
     const bool track_warp = __any_sync(0xffffffffu, track_row);
     for (int i = 0; i < n_my; ++i, ++sc) {
       // a wait that gives up (abort) skips the work but never the barriers
-      const int sb = sc & 1;
-      bool ok = __all_sync(0xffffffffu, tc::mbar_wait(&s_full[sb], (uint32_t)(sc >> 1) & 1u, abort_flag));
+      const int sb = sc % kSB;
+      bool ok = __all_sync(0xffffffffu, tc::mbar_wait(&s_full[sb], (uint32_t)(sc / kSB) & 1u, abort_flag));
       float pr[32];
       const int c0 = (t0 + i) * kBN;
       if (ok) {
@@ -561,19 +640,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&s_free[sb]);
         const uint32_t vm =
-            lse2 != -INFINITY ? vis_mask(kind, c0 + 32 * ch, kvl, m_search, bitmap, p.bitmap_words) : 0u;
+            sub != -INFINITY ? vis_mask(kind, c0 + 32 * ch, kvl, m_search, bitmap, p.bitmap_words) : 0u;
+        if (vm == 0xffffffffu) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) pr[k] = ((vm >> k) & 1u) ? ex2(pr[k] * p.scale_log2 - lse2) : 0.f;
+          for (int k = 0; k < 32; ++k) pr[k] = ex2(fmaf(pr[k], p.scale_log2, -sub));
+        } else {
+          // ex2(-inf) = 0 for the hidden keys
+#pragma unroll
+          for (int k = 0; k < 32; ++k) pr[k] = ex2(((vm >> k) & 1u) ? fmaf(pr[k], p.scale_log2, -sub) : -INFINITY);
+        }
+        if (max_only) {
+#pragma unroll
+          for (int k = 0; k < 32; k += 4) {
+            ps0 += pr[k];
+            ps1 += pr[k + 1];
+            ps2 += pr[k + 2];
+            ps3 += pr[k + 3];
+          }
+        }
       } else {
 #pragma unroll
         for (int k = 0; k < 32; ++k) pr[k] = 0.f;
       }
-      // the previous P V must have consumed the P buffer
-      ok = ok && (i == 0 || tc::mbar_wait(pv_done, (uint32_t)(i - 1) & 1u, abort_flag));
+      // P tile i & 1 was last read by the P V product of tile i - 2
+      const int pb = i & 1;
+      ok = ok && (i < 2 || tc::mbar_wait(&pv_done[pb], (uint32_t)((i - 2) >> 1) & 1u, abort_flag));
       if (ok) {
         // P in the 128-byte swizzled K-major layout: row r, 16-byte chunk q at q ^ (r & 7);
         // this warp writes chunks 4 ch .. 4 ch + 3 (its 32 keys)
-        uint8_t* prow = sp + row * 128;
+        uint8_t* prow = sp + pb * P_BYTES + row * 128;
 #pragma unroll
         for (int qq = 0; qq < 4; ++qq) {
           const int q = 4 * ch + qq;
@@ -587,9 +682,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // keys past the sequence end may hold anything: zero their V rows so
         // that 0 * V stays 0 in the P V product
-        if (c0 + kBN > nkeys) {
-          const int s = (n_my + i) % kStages;
-          uint8_t* vt = ring + s * STAGE_BYTES + KT_BYTES;
+        if (c0 + kBN > nkeys && tc::mbar_wait(&v_full[i % kVS], (uint32_t)(i / kVS) & 1u, abort_flag)) {
+          uint8_t* vt = vring + (i % kVS) * VT_BYTES;
           const int first = max(0, nkeys - c0);
           for (int e = lane; e < (kBN - first) * 16; e += 32) {
             const int r = first + e / 16, part = e % 16;
@@ -601,7 +695,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
       }
       __syncwarp();
-      if (ok && lane == 0) tc::mbar_arrive(p_full);
+      if (ok && lane == 0) tc::mbar_arrive(&p_full[pb]);
       if (track_item) {
         if (track_warp) {  // a warp without WINDOW rows adds nothing
           if (!track_row) {
@@ -621,7 +715,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::named_bar(1, 256);
       }
     }
-    if (n_my > 0) tc::mbar_wait(pv_done, (uint32_t)(n_my - 1) & 1u, abort_flag);
+    if (max_only) {
+      // the two column halves' sums of P give the row's normaliser
+      const float lmine = (ps0 + ps1) + (ps2 + ps3);
+      halfml[(ch * kBM + row) * 2 + 1] = lmine;
+      tc::named_bar(2, 256);
+      const float l = lmine + halfml[((1 - ch) * kBM + row) * 2 + 1];
+      lse2 = (mrow != -INFINITY && l > 0.f) ? mrow + log2f(l) : -INFINITY;
+      inv_l = lse2 != -INFINITY ? 1.f / l : 0.f;
+      if (p.lse && ch == 0 && row < qlen) p.lse[(size_t)(q0 + row) * p.H + h] = lse2 * kLn2;
+    }
+    if (n_my > 0) tc::mbar_wait(&pv_done[(n_my - 1) & 1], (uint32_t)((n_my - 1) >> 1) & 1u, abort_flag);
     tc::fence_after_sync();
   }
 
@@ -631,7 +735,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // per-row conditions only selecting values and guarding stores.
   constexpr int kOStride = kHD + 4;  // padded fp32 staging rows: conflict-free float4 access
   if (C == 1) {
-    if (warp >= 2) {
+    if (softmax_warp) {
       const bool store = row < qlen && !*abort_flag;
       __nv_bfloat16* orow = p.o + (size_t)(q0 + row) * p.d + h * kHD;
 #pragma unroll
@@ -640,7 +744,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float a[32];
         if (n_my > 0) tc::tmem_ld_32x32b_x32(tm_o + c0 + lane_off, a);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) a[e] = (n_my > 0 && lse2 != -INFINITY) ? a[e] : 0.f;
+        for (int e = 0; e < 32; ++e) a[e] = (n_my > 0 && lse2 != -INFINITY) ? a[e] * inv_l : 0.f;
         if (!store) continue;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -655,10 +759,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // every split stages its fp32 partial O (already normalised) in its ring;
-    // split r then sums rows [r*128/C, (r+1)*128/C) over all splits in rank order
-    float* ostage = reinterpret_cast<float*>(ring);  // [128][kOStride]
-    if (warp >= 2) {
+    // every split stages its fp32 partial O (already normalised) in its two
+    // drained rings; split r then sums its share of the valid rows over all
+    // splits in rank order
+    float* ostage = reinterpret_cast<float*>(kring);  // [128][kOStride], over both rings
+    if (softmax_warp) {
 #pragma unroll
       for (int cc = 0; cc < 64; cc += 32) {
         const int c0 = 64 * ch + cc;
@@ -673,7 +778,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     tc::cluster_sync();
-    if (warp >= 2) {
+    if (softmax_warp) {
       const uint32_t base = tc::smem_addr(ostage);
       const bool ab = *abort_flag != 0;
       if (C == 2) merge_o<2>(p, base, rank, t_local, q0, qlen, h, ab);
@@ -686,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_before_sync();
   __syncthreads();
   if (threadIdx.x == 0 && *abort_flag) fdl::raise_error(p.err, FDL_DEVERR_TIMEOUT);
-  if (warp == 1) tc::tmem_dealloc(tmem, 256);
+  if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
@@ -771,20 +876,12 @@ cudaError_t fdl_launch_attn_tc(fdl_ctx* ctx, const void* q, const void* k_cache,
   int C = 1;
   while (C < kMaxC && est_items * c.n_heads * (2 * C) <= ctx->num_sms) C *= 2;
   p.C = C;
-  cudaLaunchConfig_t cfg = {};
   // grid (split, head, item): items vary slowest, so the CTAs of real items
-  // are scheduled before the idle tail of the capacity bound
-  if (cap > 65535) return cudaErrorInvalidConfiguration;
-  cfg.gridDim = dim3((unsigned)C, (unsigned)c.n_heads, (unsigned)cap);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
-  cfg.stream = ctx->stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = C > 1 ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, attn_tc_kernel, mq, mk, mv, p);
+  // are scheduled before any idle tail. Sequence b contributes
+  // ceil(rows_b / 128) items, and summed over the sequences with rows that
+  // is at most ceil(R / 128) + B - 1, so no more CTAs are launched.
+  const int items = min(cap, est_items);
+  if (items > 65535) return cudaErrorInvalidConfiguration;
+  return fdl_launch_pdl(attn_tc_kernel, dim3((unsigned)C, (unsigned)c.n_heads, (unsigned)items), dim3(kThreads, 1, 1),
+                        SMEM_BYTES, ctx->stream, C, mq, mk, mv, p);
 }

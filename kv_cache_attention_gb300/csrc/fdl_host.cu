@@ -57,6 +57,14 @@ bool config_ok(const fdl_config* c, char* why, size_t n) {
 
 }  // namespace
 
+bool fdl_pdl_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("FDL_DISABLE_PDL");
+    return !(v && v[0] && v[0] != '0');
+  }();
+  return on;
+}
+
 extern "C" {
 
 fdl_status fdl_create(const fdl_config* cfg, void* cuda_stream, fdl_ctx** out) {

@@ -78,6 +78,21 @@ __device__ __forceinline__ long long cache_slot(const int* block_table, int bt_s
   return (long long)page * page_size + (c % page_size);
 }
 
+// Programmatic dependent launch. Every kernel of the library is launched
+// with programmatic stream serialisation, so it may become resident while
+// the previous kernel in the stream is still running. Work that touches no
+// global memory (barrier initialisation, TMEM allocation, tensor-map
+// prefetch) may run before grid_dep_wait(); every global-memory read or
+// write comes after it, because the wait is what guarantees that the
+// previous kernel has finished and its writes are visible. Without the
+// launch attribute the wait returns at once.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the next kernel in the stream launch (it still waits for this one to
+// finish before touching memory). Called once this kernel no longer needs
+// SM room for CTAs of its own that have not started.
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Order-preserving map of a float onto uint32 (-0.0 folded onto +0.0).
 __device__ __forceinline__ unsigned float_order_key(float f) {
   unsigned u = __float_as_uint(f);
@@ -86,6 +101,39 @@ __device__ __forceinline__ unsigned float_order_key(float f) {
 }
 
 }  // namespace fdl
+
+// Launches `kernel` on `stream` with programmatic stream serialisation (see
+// grid_dep_wait). Setting FDL_DISABLE_PDL=1 in the environment launches
+// plainly instead, so that each kernel starts only after the previous one
+// has finished.
+bool fdl_pdl_enabled();
+
+template <typename... KArgs, typename... Args>
+cudaError_t fdl_launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                           int cluster_x, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (fdl_pdl_enabled()) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
 
 // Launchers implemented by the kernel translation units. Each returns a
 // cudaError_t from the launch.

@@ -40,6 +40,8 @@ template <typename T>
 __global__ void __launch_bounds__(kWarps * 32) qkv_simt_kernel(QkvParams p) {
   extern __shared__ float xs[];  // [d]
   const int r = blockIdx.x;
+  fdl::grid_dep_wait();
+  fdl::grid_dep_launch();
   const T* x = reinterpret_cast<const T*>(p.x) + (size_t)r * p.d;
   for (int k = threadIdx.x; k < p.d; k += blockDim.x) xs[k] = fdl::io<T>::load(x + k);
   __syncthreads();
@@ -132,16 +134,14 @@ cudaError_t fdl_launch_qkv(fdl_ctx* ctx, const void* X, const void* W, int R, co
   p.rope_positions = ctx->rope_positions;
   p.err = ctx->err_word;
   const int pairs = 3 * c.d_model / 2;
-  dim3 grid(R, (pairs + kWarps - 1) / kWarps);
+  const dim3 grid(R, (pairs + kWarps - 1) / kWarps), block(kWarps * 32);
   size_t smem = (size_t)c.d_model * sizeof(float);
   if (c.dtype == FDL_BF16) {
     if (smem > 48 * 1024)
       cudaFuncSetAttribute(qkv_simt_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    qkv_simt_kernel<__nv_bfloat16><<<grid, kWarps * 32, smem, ctx->stream>>>(p);
-  } else {
-    if (smem > 48 * 1024)
-      cudaFuncSetAttribute(qkv_simt_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    qkv_simt_kernel<float><<<grid, kWarps * 32, smem, ctx->stream>>>(p);
+    return fdl_launch_pdl(qkv_simt_kernel<__nv_bfloat16>, grid, block, smem, ctx->stream, 1, p);
   }
-  return cudaGetLastError();
+  if (smem > 48 * 1024)
+    cudaFuncSetAttribute(qkv_simt_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  return fdl_launch_pdl(qkv_simt_kernel<float>, grid, block, smem, ctx->stream, 1, p);
 }

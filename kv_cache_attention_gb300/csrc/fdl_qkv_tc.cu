@@ -98,6 +98,8 @@ __global__ void __launch_bounds__(kThreads, BN == 64 ? 2 : 1)
   const int kb0 = (int)(rank * p.nkb / ks), kb1 = (int)((rank + 1) * p.nkb / ks);
 
   const int pre = min(kb1 - kb0, C::STAGES);  // loads issued before the CTA barrier
+  // Barriers, TMEM and the tensor-map prefetch touch no global memory, so
+  // they overlap the end of the previous kernel in the stream.
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       tc::mbar_init(&full[s], 1);
@@ -107,21 +109,25 @@ __global__ void __launch_bounds__(kThreads, BN == 64 ? 2 : 1)
     *abort_flag = 0;
     *is_last = ks == 1;
     tc::fence_mbar_init();
+    tc::prefetch_tensormap(&tmap_w);
+    tc::prefetch_tensormap(&tmap_x);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_slot, BN);
+    tc::tmem_relinquish();
+  }
+  fdl::grid_dep_wait();
+  fdl::grid_dep_launch();
+  if (threadIdx.x == 0) {
     // The first ring of loads needs no free slot: the producer (this thread)
     // issues it before the CTA barrier, so the weight stream starts while
     // the other warps are still setting up.
-    tc::prefetch_tensormap(&tmap_w);
-    tc::prefetch_tensormap(&tmap_x);
     for (int it = 0; it < pre; ++it) {
       uint8_t* a = pipe + it * C::STAGE_BYTES;
       tc::mbar_arrive_expect_tx(&full[it], C::STAGE_BYTES);
       tc::tma_load_2d(a, &tmap_w, (kb0 + it) * kBK, f0, &full[it]);
       tc::tma_load_2d(a + C::A_BYTES, &tmap_x, (kb0 + it) * kBK, tile_r * BN, &full[it]);
     }
-  }
-  if (warp == 1) {
-    tc::tmem_alloc(tmem_slot, BN);
-    tc::tmem_relinquish();
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -372,12 +378,8 @@ cudaError_t launch(fdl_ctx* ctx, const TcParams& p0, const void* X, const void* 
   p.ksplit = ks;
   p.partials = ctx->qkv_partials;
   p.tickets = ctx->qkv_ticket_buf;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(ks, tiles_r, tiles_f);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = Cf::SMEM_BYTES;
-  cfg.stream = ctx->stream;
-  return cudaLaunchKernelEx(&cfg, qkv_tc_kernel<BN>, mw, mx, p);
+  return fdl_launch_pdl(qkv_tc_kernel<BN>, dim3(ks, tiles_r, tiles_f), dim3(kThreads, 1, 1), Cf::SMEM_BYTES,
+                        ctx->stream, 1, mw, mx, p);
 }
 
 }  // namespace

@@ -42,6 +42,8 @@ topk_large_kernel(const float* __restrict__ scores, const unsigned char* __restr
 
   const int b = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  fdl::grid_dep_wait();
+  fdl::grid_dep_launch();
   int n = seq_len[b];
   if (n < 0 || n > ld) {
     if (tid == 0) fdl::raise_error(err, FDL_DEVERR_INDEX);
@@ -213,6 +215,8 @@ topk_kernel(const float* __restrict__ scores, const unsigned char* __restrict__ 
 
   const int b = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  fdl::grid_dep_wait();
+  fdl::grid_dep_launch();
   int n = seq_len[b];
   if (n < 0 || n > ld) {
     if (tid == 0) fdl::raise_error(err, FDL_DEVERR_INDEX);
@@ -404,10 +408,8 @@ topk_kernel(const float* __restrict__ scores, const unsigned char* __restrict__ 
 cudaError_t fdl_launch_topk(fdl_ctx* ctx, const float* scores, const unsigned char* eligible, int ld,
                             const int* seq_len, int B, int k, int* idx_out, int* cnt_out) {
   if (ld <= kStage)
-    topk_kernel<<<B, kThreads, 0, ctx->stream>>>(scores, eligible, ld, seq_len, k, idx_out, cnt_out,
-                                                ctx->err_word);
-  else
-    topk_large_kernel<<<B, kThreads, 0, ctx->stream>>>(scores, eligible, ld, seq_len, k, idx_out, cnt_out,
-                                                      ctx->err_word);
-  return cudaGetLastError();
+    return fdl_launch_pdl(topk_kernel, dim3(B), dim3(kThreads), 0, ctx->stream, 1, scores, eligible, ld, seq_len, k,
+                          idx_out, cnt_out, ctx->err_word);
+  return fdl_launch_pdl(topk_large_kernel, dim3(B), dim3(kThreads), 0, ctx->stream, 1, scores, eligible, ld, seq_len,
+                        k, idx_out, cnt_out, ctx->err_word);
 }

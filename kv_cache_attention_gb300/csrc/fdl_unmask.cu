@@ -374,6 +374,8 @@ __global__ void __launch_bounds__(kThreads) row_reduce_kernel(RowParams p) {
   const int row = blockIdx.x / p.split;
   const int sp = blockIdx.x % p.split;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  fdl::grid_dep_wait();
+  fdl::grid_dep_launch();
   // verify phase: row r = b*max_search + j is valid only when j < n_search[b]
   const int n_rows_all = p.n_rows, phase = p.phase, ms_all = p.max_search;
   const int* n_search_in = p.n_search;
@@ -497,8 +499,8 @@ cudaError_t launch_phase(fdl_ctx* ctx, RowParams p) {
   p.chunk = chunk;
   p.part = ctx->row_part;
   p.vec_ok = ((reinterpret_cast<uintptr_t>(p.logits) & 15) == 0) && ((size_t)V * sizeof(T)) % 16 == 0;
-  row_reduce_kernel<T><<<(unsigned)(p.n_rows * split), kThreads, 0, ctx->stream>>>(p);
-  return cudaGetLastError();
+  return fdl_launch_pdl(row_reduce_kernel<T>, dim3((unsigned)(p.n_rows * split)), dim3(kThreads), 0, ctx->stream, 1,
+                        p);
 }
 
 }  // namespace
