@@ -13,33 +13,34 @@
 //
 // One CTA = (work item of <= 128 query rows of one sequence, head, KV split).
 // The KV splits of an item form a thread-block cluster of C CTAs (C = 1 when
-// items x heads already fill the GPU). Two passes over the CTA's key tiles:
-//   pass A  S = Q K^T (tcgen05, fp32 in TMEM) -> running row max and sum;
-//           the C partial (max, sum) pairs meet through distributed shared
-//           memory and every CTA forms the exact log-sum-exp of each row;
-//   pass B  S again -> P = exp(S - lse) (final probabilities, no rescaling)
-//           -> bf16 P staged in shared memory -> O += P V (tcgen05); the
-//           tracker column sums of the masked-window rows come from the same
-//           P. K is read twice (the second time mostly from L2); V once.
-// An unsplit item (C = 1) without masked-window rows needs no final
-// probabilities: its pass A takes only the row maximum m (no exponentials),
-// pass B stages P = exp(S - m) and sums it per row, and the epilogue divides
-// O by that sum. The two P tiles alternate, so the softmax of key tile i+1
-// overlaps the P V product of tile i.
+// items x heads already fill the GPU).
+//
+// Scores S = Q K^T and the products O += P V run on tcgen05 with fp32
+// accumulators in TMEM. Eight softmax warps form two groups; group g takes
+// the key tiles i with i % 2 == g and owns a P tile in shared memory and an O
+// accumulator O_g in TMEM, so one group's softmax overlaps the other's
+// products. An item takes one of two modes:
+//   online    (C = 1, no masked-window row feeds the tracker) one pass: P =
+//             exp(S - m) against a running row max m that moves only when a
+//             tile's max exceeds it by more than 2^kRescale; O_g and the row
+//             sum are then scaled to the new m in TMEM. At the end O =
+//             (O_0 w_0 + O_1 w_1) / l with the two groups' weights w_g.
+//   two-pass  (split items, and items whose WINDOW rows feed Eq. (2))
+//             pass A gives each row's exact log-sum-exp (the C splits' (max,
+//             sum) pairs meet through distributed shared memory); pass B
+//             forms the final probabilities P = exp(S - lse), whose column
+//             sums over WINDOW rows are the tracker's contribution, and O =
+//             O_0 + O_1. K is read twice, the second time mostly from L2.
 // The C partial O tiles are summed through distributed shared memory in rank
 // order, so results do not depend on timing.
 //
-// Pass B issues the S product of tile i + 3 before the P V product of tile i
-// (four S buffers in TMEM), so a tile's scores are ready before its softmax
-// turn comes and the tensor pipe never waits behind a P V product for them.
-//
 // Warp roles (352 threads): warp 0 TMA producer of Q and of a 4-stage K
-// ring (each K stage is released as soon as its S product finishes), warp 10
-// TMA producer of a 4-stage V ring (the first V tiles land during pass A),
-// warp 1 TMEM owner and MMA issuer (one lane), warps 2-9 softmax and
-// epilogue: one query row per thread (TMEM lane quadrant = warp % 4) and half
-// of each key tile's columns per warp. The cache slot of every key tile of
-// the CTA is looked up once, before the main loops, into shared memory.
+// ring (a stage is released as soon as its S product finishes), warp 10 TMA
+// producer of a 4-stage V ring, warp 1 TMEM owner and MMA issuer (one lane,
+// issuing whichever of the next P V or the next S is ready, from four S
+// buffers), warps 2-9 softmax and epilogue: one query row per thread (TMEM
+// lane quadrant = warp % 4). The cache slot of every key tile of the CTA is
+// looked up once, before the main loops, into shared memory.
 #include <cudaTypedefs.h>
 #include <math.h>
 
@@ -56,8 +57,8 @@ constexpr int kVWarp = 10;  // V producer
 constexpr int kKS = 4;      // K ring stages
 constexpr int kVS = 4;      // V ring stages
 constexpr int kSB = 4;      // S buffers in TMEM (64 columns each)
-constexpr int kLook = 3;    // pass B issues S of tile i + kLook before P V of tile i
-constexpr int kTmemCols = 512;  // O (128 columns) + kSB S buffers, rounded to a power of two
+constexpr int kTmemCols = 512;  // O_0, O_1 (128 columns each) + kSB S buffers
+constexpr float kRescale = 8.f;  // online mode: log2 headroom of P before the row max moves
 constexpr int kMaxC = 8;
 constexpr int kMaxTiles = 384;  // key tiles of one item: (max_seq + max_views) / 64
 
@@ -73,14 +74,18 @@ constexpr int OFF_VRING = OFF_KRING + kKS * KT_BYTES;  // directly after the K r
 constexpr int OFF_P = OFF_VRING + kVS * VT_BYTES;
 constexpr int OFF_ML = OFF_P + 2 * P_BYTES;
 constexpr int OFF_MISC = OFF_ML + ML_BYTES;
-// misc: barriers [0, 256), row kinds [256, 768), column sums [768, 1024),
-// search bitmap [1024, 4096) (<= 768 words), half-row (max, sum) pairs
-// [4096, 6144), flags [6144, 6160), key-tile slots [6400, 6400 + 4 kMaxTiles)
-constexpr int OFF_SLOTS = 6400;
+// misc: barriers [0, 256), row kinds, the two groups' tracker column sums,
+// the search bitmap (<= 768 words), the two groups' (max, sum) per row,
+// flags, key-tile slots
+constexpr int OFF_KINDS = 256;                      // int [128]
+constexpr int OFF_COLACC = OFF_KINDS + 4 * kBM;     // float [2][64]
+constexpr int OFF_BITMAP = OFF_COLACC + 2 * 64 * 4;  // uint32 [768]
+constexpr int OFF_HALFML = OFF_BITMAP + 768 * 4;    // float [2][128][2]
+constexpr int OFF_FLAGS = OFF_HALFML + 2 * kBM * 2 * 4;
+constexpr int OFF_SLOTS = OFF_FLAGS + 256;          // int [kMaxTiles]
 constexpr int MISC_BYTES = OFF_SLOTS + 4 * kMaxTiles;
-static_assert(4096 + 2 * kBM * 2 * 4 + 16 <= OFF_SLOTS, "misc layout fits");
-static_assert(8 * (1 + 2 * kKS + 2 * kVS + 2 * kSB + 5) + 8 <= 256, "barriers fit");
-static_assert(128 + 64 * kSB <= kTmemCols && kLook < kSB, "TMEM columns and S lookahead");
+static_assert(8 * (1 + 2 * kKS + 2 * kVS + 2 * kSB + 5) + 8 <= OFF_KINDS, "barriers fit");
+static_assert(256 + 64 * kSB <= kTmemCols, "TMEM columns");
 constexpr int SMEM_BYTES = 1024 + OFF_MISC + MISC_BYTES;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 static_assert(kKS * KT_BYTES + kVS * VT_BYTES >= kBM * (kHD + 4) * 4,
@@ -288,23 +293,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* v_empty = v_full + kVS;              // [kVS]
   uint64_t* s_full = v_empty + kVS;              // [kSB]
   uint64_t* s_free = s_full + kSB;               // [kSB]
-  uint64_t* p_full = s_free + kSB;               // [2], one per P tile
-  uint64_t* pv_done = p_full + 2;                // [2], one per P tile
+  uint64_t* p_full = s_free + kSB;               // [2], one per softmax group (P tile)
+  uint64_t* pv_done = p_full + 2;                // [2], one per softmax group (P tile, O accumulator)
   uint64_t* ml_ready = pv_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ml_ready + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* kinds = reinterpret_cast<int*>(misc + 256);              // [128]
-  float* colacc = reinterpret_cast<float*>(misc + 768);         // [64]
-  uint32_t* bitmap = reinterpret_cast<uint32_t*>(misc + 1024);  // [bitmap_words] (<= 768)
-  float* halfml = reinterpret_cast<float*>(misc + 4096);        // [2][128][2]
-  volatile int* any_window = reinterpret_cast<volatile int*>(misc + 4096 + 2 * kBM * 2 * 4);  // item has WINDOW rows
-  int* slots = reinterpret_cast<int*>(misc + OFF_SLOTS);        // [n_my] cache slot of each key tile
+  int* kinds = reinterpret_cast<int*>(misc + OFF_KINDS);            // [128]
+  float* colacc = reinterpret_cast<float*>(misc + OFF_COLACC);      // [2][64]
+  uint32_t* bitmap = reinterpret_cast<uint32_t*>(misc + OFF_BITMAP);  // [bitmap_words] (<= 768)
+  float* halfml = reinterpret_cast<float*>(misc + OFF_HALFML);      // [2][128][2]
+  volatile int* any_window = reinterpret_cast<volatile int*>(misc + OFF_FLAGS);  // item has WINDOW rows
+  int* slots = reinterpret_cast<int*>(misc + OFF_SLOTS);            // [n_my] cache slot of each key tile
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int C = p.C;
   const uint32_t rank = C > 1 ? tc::cluster_ctarank() : 0u;
   const int item = blockIdx.z;
   const int h = blockIdx.y;
+  const bool softmax_warp = warp >= 2 && warp < 10;
+  const int t_local = threadIdx.x - 64;  // 0..255 over the softmax warps
 
   // ---------------------------------------------------------------- setup
   // Barriers, TMEM and the tensor-map prefetch touch no global memory, so
@@ -322,13 +329,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < kSB; ++s) {
       tc::mbar_init(&s_full[s], 1);
-      tc::mbar_init(&s_free[s], 8);
+      tc::mbar_init(&s_free[s], 4);  // the four warps of the group that reads it
     }
     for (int s = 0; s < 2; ++s) {
-      tc::mbar_init(&p_full[s], 8);
+      tc::mbar_init(&p_full[s], 4);
       tc::mbar_init(&pv_done[s], 1);
     }
-    tc::mbar_init(ml_ready, 4 * C);  // the four column-half-0 warps of every split
+    tc::mbar_init(ml_ready, 4 * C);  // the four group-0 warps of every split
     *abort_flag = 0;
     *any_window = 0;
     tc::fence_mbar_init();
@@ -363,19 +370,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // slot of key tile j's first key; an unmapped page points past the cache
   // so the TMA zero-fills the tile (and the error word says so)
-  auto tile_slot = [&](int j, bool report) -> int {
+  auto tile_slot = [&](int j) -> int {
     const int c0 = j * kBN;
     const int pi = c0 / p.page_size;
     const int page = pi < p.bt_stride ? p.block_table[(size_t)b * p.bt_stride + pi] : -1;
     if (page >= 0 && page < p.n_pages) return page * p.page_size + c0 % p.page_size;
-    if (report) fdl::raise_error(p.err, FDL_DEVERR_INDEX);
+    fdl::raise_error(p.err, FDL_DEVERR_INDEX);
     return p.n_slots;
   };
 
-  const int pre = min(n_my, kKS);  // pass-A key tiles issued before the CTA barrier
+  const int pre = min(n_my, kKS);  // key tiles issued before the CTA barrier
   if (warp == 0) {
     // every key tile's slot, looked up once by the whole warp
-    for (int i = lane; i < n_my; i += 32) slots[i] = tile_slot(t0 + i, true);
+    for (int i = lane; i < n_my; i += 32) slots[i] = tile_slot(t0 + i);
     __syncwarp();
     if (lane == 0 && n_my > 0) {
       // Q and the first ring of key tiles need no free slot: the producer
@@ -390,6 +397,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tma_load_2d(st + KT_BYTES / 2, &tm_k, h * kHD + 64, slots[lc], &k_full[lc]);
       }
     }
+  } else if (softmax_warp) {
+    // row kinds (they decide the item's mode, so every warp needs them after
+    // the barrier), a cleared search bitmap and cleared tracker column sums
+    for (int r = t_local; r < kBM; r += 256) {
+      int k = -1;
+      if (r < qlen) {
+        k = p.row_kind[q0 + r];
+        if (k >= 2 && ((k - 2) >> 1) >= m_search) {
+          fdl::raise_error(p.err, FDL_DEVERR_SHAPE);
+          k = -1;
+        }
+      }
+      kinds[r] = k;
+      if (k == FDL_KIND_WINDOW) *any_window = 1;
+    }
+    for (int w = t_local; w < p.bitmap_words; w += 256) bitmap[w] = 0u;
+    if (t_local < 128) colacc[t_local] = 0.f;
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -398,15 +422,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   // thread arrives now and waits just before its first remote access
   if (C > 1) tc::cluster_arrive();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tm_o = tmem;            // columns [0, 128)
-  const uint32_t tm_s = tmem + 128;      // kSB 64-column S buffers
+  const uint32_t tm_s = tmem + 256;  // kSB 64-column S buffers; O accumulators at 0 and 128
   const bool do_track = p.track != nullptr && p.n_masked[b] > 0;
+  const bool track_item = do_track && *any_window != 0;
+  // Split items and items that feed the tracker take two exact passes; the
+  // others one online pass.
+  const bool two_pass = C > 1 || track_item;
+  // A two-pass item whose tiles all fit in the S buffers keeps pass A's
+  // scores in TMEM for pass B instead of reloading K and recomputing them.
+  const bool keep_s = two_pass && n_my <= kSB;
+  const int n_s = two_pass && !keep_s ? 2 * n_my : n_my;  // S products = K tile loads
 
   if (warp == 0) {
     // ------------------------------------------------------------ K producer
-    // K load lc = 0 .. 2 n_my - 1: key tile lc % n_my, for pass A then pass B
+    // K load lc = 0 .. n_s - 1: key tile lc % n_my (pass A, then pass B)
     if (lane == 0 && n_my > 0) {
-      for (int lc = pre; lc < 2 * n_my; ++lc) {
+      for (int lc = pre; lc < n_s; ++lc) {
         const int s = lc % kKS;
         if (!tc::mbar_wait(&k_empty[s], ((uint32_t)(lc / kKS) & 1u) ^ 1u, abort_flag)) break;
         const int slot = slots[lc % n_my];
@@ -435,54 +466,59 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (C > 1) tc::cluster_wait();  // matches the setup arrive
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Issues whichever product is ready: O_g += P V for the next tile whose P
+    // and V have landed (first, since it frees a P tile), else the next S =
+    // Q K^T whose K tile and S buffer are free. Neither kind waits for the
+    // other, so a late K load never holds back a P V product.
     if (lane == 0 && n_my > 0) {
       constexpr uint32_t id_s = tc::idesc_bf16_f32(kBM, kBN);
       constexpr uint32_t id_pv = idesc_pv(kBM, kHD);
       const uint32_t aq = tc::smem_addr(sq);
       const uint32_t ap = tc::smem_addr(sp);
       bool ok = tc::mbar_wait(q_full, 0, abort_flag);
-      int sc = 0;
-      // S #sc = Q K(load_idx)^T into TMEM buffer sc % kSB; the K stage is
-      // released as soon as the product finishes
-      auto issue_s = [&](int load_idx) -> bool {
-        const int s = load_idx % kKS;
-        if (!tc::mbar_wait(&k_full[s], (uint32_t)(load_idx / kKS) & 1u, abort_flag)) return false;
-        const int sb = sc % kSB;
-        if (sc >= kSB && !tc::mbar_wait(&s_free[sb], (uint32_t)((sc - kSB) / kSB) & 1u, abort_flag)) return false;
-        tc::fence_after_sync();
-        const uint32_t ak = tc::smem_addr(kring + s * KT_BYTES);
+      int si = 0, pi = 0;
+      long long t_last = clock64();
+      while (ok && pi < n_my) {
+        bool progressed = false;
+        if (tc::mbar_try_wait(&p_full[pi & 1], (uint32_t)(pi >> 1) & 1u) &&
+            tc::mbar_try_wait(&v_full[pi % kVS], (uint32_t)(pi / kVS) & 1u)) {
+          tc::fence_after_sync();
+          const int g = pi & 1;
+          const uint32_t av = tc::smem_addr(vring + (pi % kVS) * VT_BYTES);
+          const uint32_t apg = ap + (uint32_t)(g * P_BYTES);
 #pragma unroll
-        for (int k = 0; k < kHD / 16; ++k) {
-          const uint32_t half = (uint32_t)(k >> 2), kk = (uint32_t)(k & 3) * 32u;
-          tc::mma_bf16_ss(tm_s + 64 * sb, tc::desc_kmajor_sw128(aq + half * (Q_BYTES / 2) + kk),
-                          tc::desc_kmajor_sw128(ak + half * (KT_BYTES / 2) + kk), id_s, k > 0 ? 1u : 0u);
+          for (int k = 0; k < kBN / 16; ++k)
+            tc::mma_bf16_ss(tmem + 128 * g, tc::desc_kmajor_sw128(apg + k * 32),
+                            desc_mnmajor_sw128(av + k * 2048, VT_BYTES / 2), id_pv, (pi >= 2 || k > 0) ? 1u : 0u);
+          tc::mma_commit(&pv_done[g]);
+          tc::mma_commit(&v_empty[pi % kVS]);
+          ++pi;
+          progressed = true;
         }
-        tc::mma_commit(&s_full[sb]);
-        tc::mma_commit(&k_empty[s]);
-        ++sc;
-        return true;
-      };
-      // pass A: scores only
-      for (int i = 0; ok && i < n_my; ++i) ok = issue_s(i);
-      // pass B: S(i+1) is issued before O += P(i) V(i) so the softmax overlaps
-      const int lb = n_my;
-      for (int i = 0; ok && i < min(kLook, n_my); ++i) ok = issue_s(lb + i);
-      for (int i = 0; ok && i < n_my; ++i) {
-        if (i + kLook < n_my) ok = issue_s(lb + i + kLook);
-        if (!ok) break;
-        const int pb = i & 1;
-        if (!tc::mbar_wait(&p_full[pb], (uint32_t)(i >> 1) & 1u, abort_flag)) break;
-        const int s = i % kVS;
-        if (!tc::mbar_wait(&v_full[s], (uint32_t)(i / kVS) & 1u, abort_flag)) break;
-        tc::fence_after_sync();
-        const uint32_t av = tc::smem_addr(vring + s * VT_BYTES);
-        const uint32_t apb = ap + (uint32_t)(pb * P_BYTES);
+        if (si < n_s && tc::mbar_try_wait(&k_full[si % kKS], (uint32_t)(si / kKS) & 1u) &&
+            (si < kSB || tc::mbar_try_wait(&s_free[si % kSB], (uint32_t)((si - kSB) / kSB) & 1u))) {
+          tc::fence_after_sync();
+          const int sb = si % kSB;
+          const uint32_t ak = tc::smem_addr(kring + (si % kKS) * KT_BYTES);
 #pragma unroll
-        for (int k = 0; k < kBN / 16; ++k)
-          tc::mma_bf16_ss(tm_o, tc::desc_kmajor_sw128(apb + k * 32), desc_mnmajor_sw128(av + k * 2048, VT_BYTES / 2),
-                          id_pv, (i > 0 || k > 0) ? 1u : 0u);
-        tc::mma_commit(&pv_done[pb]);
-        tc::mma_commit(&v_empty[s]);
+          for (int k = 0; k < kHD / 16; ++k) {
+            const uint32_t half = (uint32_t)(k >> 2), kk = (uint32_t)(k & 3) * 32u;
+            tc::mma_bf16_ss(tm_s + 64 * sb, tc::desc_kmajor_sw128(aq + half * (Q_BYTES / 2) + kk),
+                            tc::desc_kmajor_sw128(ak + half * (KT_BYTES / 2) + kk), id_s, k > 0 ? 1u : 0u);
+          }
+          tc::mma_commit(&s_full[sb]);
+          tc::mma_commit(&k_empty[si % kKS]);
+          ++si;
+          progressed = true;
+        }
+        if (progressed) {
+          t_last = clock64();
+        } else if (*abort_flag) {
+          ok = false;
+        } else if (clock64() - t_last > tc::kWaitBudgetCycles) {
+          *abort_flag = 1;
+          ok = false;
+        }
       }
     }
     __syncwarp();
@@ -490,192 +526,224 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ------------------------------------------------------------ softmax warps
-  // Eight warps: warp w in [2, 10) owns TMEM lane quadrant w % 4 (32 query
-  // rows) and key columns [32 ch, 32 ch + 32) of every 64-key tile, with
-  // ch = (w - 2) / 4, so two warps share each sub-partition's issue slots.
+  // Two groups of four warps; group g takes the key tiles i with i % 2 == g
+  // (all 64 columns of each), accumulates into its own O_g in TMEM and writes
+  // its own P tile, so the two groups' tiles overlap. Warp w owns TMEM lane
+  // quadrant w % 4 (32 query rows).
   const int qd = warp & 3;
-  const int ch = (warp - 2) >> 2;
+  const int g = (warp - 2) >> 2;
   const int row = qd * 32 + lane;
   const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
-  const int t_local = threadIdx.x - 64;  // 0..255 over the softmax warps
-  const bool softmax_warp = warp >= 2 && warp < 10;
+  const uint32_t tm_og = tmem + 128 * (uint32_t)g;  // this group's O accumulator
+  const int n_g = (n_my + 1 - g) / 2;               // tiles of this group
+  const int n_g0 = (n_my + 1) / 2, n_g1 = n_my / 2;
   float lse2 = -INFINITY;  // log2-domain log-sum-exp of this row over all splits
-  float inv_l = 1.f;       // scale of the accumulated O (1 unless P was relative to the max)
+  float beta0 = 1.f, beta1 = 1.f, inv_l = 1.f;  // epilogue weights of O_0, O_1 and the final scale
   if (softmax_warp) {
-    // row kinds and the search-position bitmap, read only by these warps
-    for (int r = t_local; r < kBM; r += 256) {
-      int k = -1;
-      if (r < qlen) {
-        k = p.row_kind[q0 + r];
-        if (k >= 2 && ((k - 2) >> 1) >= m_search) {
-          fdl::raise_error(p.err, FDL_DEVERR_SHAPE);
-          k = -1;
-        }
-      }
-      kinds[r] = k;
-      if (k == FDL_KIND_WINDOW) *any_window = 1;
-    }
-    for (int w = t_local; w < p.bitmap_words; w += 256) bitmap[w] = 0u;
-    if (t_local < 64) colacc[t_local] = 0.f;
-    tc::named_bar(3, 256);
     for (int j = t_local; j < m_search; j += 256) {
       const int s = p.search_pos[(size_t)b * p.search_ld + j];
       if (s >= 0 && s < kvl && (s >> 5) < p.bitmap_words) atomicOr(&bitmap[s >> 5], 1u << (s & 31));
     }
     tc::named_bar(3, 256);
     const int kind = kinds[row];
-    // items with masked-window rows feed the tracker and need the final
-    // probabilities in pass B; so do split items (their O partials are
-    // summed over the cluster). The flag is the same for every softmax warp
-    // (any_window was set before barrier 3).
-    const bool track_item = do_track && *any_window != 0;
-    const bool max_only = C == 1 && !track_item;
-    float mrow = -INFINITY, lrow = 0.f;
-    int sc = 0;
-    // ---- pass A: running max (and, unless max_only, sum) over this warp's columns
-    for (int i = 0; i < n_my; ++i, ++sc) {
+
+    // S of tile sc (global S index) into x[64]. Waits for the product and
+    // releases the S buffer afterwards, except where keep_s holds the scores
+    // for pass B: pass A then only waits, pass B (second) neither.
+    auto load_s = [&](int sc, float (&x)[64], bool second) -> bool {
       const int sb = sc % kSB;
       // tcgen05.ld is warp-collective: the whole warp proceeds or none of it
-      if (!__all_sync(0xffffffffu, tc::mbar_wait(&s_full[sb], (uint32_t)(sc / kSB) & 1u, abort_flag))) break;
+      if (!second &&
+          !__all_sync(0xffffffffu, tc::mbar_wait(&s_full[sb], (uint32_t)(sc / kSB) & 1u, abort_flag)))
+        return false;
       tc::fence_after_sync();
-      float x[32];
-      tc::tmem_ld_32x32b_x32(tm_s + 64 * sb + 32 * ch + lane_off, x);
+      tc::tmem_ld_32x32b_x64(tm_s + 64 * sb + lane_off, x);
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&s_free[sb]);
-      const uint32_t vm = vis_mask(kind, (t0 + i) * kBN + 32 * ch, kvl, m_search, bitmap, p.bitmap_words);
+      if (!keep_s && lane == 0) tc::mbar_arrive(&s_free[sb]);
+      return true;
+    };
+    // scaled scores of the visible keys, -inf elsewhere; returns the tile max
+    auto mask_scale = [&](int c0, float (&x)[64]) -> float {
+      const uint32_t vm0 = vis_mask(kind, c0, kvl, m_search, bitmap, p.bitmap_words);
+      const uint32_t vm1 = vis_mask(kind, c0 + 32, kvl, m_search, bitmap, p.bitmap_words);
+      if ((vm0 & vm1) == 0xffffffffu) {
 #pragma unroll
-      for (int k = 0; k < 32; ++k) x[k] = ((vm >> k) & 1u) ? x[k] * p.scale_log2 : -INFINITY;
+        for (int k = 0; k < 64; ++k) x[k] *= p.scale_log2;
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          x[k] = ((vm0 >> k) & 1u) ? x[k] * p.scale_log2 : -INFINITY;
+          x[k + 32] = ((vm1 >> k) & 1u) ? x[k + 32] * p.scale_log2 : -INFINITY;
+        }
+      }
       float t16[16];
 #pragma unroll
-      for (int k = 0; k < 16; ++k) t16[k] = fmaxf(x[k], x[k + 16]);
+      for (int k = 0; k < 16; ++k) t16[k] = fmaxf(fmaxf(x[k], x[k + 16]), fmaxf(x[k + 32], x[k + 48]));
 #pragma unroll
       for (int w = 8; w >= 1; w >>= 1)
 #pragma unroll
         for (int k = 0; k < w; ++k) t16[k] = fmaxf(t16[k], t16[k + w]);
-      const float tmax = t16[0];
-      if (tmax == -INFINITY) continue;
-      const float mnew = fmaxf(mrow, tmax);
-      if (max_only) {
-        mrow = mnew;
-        continue;
-      }
-      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-      for (int k = 0; k < 32; k += 4) {
-        a0 += ex2(x[k] - mnew);
-        a1 += ex2(x[k + 1] - mnew);
-        a2 += ex2(x[k + 2] - mnew);
-        a3 += ex2(x[k + 3] - mnew);
-      }
-      lrow = (mrow == -INFINITY ? 0.f : lrow * ex2(mrow - mnew)) + ((a0 + a1) + (a2 + a3));
-      mrow = mnew;
-    }
-    // ---- the two column halves of each row combine their (max, sum); a
-    // max_only pass A publishes only the max (slot 0), and its pass B the
-    // sum (slot 1), so the partner's slot-0 read never races a slot-1 write
-    halfml[(ch * kBM + row) * 2] = mrow;
-    if (!max_only) halfml[(ch * kBM + row) * 2 + 1] = lrow;
-    tc::named_bar(2, 256);
-    if (max_only) {
-      mrow = fmaxf(mrow, halfml[((1 - ch) * kBM + row) * 2]);
-    } else {
-      const float mo = halfml[((1 - ch) * kBM + row) * 2], lo = halfml[((1 - ch) * kBM + row) * 2 + 1];
-      const float mm = fmaxf(mrow, mo);
-      float ll = 0.f;
-      if (mm != -INFINITY) {
-        if (mrow != -INFINITY) ll += lrow * ex2(mrow - mm);
-        if (mo != -INFINITY) ll += lo * ex2(mo - mm);
-      }
-      mrow = mm;
-      lrow = ll;
-    }
-    // ---- combine (max, sum) over the cluster
-    if (C > 1) {
-      tc::cluster_wait();  // peers have initialised their barriers (setup arrive)
-      if (ch == 0) {
-        // push this row's (max, sum) into every split, then release-arrive there
-        const uint32_t mine = tc::smem_addr(ml + ((size_t)rank * kBM + row) * 2);
-        for (int r = 0; r < C; ++r) st_cluster_v2(tc::map_cluster(mine, (uint32_t)r), mrow, lrow);
-        // one release-arrive per warp and destination: every lane's remote
-        // stores are ordered before lane 0's arrive by its cluster-scope
-        // fence and the warp barrier
-        fence_acq_rel_cluster();
-        __syncwarp();
-        if (lane == 0)
-          for (int r = 0; r < C; ++r) mbar_arrive_remote(ml_ready, (uint32_t)r);
-      }
-      mbar_wait_cluster(ml_ready, 0, abort_flag);
-      float mm = -INFINITY;
-      for (int r = 0; r < C; ++r) mm = fmaxf(mm, ml[((size_t)r * kBM + row) * 2]);
-      float ll = 0.f;
-      if (mm != -INFINITY)
-        for (int r = 0; r < C; ++r) {
-          const float mr = ml[((size_t)r * kBM + row) * 2], lr = ml[((size_t)r * kBM + row) * 2 + 1];
-          if (mr != -INFINITY) ll += lr * ex2(mr - mm);
-        }
-      lse2 = ll > 0.f ? mm + log2f(ll) : -INFINITY;
-    } else if (!max_only) {
-      lse2 = lrow > 0.f ? mrow + log2f(lrow) : -INFINITY;
-    }
-    if (p.lse && !max_only && rank == 0 && ch == 0 && row < qlen) p.lse[(size_t)(q0 + row) * p.H + h] = lse2 * kLn2;
+      return t16[0];
+    };
 
-    // ---- pass B: probabilities (final, or relative to the row max when
-    // max_only), P V, tracker column sums
-    const float sub = max_only ? mrow : lse2;  // exponent offset of P
-    float ps0 = 0.f, ps1 = 0.f, ps2 = 0.f, ps3 = 0.f;  // max_only: row sums of P
+    float m_run = -INFINITY, l_run = 0.f;
+    if (two_pass) {
+      // ---- pass A: exact running max and sum over this group's tiles
+      for (int k = 0; k < n_g; ++k) {
+        const int i = 2 * k + g;
+        float x[64];
+        if (!load_s(i, x, false)) break;
+        const float tmax = mask_scale((t0 + i) * kBN, x);
+        if (tmax == -INFINITY) continue;
+        const float mnew = fmaxf(m_run, tmax);
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+        for (int e = 0; e < 64; e += 4) {
+          a0 += ex2(x[e] - mnew);
+          a1 += ex2(x[e + 1] - mnew);
+          a2 += ex2(x[e + 2] - mnew);
+          a3 += ex2(x[e + 3] - mnew);
+        }
+        l_run = (m_run == -INFINITY ? 0.f : l_run * ex2(m_run - mnew)) + ((a0 + a1) + (a2 + a3));
+        m_run = mnew;
+      }
+      // ---- the two groups of each row combine their (max, sum)
+      halfml[(g * kBM + row) * 2] = m_run;
+      halfml[(g * kBM + row) * 2 + 1] = l_run;
+      tc::named_bar(2, 256);
+      float mrow, lrow;
+      {
+        const float mo = halfml[((1 - g) * kBM + row) * 2], lo = halfml[((1 - g) * kBM + row) * 2 + 1];
+        mrow = fmaxf(m_run, mo);
+        lrow = 0.f;
+        if (mrow != -INFINITY) {
+          if (m_run != -INFINITY) lrow += l_run * ex2(m_run - mrow);
+          if (mo != -INFINITY) lrow += lo * ex2(mo - mrow);
+        }
+      }
+      // ---- combine (max, sum) over the cluster
+      if (C > 1) {
+        tc::cluster_wait();  // peers have initialised their barriers (setup arrive)
+        if (g == 0) {
+          // push this row's (max, sum) into every split, then release-arrive there
+          const uint32_t mine = tc::smem_addr(ml + ((size_t)rank * kBM + row) * 2);
+          for (int r = 0; r < C; ++r) st_cluster_v2(tc::map_cluster(mine, (uint32_t)r), mrow, lrow);
+          // one release-arrive per warp and destination: every lane's remote
+          // stores are ordered before lane 0's arrive by its cluster-scope
+          // fence and the warp barrier
+          fence_acq_rel_cluster();
+          __syncwarp();
+          if (lane == 0)
+            for (int r = 0; r < C; ++r) mbar_arrive_remote(ml_ready, (uint32_t)r);
+        }
+        mbar_wait_cluster(ml_ready, 0, abort_flag);
+        float mm = -INFINITY;
+        for (int r = 0; r < C; ++r) mm = fmaxf(mm, ml[((size_t)r * kBM + row) * 2]);
+        float ll = 0.f;
+        if (mm != -INFINITY)
+          for (int r = 0; r < C; ++r) {
+            const float mr = ml[((size_t)r * kBM + row) * 2], lr = ml[((size_t)r * kBM + row) * 2 + 1];
+            if (mr != -INFINITY) ll += lr * ex2(mr - mm);
+          }
+        lse2 = ll > 0.f ? mm + log2f(ll) : -INFINITY;
+      } else {
+        lse2 = lrow > 0.f ? mrow + log2f(lrow) : -INFINITY;
+      }
+      if (p.lse && rank == 0 && g == 0 && row < qlen) p.lse[(size_t)(q0 + row) * p.H + h] = lse2 * kLn2;
+      m_run = -INFINITY;
+      l_run = 0.f;
+    }
+
+    // ---- pass B (two_pass: final probabilities P = exp(S - lse)) or the one
+    // online pass (P = exp(S - m) against a running row max m that moves only
+    // when a tile's max exceeds it by more than kRescale; O_g and the row sum
+    // are then scaled down to the new m)
+    const int sc0 = two_pass && !keep_s ? n_my : 0;
     const float wscale = do_track ? 1.f / ((float)p.H * (float)p.n_masked[b]) : 0.f;
     const bool track_row = do_track && kind == FDL_KIND_WINDOW;
     const bool track_warp = __any_sync(0xffffffffu, track_row);
-    for (int i = 0; i < n_my; ++i, ++sc) {
+    const int t_g = t_local - 128 * g;  // 0..127 within the group
+    for (int k = 0; k < n_g; ++k) {
       // a wait that gives up (abort) skips the work but never the barriers
-      const int sb = sc % kSB;
-      bool ok = __all_sync(0xffffffffu, tc::mbar_wait(&s_full[sb], (uint32_t)(sc / kSB) & 1u, abort_flag));
-      float pr[32];
+      const int i = 2 * k + g;
       const int c0 = (t0 + i) * kBN;
+      float pr[64];
+      bool ok = load_s(sc0 + i, pr, keep_s);
+      bool waited_pv = false;
       if (ok) {
-        tc::fence_after_sync();
-        tc::tmem_ld_32x32b_x32(tm_s + 64 * sb + 32 * ch + lane_off, pr);
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&s_free[sb]);
-        const uint32_t vm =
-            sub != -INFINITY ? vis_mask(kind, c0 + 32 * ch, kvl, m_search, bitmap, p.bitmap_words) : 0u;
-        if (vm == 0xffffffffu) {
+        if (two_pass) {
+          if (lse2 == -INFINITY) {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) pr[k] = ex2(fmaf(pr[k], p.scale_log2, -sub));
+            for (int e = 0; e < 64; ++e) pr[e] = 0.f;
+          } else {
+            mask_scale(c0, pr);
+#pragma unroll
+            for (int e = 0; e < 64; ++e) pr[e] = ex2(pr[e] - lse2);
+          }
         } else {
-          // ex2(-inf) = 0 for the hidden keys
+          const float tmax = mask_scale(c0, pr);
+          float alpha = 1.f;
+          bool resc = false;
+          if (tmax != -INFINITY) {
+            if (m_run == -INFINITY) {
+              m_run = tmax;  // this row's O_g holds only zeros so far
+            } else if (tmax > m_run + kRescale) {
+              alpha = ex2(m_run - tmax);
+              m_run = tmax;
+              resc = true;
+            }
+          }
+          if (m_run == -INFINITY) {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) pr[k] = ex2(((vm >> k) & 1u) ? fmaf(pr[k], p.scale_log2, -sub) : -INFINITY);
-        }
-        if (max_only) {
+            for (int e = 0; e < 64; ++e) pr[e] = 0.f;
+          } else {
 #pragma unroll
-          for (int k = 0; k < 32; k += 4) {
-            ps0 += pr[k];
-            ps1 += pr[k + 1];
-            ps2 += pr[k + 2];
-            ps3 += pr[k + 3];
+            for (int e = 0; e < 64; ++e) pr[e] = ex2(pr[e] - m_run);
+          }
+          float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+          for (int e = 0; e < 64; e += 4) {
+            s0 += pr[e];
+            s1 += pr[e + 1];
+            s2 += pr[e + 2];
+            s3 += pr[e + 3];
+          }
+          l_run = l_run * alpha + ((s0 + s1) + (s2 + s3));
+          if (__any_sync(0xffffffffu, resc)) {
+            // O_g rows move to the new max once the group's previous P V
+            // product (tile i - 2) has finished and before this tile's starts
+            ok = i < 2 || __all_sync(0xffffffffu, tc::mbar_wait(&pv_done[g], (uint32_t)((i - 2) >> 1) & 1u, abort_flag));
+            waited_pv = true;
+            if (ok && i >= 2) {
+              tc::fence_after_sync();
+#pragma unroll 1
+              for (int cc = 0; cc < kHD; cc += 32) {
+                float o[32];
+                tc::tmem_ld_32x32b_x32(tm_og + cc + lane_off, o);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                tc::tmem_st_32x32b_x32(tm_og + cc + lane_off, o);
+              }
+              tc::tmem_wait_st();
+            }
           }
         }
       } else {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) pr[k] = 0.f;
+        for (int e = 0; e < 64; ++e) pr[e] = 0.f;
       }
-      // P tile i & 1 was last read by the P V product of tile i - 2
-      const int pb = i & 1;
-      ok = ok && (i < 2 || tc::mbar_wait(&pv_done[pb], (uint32_t)((i - 2) >> 1) & 1u, abort_flag));
+      // P tile g was last read by the P V product of tile i - 2
+      if (!waited_pv) ok = ok && (i < 2 || tc::mbar_wait(&pv_done[g], (uint32_t)((i - 2) >> 1) & 1u, abort_flag));
       if (ok) {
-        // P in the 128-byte swizzled K-major layout: row r, 16-byte chunk q at q ^ (r & 7);
-        // this warp writes chunks 4 ch .. 4 ch + 3 (its 32 keys)
-        uint8_t* prow = sp + pb * P_BYTES + row * 128;
+        // P in the 128-byte swizzled K-major layout: row r, 16-byte chunk q at q ^ (r & 7)
+        uint8_t* prow = sp + g * P_BYTES + row * 128;
 #pragma unroll
-        for (int qq = 0; qq < 4; ++qq) {
-          const int q = 4 * ch + qq;
+        for (int q = 0; q < 8; ++q) {
           uint32_t w[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(pr[qq * 8 + 2 * e], pr[qq * 8 + 2 * e + 1]);
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(pr[q * 8 + 2 * e], pr[q * 8 + 2 * e + 1]);
             w[e] = *reinterpret_cast<uint32_t*>(&h2);
           }
           *reinterpret_cast<uint4*>(prow + ((q ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -687,64 +755,96 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int first = max(0, nkeys - c0);
           for (int e = lane; e < (kBN - first) * 16; e += 32) {
             const int r = first + e / 16, part = e % 16;
-            if ((r & 7) != warp - 2) continue;  // the eight warps split the rows
+            if ((r & 3) != qd) continue;  // the group's four warps split the rows
             *reinterpret_cast<uint4*>(vt + (part >> 3) * (VT_BYTES / 2) + r * 128 + (part & 7) * 16) =
                 make_uint4(0u, 0u, 0u, 0u);
           }
         }
         fence_proxy_async_smem();
+        tc::fence_before_sync();
       }
       __syncwarp();
-      if (ok && lane == 0) tc::mbar_arrive(&p_full[pb]);
-      if (track_item) {
+      if (ok && lane == 0) tc::mbar_arrive(&p_full[g]);
+      if (two_pass && track_item) {
         if (track_warp) {  // a warp without WINDOW rows adds nothing
           if (!track_row) {
 #pragma unroll
-            for (int k = 0; k < 32; ++k) pr[k] = 0.f;
+            for (int e = 0; e < 64; ++e) pr[e] = 0.f;
           }
-          warp_colsum32(pr, lane);
-          atomicAdd(&colacc[32 * ch + lane], pr[0]);
+          float* lo = pr;
+          float* hi = pr + 32;
+          warp_colsum32(*reinterpret_cast<float(*)[32]>(lo), lane);
+          warp_colsum32(*reinterpret_cast<float(*)[32]>(hi), lane);
+          atomicAdd(&colacc[g * 64 + lane], pr[0]);
+          atomicAdd(&colacc[g * 64 + 32 + lane], pr[32]);
         }
-        tc::named_bar(1, 256);
-        if (t_local < 64) {
-          const int c = c0 + t_local;
-          const float v = colacc[t_local];
-          colacc[t_local] = 0.f;
+        tc::named_bar(4 + g, 128);
+        if (t_g < 64) {
+          const int c = c0 + t_g;
+          const float v = colacc[g * 64 + t_g];
+          colacc[g * 64 + t_g] = 0.f;
           if (c < kvl && v != 0.f) atomicAdd(p.track + (size_t)b * p.track_ld + c, v * wscale);
         }
-        tc::named_bar(1, 256);
+        tc::named_bar(4 + g, 128);
       }
     }
-    if (max_only) {
-      // the two column halves' sums of P give the row's normaliser
-      const float lmine = (ps0 + ps1) + (ps2 + ps3);
-      halfml[(ch * kBM + row) * 2 + 1] = lmine;
-      tc::named_bar(2, 256);
-      const float l = lmine + halfml[((1 - ch) * kBM + row) * 2 + 1];
-      lse2 = (mrow != -INFINITY && l > 0.f) ? mrow + log2f(l) : -INFINITY;
-      inv_l = lse2 != -INFINITY ? 1.f / l : 0.f;
-      if (p.lse && ch == 0 && row < qlen) p.lse[(size_t)(q0 + row) * p.H + h] = lse2 * kLn2;
+    // Every P V product of both groups has finished before O is read: each
+    // group waits for its own last product (a parity wait is exact only one
+    // phase ahead, which holds for the group that waited on the earlier
+    // phases), then the two groups meet at barrier 2.
+    if (n_g > 0) tc::mbar_wait(&pv_done[g], (uint32_t)(n_g - 1) & 1u, abort_flag);
+    if (!two_pass) {
+      halfml[(g * kBM + row) * 2] = m_run;
+      halfml[(g * kBM + row) * 2 + 1] = l_run;
     }
-    if (n_my > 0) tc::mbar_wait(&pv_done[(n_my - 1) & 1], (uint32_t)((n_my - 1) >> 1) & 1u, abort_flag);
+    tc::fence_before_sync();
+    tc::named_bar(2, 256);
     tc::fence_after_sync();
+    if (!two_pass) {
+      // the two groups' (max, sum) give the row's normaliser and the weights of O_0, O_1
+      const float m0 = halfml[row * 2], l0 = halfml[row * 2 + 1];
+      const float m1 = halfml[(kBM + row) * 2], l1 = halfml[(kBM + row) * 2 + 1];
+      const float m = fmaxf(m0, m1);
+      if (m != -INFINITY) {
+        beta0 = m0 != -INFINITY ? ex2(m0 - m) : 0.f;
+        beta1 = m1 != -INFINITY ? ex2(m1 - m) : 0.f;
+        const float l = l0 * beta0 + l1 * beta1;
+        lse2 = l > 0.f ? m + log2f(l) : -INFINITY;
+        inv_l = l > 0.f ? 1.f / l : 0.f;
+      }
+      if (p.lse && g == 0 && row < qlen) p.lse[(size_t)(q0 + row) * p.H + h] = lse2 * kLn2;
+    }
+    if (n_g0 == 0) beta0 = 0.f;  // an accumulator no product wrote holds garbage
+    if (n_g1 == 0) beta1 = 0.f;
   }
 
   // ------------------------------------------------------------ output
-  // Each softmax warp owns O columns [64 ch, 64 ch + 64) of its 32 rows. TMEM
-  // loads are warp-collective: issued by whole warps (n_my is uniform), with
-  // per-row conditions only selecting values and guarding stores.
+  // Each softmax warp owns O columns [64 g, 64 g + 64) of its 32 rows and
+  // combines O_0 and O_1 there. TMEM loads are warp-collective: issued by
+  // whole warps, with per-row conditions only selecting values and guarding
+  // stores.
   constexpr int kOStride = kHD + 4;  // padded fp32 staging rows: conflict-free float4 access
+  auto o_cols = [&](int c0, float (&a)[32]) {
+    float o1[32];
+    tc::tmem_ld_32x32b_x32(tmem + c0 + lane_off, a);
+    tc::tmem_ld_32x32b_x32(tmem + 128 + c0 + lane_off, o1);
+    const bool live = n_my > 0 && lse2 != -INFINITY;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const float v0 = beta0 != 0.f ? a[e] * beta0 : 0.f;
+      const float v1 = beta1 != 0.f ? o1[e] * beta1 : 0.f;
+      a[e] = live ? (v0 + v1) * inv_l : 0.f;
+    }
+  };
   if (C == 1) {
     if (softmax_warp) {
       const bool store = row < qlen && !*abort_flag;
       __nv_bfloat16* orow = p.o + (size_t)(q0 + row) * p.d + h * kHD;
-#pragma unroll
+#pragma unroll 1
       for (int cc = 0; cc < 64; cc += 32) {
-        const int c0 = 64 * ch + cc;
+        const int c0 = 64 * g + cc;
         float a[32];
-        if (n_my > 0) tc::tmem_ld_32x32b_x32(tm_o + c0 + lane_off, a);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) a[e] = (n_my > 0 && lse2 != -INFINITY) ? a[e] * inv_l : 0.f;
+        o_cols(c0, a);
         if (!store) continue;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -764,13 +864,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // splits in rank order
     float* ostage = reinterpret_cast<float*>(kring);  // [128][kOStride], over both rings
     if (softmax_warp) {
-#pragma unroll
+#pragma unroll 1
       for (int cc = 0; cc < 64; cc += 32) {
-        const int c0 = 64 * ch + cc;
+        const int c0 = 64 * g + cc;
         float a[32];
-        if (n_my > 0) tc::tmem_ld_32x32b_x32(tm_o + c0 + lane_off, a);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) a[e] = (n_my > 0 && lse2 != -INFINITY) ? a[e] : 0.f;
+        o_cols(c0, a);
 #pragma unroll
         for (int q = 0; q < 8; ++q)
           *reinterpret_cast<float4*>(ostage + row * kOStride + c0 + 4 * q) =
