@@ -302,7 +302,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* colacc = reinterpret_cast<float*>(misc + OFF_COLACC);      // [2][64]
   uint32_t* bitmap = reinterpret_cast<uint32_t*>(misc + OFF_BITMAP);  // [bitmap_words] (<= 768)
   float* halfml = reinterpret_cast<float*>(misc + OFF_HALFML);      // [2][128][2]
-  volatile int* any_window = reinterpret_cast<volatile int*>(misc + OFF_FLAGS);  // item has WINDOW rows
+  // per row-staging warp: its 32 rows hold a WINDOW row (written by that
+  // warp alone, so nothing has to clear it first)
+  int* win_flags = reinterpret_cast<int*>(misc + OFF_FLAGS);  // [4]
   int* slots = reinterpret_cast<int*>(misc + OFF_SLOTS);            // [n_my] cache slot of each key tile
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -337,7 +339,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc::mbar_init(ml_ready, 4 * C);  // the four group-0 warps of every split
     *abort_flag = 0;
-    *any_window = 0;
     tc::fence_mbar_init();
     tc::prefetch_tensormap(&tm_q);
     tc::prefetch_tensormap(&tm_k);
@@ -400,7 +401,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (softmax_warp) {
     // row kinds (they decide the item's mode, so every warp needs them after
     // the barrier), a cleared search bitmap and cleared tracker column sums
-    for (int r = t_local; r < kBM; r += 256) {
+    if (t_local < kBM) {  // warps 2-5, one row per thread
+      const int r = t_local;
       int k = -1;
       if (r < qlen) {
         k = p.row_kind[q0 + r];
@@ -410,7 +412,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       kinds[r] = k;
-      if (k == FDL_KIND_WINDOW) *any_window = 1;
+      const bool w = __any_sync(0xffffffffu, k == FDL_KIND_WINDOW);
+      if (lane == 0) win_flags[r >> 5] = w ? 1 : 0;
     }
     for (int w = t_local; w < p.bitmap_words; w += 256) bitmap[w] = 0u;
     if (t_local < 128) colacc[t_local] = 0.f;
@@ -424,7 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const uint32_t tm_s = tmem + 256;  // kSB 64-column S buffers; O accumulators at 0 and 128
   const bool do_track = p.track != nullptr && p.n_masked[b] > 0;
-  const bool track_item = do_track && *any_window != 0;
+  const bool any_window = (win_flags[0] | win_flags[1] | win_flags[2] | win_flags[3]) != 0;
+  const bool track_item = do_track && any_window;
   // Split items and items that feed the tracker take two exact passes; the
   // others one online pass.
   const bool two_pass = C > 1 || track_item;

@@ -209,8 +209,9 @@ topk_kernel(const float* __restrict__ scores, const unsigned char* __restrict__ 
   __shared__ unsigned skey[kStage];
   __shared__ __align__(16) unsigned hist[3][256];
   __shared__ unsigned w_cnt[kWarps], w_or[kWarps], w_and[kWarps], w_tie[kWarps];
-  __shared__ unsigned cand_key[kMaxK];
-  __shared__ int cand_pos[kMaxK];
+  // candidate (key, position) packed as key << 32 | ~position: a larger
+  // value ranks first, so ties on the key go to the lower position
+  __shared__ __align__(16) unsigned long long cand[kMaxK];
   __shared__ unsigned n_cand;
 
   const int b = blockIdx.x;
@@ -378,8 +379,7 @@ topk_kernel(const float* __restrict__ scores, const unsigned char* __restrict__ 
     if (take) {
       const unsigned slot = atomicAdd(&n_cand, 1u);
       if (slot < (unsigned)kMaxK) {
-        cand_key[slot] = key;
-        cand_pos[slot] = lo + j;
+        cand[slot] = ((unsigned long long)key << 32) | (unsigned)~(unsigned)(lo + j);
       }
     }
   }
@@ -389,13 +389,16 @@ topk_kernel(const float* __restrict__ scores, const unsigned char* __restrict__ 
   // rank every candidate by (key desc, position asc) among the candidates
   // (which hold every key that can rank above it) and scatter the first kk
   for (int c = tid; c < m; c += kThreads) {
-    const unsigned key = cand_key[c];
-    const int pos = cand_pos[c];
+    const unsigned long long v = cand[c];
+    const int pos = (int)~(unsigned)v;
+    // branch-free count of the candidates above v, two per 16-byte load (an
+    // odd count's last pair holds one candidate)
     int rank = 0;
+    const ulonglong2* c2 = reinterpret_cast<const ulonglong2*>(cand);
 #pragma unroll 4
-    for (int o = 0; o < m; ++o) {
-      const unsigned ko = cand_key[o];
-      rank += (ko > key || (ko == key && cand_pos[o] < pos)) ? 1 : 0;
+    for (int o = 0; o < (m + 1) / 2; ++o) {
+      const ulonglong2 w = c2[o];
+      rank += (int)(w.x > v) + (int)((2 * o + 1 < m) & (w.y > v));
     }
     if (rank < (int)kk) idx_out[(size_t)b * k + rank] = pos;
   }

@@ -211,7 +211,7 @@ struct RowParams {
 constexpr int kStageRows = 2048;
 constexpr int kStageSeqs = 1024;
 
-__device__ void decide_unmask(const RowParams& p) {
+__device__ void decide_unmask(const RowParams& p, const int* st_seq, const int* st_pos, const float* st_conf) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   // parameters used inside loops, read once into registers
   const int R = p.n_rows, B = p.B, max_search = p.max_search;
@@ -232,14 +232,17 @@ __device__ void decide_unmask(const RowParams& p) {
   if (ranged)
     for (int b = threadIdx.x; b < B; b += blockDim.x) s_lo[b] = s_hi[b] = 0;
   __syncthreads();
+  // rows' sequences, positions and confidences: from the caller's shared
+  // copies when given (no global round trip), else from global memory
+  const int* seq_src = st_seq ? st_seq : row_seq;
   for (int r = threadIdx.x; r < R; r += blockDim.x) {
-    const int sq = row_seq[r];
-    const int prev = r > 0 ? row_seq[r - 1] : -1;
-    const int next = r + 1 < R ? row_seq[r + 1] : B;
+    const int sq = seq_src[r];
+    const int prev = r > 0 ? seq_src[r - 1] : -1;
+    const int next = r + 1 < R ? seq_src[r + 1] : B;
     if (sq < 0 || sq >= B || next < sq) bad = 1;
     if (staged) {
-      s_conf[r] = __ldcg(out_conf + r);
-      s_pos[r] = row_pos[r];
+      s_conf[r] = st_conf ? st_conf[r] : __ldcg(out_conf + r);
+      s_pos[r] = st_pos ? st_pos[r] : row_pos[r];
     }
     if (ranged && sq >= 0 && sq < B) {  // rows are sorted by sequence (checked)
       if (prev != sq) s_lo[sq] = r;
@@ -367,10 +370,18 @@ __device__ void decide_verify(const RowParams& p) {
   }
 }
 
+// Calls with at most kThreads rows stage their decision inputs (rows'
+// sequences and positions, and the merged confidences) in shared memory of
+// the CTA that takes the decisions; every CTA loads the first two at its
+// start, since any of them may be the last to arrive.
+constexpr int kPreRows = kThreads;
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads) row_reduce_kernel(RowParams p) {
   __shared__ Stat warp_stat[kThreads / 32];
   __shared__ unsigned go;
+  __shared__ int pre_seq[kPreRows], pre_pos[kPreRows];
+  __shared__ float pre_conf[kPreRows];
   const int row = blockIdx.x / p.split;
   const int sp = blockIdx.x % p.split;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -386,6 +397,11 @@ __global__ void __launch_bounds__(kThreads) row_reduce_kernel(RowParams p) {
   };
   const bool valid = row_valid(row);
   const Stat none{-INFINITY, 0.f, 0x7fffffff};
+  const bool pre = phase == 0 && n_rows_all <= kPreRows;
+  if (pre && (int)threadIdx.x < n_rows_all) {
+    pre_seq[threadIdx.x] = p.row_seq[threadIdx.x];
+    pre_pos[threadIdx.x] = p.row_pos[threadIdx.x];
+  }
   Stat st = none;
   if (valid) {
     const T* base = reinterpret_cast<const T*>(p.logits) + (size_t)row * p.vocab;
@@ -413,11 +429,12 @@ __global__ void __launch_bounds__(kThreads) row_reduce_kernel(RowParams p) {
           p.out_arg[row] = acc.i;
         }
       }
-      // one ticket for the whole grid: the last CTA finishes every row
-      __threadfence();
-      const unsigned t = atomicAdd(p.ticket, 1u);
+      // one ticket for the whole grid: the last CTA finishes every row. The
+      // add releases this CTA's partial and, for the last arrival, acquires
+      // every other CTA's (passed on to the CTA's threads by the barrier)
+      unsigned t;
+      asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(t) : "l"(p.ticket) : "memory");
       go = t == gridDim.x - 1u ? 1u : 0u;
-      if (go) __threadfence();  // acquire: every CTA's results, for all threads after the barrier
     }
   }
   __syncthreads();
@@ -444,6 +461,7 @@ __global__ void __launch_bounds__(kThreads) row_reduce_kernel(RowParams p) {
         const Stat m = merge(merge(a[0], a[1]), merge(a[2], a[3]));
         out_conf[r] = 1.f / m.s;
         out_arg[r] = m.i;
+        if (pre) pre_conf[r] = 1.f / m.s;
       }
     } else {
       // few rows, many slices: a warp takes 4 rows per round with all their
@@ -472,14 +490,23 @@ __global__ void __launch_bounds__(kThreads) row_reduce_kernel(RowParams p) {
           if (v[u] && lane == 0) {
             out_conf[r0 + u] = 1.f / a[u].s;
             out_arg[r0 + u] = a[u].i;
+            if (pre) pre_conf[r0 + u] = 1.f / a[u].s;
           }
         }
       }
     }
     __syncthreads();  // this CTA's confidences are written before the decisions read them
   }
-  if (p.phase == 0) decide_unmask(p);
-  else decide_verify(p);
+  if (p.phase == 0) {
+    if (pre && p.split == 1) {
+      // one slice per row: every CTA wrote its row's confidence to global memory
+      for (int r = threadIdx.x; r < n_rows_all; r += kThreads) pre_conf[r] = __ldcg(p.out_conf + r);
+    }
+    __syncthreads();
+    decide_unmask(p, pre ? pre_seq : nullptr, pre ? pre_pos : nullptr, pre ? pre_conf : nullptr);
+  } else {
+    decide_verify(p);
+  }
   if (threadIdx.x == 0) *p.ticket = 0u;  // ready for the next call
 }
 
