@@ -281,7 +281,7 @@ def run_gpu(args, world, rank, local):
     com = torch.empty(Rw, dtype=torch.uint8, device="cuda")
     srows = torch.empty((1, ms), dtype=torch.int32, device="cuda")
     nsr = torch.empty((1,), dtype=torch.int32, device="cuda")
-    launches_per_step = 5  # qkv, work-list build, attention, top-k, unmask (our kernels)
+    launches_per_step = 4  # qkv, attention (finds its own work items), top-k, unmask (our kernels)
 
     def qkv_part(c, X=None):
         X = Xs[c] if X is None else X

@@ -286,9 +286,11 @@ __global__ void __launch_bounds__(kWarps * 32) attn_simt_kernel(AttnParams p) {
 
 bool fdl_attn_tc_supported(const fdl_config& c);
 cudaError_t fdl_launch_attn_tc(fdl_ctx* ctx, const void* q, const void* k_cache, const void* v_cache,
-                               const int* block_table, int bt_stride, const int* kv_len, int B, int R,
-                               const int* row_kind, const int* search_pos, int search_ld, const int* n_search,
-                               void* o_out, float* lse_out, float* track, int track_ld, int cap);
+                               const int* block_table, int bt_stride, const int* cu_seqlens_q, const int* kv_len,
+                               int B, int R, const int* row_kind, const int* search_pos, int search_ld,
+                               const int* n_search, int max_search_tokens, void* o_out, float* lse_out, float* track,
+                               int track_ld, int cap, bool decode, int* worklist_out);
+int fdl_attn_tc_decode_max_batch();
 
 cudaError_t fdl_launch_attn(fdl_ctx* ctx, const void* q, const void* k_cache, const void* v_cache,
                             const int* block_table, int bt_stride, const int* cu_seqlens_q,
@@ -299,6 +301,12 @@ cudaError_t fdl_launch_attn(fdl_ctx* ctx, const void* q, const void* k_cache, co
   const int tile = ctx->attn_tile_m;
   const int cap = (R + tile - 1) / tile + B;
   const int max_search_tokens = min(c.max_views / 2, search_pos ? search_ld : 0);
+  // The tensor-core kernel finds its own work item from cu_seqlens_q (up to
+  // a batch it can stage in shared memory): no separate work-list launch.
+  if (tile == FDL_TILE_M_TC && B <= fdl_attn_tc_decode_max_batch())
+    return fdl_launch_attn_tc(ctx, q, k_cache, v_cache, block_table, bt_stride, cu_seqlens_q, kv_len, B, R, row_kind,
+                              search_pos, search_ld, n_search, max_search_tokens, o_out, lse_out, track, track_ld,
+                              cap, true, worklist_out);
   cudaError_t e = fdl_launch_pdl(build_worklist_kernel, dim3(1), dim3(kBuildThreads), (B + 1) * sizeof(int),
                                  ctx->stream, 1, cu_seqlens_q, kv_len, search_pos ? n_search : nullptr, B, R,
                                  tile, row_kind, c.max_seq, max_search_tokens, ctx->worklist,
@@ -310,8 +318,9 @@ cudaError_t fdl_launch_attn(fdl_ctx* ctx, const void* q, const void* k_cache, co
     if (e != cudaSuccess) return e;
   }
   if (ctx->attn_tile_m == FDL_TILE_M_TC)
-    return fdl_launch_attn_tc(ctx, q, k_cache, v_cache, block_table, bt_stride, kv_len, B, R, row_kind,
-                              search_pos, search_ld, n_search, o_out, lse_out, track, track_ld, cap);
+    return fdl_launch_attn_tc(ctx, q, k_cache, v_cache, block_table, bt_stride, cu_seqlens_q, kv_len, B, R, row_kind,
+                              search_pos, search_ld, n_search, max_search_tokens, o_out, lse_out, track, track_ld,
+                              cap, false, nullptr);
   AttnParams p;
   p.q = q;
   p.k_cache = k_cache;

@@ -83,7 +83,10 @@ constexpr int OFF_BITMAP = OFF_COLACC + 2 * 64 * 4;  // uint32 [768]
 constexpr int OFF_HALFML = OFF_BITMAP + 768 * 4;    // float [2][128][2]
 constexpr int OFF_FLAGS = OFF_HALFML + 2 * kBM * 2 * 4;
 constexpr int OFF_SLOTS = OFF_FLAGS + 256;          // int [kMaxTiles]
-constexpr int MISC_BYTES = OFF_SLOTS + 4 * kMaxTiles;
+constexpr int OFF_ITEM = OFF_SLOTS + 4 * kMaxTiles;  // int [8]: item count, b, q0, qlen, n_keys, WINDOW rows of b
+constexpr int kMaxDecodeB = 1024;                   // batch whose cu_seqlens_q the kernel stages
+constexpr int OFF_CU = OFF_ITEM + 32;               // int [kMaxDecodeB + 1]
+constexpr int MISC_BYTES = OFF_CU + 4 * (kMaxDecodeB + 1);
 static_assert(8 * (1 + 2 * kKS + 2 * kVS + 2 * kSB + 5) + 8 <= OFF_KINDS, "barriers fit");
 static_assert(256 + 64 * kSB <= kTmemCols, "TMEM columns");
 constexpr int SMEM_BYTES = 1024 + OFF_MISC + MISC_BYTES;
@@ -94,7 +97,11 @@ static_assert(kKS * KT_BYTES + kVS * VT_BYTES >= kBM * (kHD + 4) * 4,
 constexpr float kLn2 = 0.6931471805599453f;
 
 struct TcAttnParams {
-  const int* wl;            // count, then (b, q_start, q_len, n_keys)
+  const int* wl;            // count, then (b, q_start, q_len, n_keys); null: decode from cu
+  const int* cu;            // cu_seqlens_q [B + 1] (decode mode)
+  const int* n_search;      // [B] or null (decode mode)
+  int B, max_seq, max_search_tokens;
+  int* wl_out;              // decode mode: optional copy of the work list the kernel used
   const int* kv_len;
   const int* row_kind;
   const int* search_pos;
@@ -189,6 +196,15 @@ __device__ __forceinline__ bool visible(int kind, int c, int kvl, int m, bool is
   if (v < m) return mask_view ? (v < k) : (v <= k);
   const int j = v - m;
   return mask_view ? (j >= k) : (j > k);
+}
+
+__device__ __forceinline__ int warp_incl_scan(int v, int lane) {
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, v, off);
+    if (lane >= off) v += y;
+  }
+  return v;
 }
 
 // Hardware base-2 exponential (ex2.approx, relative error ~2^-22); ex2(-inf) = 0.
@@ -350,15 +366,92 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   fdl::grid_dep_wait();
   fdl::grid_dep_launch();
-  if (item >= p.wl[0]) {  // uniform over the cluster (a cluster spans x only)
+  int* s_item = reinterpret_cast<int*>(misc + OFF_ITEM);
+  if (!p.wl) {
+    // The work item from cu_seqlens_q: sequence b contributes ceil(rows_b /
+    // 128) items in order, item z of the grid is found by a prefix sum over
+    // the staged offsets. Inconsistent offsets (cu[0] != 0, cu[B] != R, a
+    // negative row count) leave no items and set the shape error.
+    int* s_cu = reinterpret_cast<int*>(misc + OFF_CU);
+    for (int i = threadIdx.x; i <= p.B; i += kThreads) s_cu[i] = p.cu[i];
+    if (threadIdx.x == 0) s_item[5] = 0;
+    __syncthreads();
+    if (warp == 0) {
+      bool bad = s_cu[0] != 0 || s_cu[p.B] != p.R;
+      int acc = 0, fb = -1, fbase = 0;
+      for (int base = 0; base < p.B; base += 32) {
+        const int bb = base + lane;
+        int rows = bb < p.B ? s_cu[bb + 1] - s_cu[bb] : 0;
+        if (rows < 0) {
+          bad = true;
+          rows = 0;
+        }
+        const int tiles = (rows + kBM - 1) / kBM;
+        const int incl = warp_incl_scan(tiles, lane);
+        const bool mine = item >= acc + incl - tiles && item < acc + incl;
+        const unsigned hit = __ballot_sync(0xffffffffu, mine);
+        if (hit) {
+          const int src = __ffs(hit) - 1;
+          fb = base + src;
+          fbase = acc + __shfl_sync(0xffffffffu, incl - tiles, src);
+        }
+        acc += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      bad = __any_sync(0xffffffffu, bad);
+      const int count = bad ? 0 : acc;
+      if (lane == 0) {
+        s_item[0] = count;
+        if (bad && item == 0 && h == 0 && rank == 0) fdl::raise_error(p.err, FDL_DEVERR_SHAPE);
+        if (item < count) {
+          const int bq0 = s_cu[fb] + (item - fbase) * kBM;
+          int kv = p.kv_len[fb];
+          if (kv < 0 || kv > p.max_seq) {
+            if (h == 0 && rank == 0) fdl::raise_error(p.err, FDL_DEVERR_INDEX);
+            kv = max(0, min(kv, p.max_seq));
+          }
+          int m = 0;
+          if (p.n_search) {
+            m = p.n_search[fb];
+            if (m < 0 || m > p.max_search_tokens) {
+              if (h == 0 && rank == 0) fdl::raise_error(p.err, FDL_DEVERR_INDEX);
+              m = max(0, min(m, p.max_search_tokens));
+            }
+          }
+          s_item[1] = fb;
+          s_item[2] = bq0;
+          s_item[3] = min(kBM, s_cu[fb + 1] - bq0);
+          s_item[4] = kv + 2 * m;
+          if (p.wl_out && h == 0 && rank == 0) {
+            int* w = p.wl_out + 1 + 4 * item;
+            w[0] = fb;
+            w[1] = bq0;
+            w[2] = s_item[3];
+            w[3] = s_item[4];
+          }
+        }
+        if (p.wl_out && item == 0 && h == 0 && rank == 0) p.wl_out[0] = count;
+      }
+    }
+    __syncthreads();
+  } else if (threadIdx.x == 0) {
+    s_item[0] = p.wl[0];
+    if (item < s_item[0]) {
+      const int* it = p.wl + 1 + 4 * item;
+      s_item[1] = it[0];
+      s_item[2] = it[1];
+      s_item[3] = it[2];
+      s_item[4] = it[3];
+    }
+  }
+  if (p.wl) __syncthreads();
+  if (item >= s_item[0]) {  // uniform over the cluster (a cluster spans x only)
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     if (warp == 1) tc::tmem_dealloc(*tmem_slot, kTmemCols);
     return;
   }
-  const int* it = p.wl + 1 + 4 * item;
-  const int b = it[0], q0 = it[1], qlen = it[2], nkeys = it[3];
+  const int b = s_item[1], q0 = s_item[2], qlen = s_item[3], nkeys = s_item[4];
   const int kvl = min(p.kv_len[b], nkeys);
   const int m_search = p.search_pos ? (nkeys - kvl) / 2 : 0;
   int n_tiles = (nkeys + kBN - 1) / kBN;
@@ -417,6 +510,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int w = t_local; w < p.bitmap_words; w += 256) bitmap[w] = 0u;
     if (t_local < 128) colacc[t_local] = 0.f;
+    if (!p.wl && p.track) {
+      // WINDOW rows of the whole sequence (the tracker's |M_b|)
+      const int* s_cu = reinterpret_cast<const int*>(misc + OFF_CU);
+      int cnt = 0;
+      for (int r = s_cu[b] + t_local; r < s_cu[b + 1]; r += 256) cnt += p.row_kind[r] == FDL_KIND_WINDOW ? 1 : 0;
+      for (int off = 16; off; off >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
+      if (lane == 0 && cnt) atomicAdd(&s_item[5], cnt);
+    }
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -426,7 +527,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (C > 1) tc::cluster_arrive();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tm_s = tmem + 256;  // kSB 64-column S buffers; O accumulators at 0 and 128
-  const bool do_track = p.track != nullptr && p.n_masked[b] > 0;
+  const int n_masked_b = p.wl ? p.n_masked[b] : s_item[5];
+  const bool do_track = p.track != nullptr && n_masked_b > 0;
   const bool any_window = (win_flags[0] | win_flags[1] | win_flags[2] | win_flags[3]) != 0;
   const bool track_item = do_track && any_window;
   // Split items and items that feed the tracker take two exact passes; the
@@ -664,7 +766,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // when a tile's max exceeds it by more than kRescale; O_g and the row sum
     // are then scaled down to the new m)
     const int sc0 = two_pass && !keep_s ? n_my : 0;
-    const float wscale = do_track ? 1.f / ((float)p.H * (float)p.n_masked[b]) : 0.f;
+    const float wscale = do_track ? 1.f / ((float)p.H * (float)n_masked_b) : 0.f;
     const bool track_row = do_track && kind == FDL_KIND_WINDOW;
     const bool track_warp = __any_sync(0xffffffffu, track_row);
     const int t_g = t_local - 128 * g;  // 0..127 within the group
@@ -931,12 +1033,18 @@ bool fdl_attn_tc_supported(const fdl_config& c) {
          (c.max_seq + c.max_views + 31) / 32 <= 768;
 }
 
+int fdl_attn_tc_decode_max_batch() { return kMaxDecodeB; }
+
+// decode: the kernel finds its work items from cu_seqlens_q itself (and
+// writes them to worklist_out when given); otherwise it reads the work list
+// built into the context's workspace.
 cudaError_t fdl_launch_attn_tc(fdl_ctx* ctx, const void* q, const void* k_cache, const void* v_cache,
-                               const int* block_table, int bt_stride, const int* kv_len, int B, int R,
-                               const int* row_kind, const int* search_pos, int search_ld, const int* n_search,
-                               void* o_out, float* lse_out, float* track, int track_ld, int cap) {
-  (void)n_search;  // the work list already carries kv_len + 2 * n_search per item
+                               const int* block_table, int bt_stride, const int* cu_seqlens_q, const int* kv_len,
+                               int B, int R, const int* row_kind, const int* search_pos, int search_ld,
+                               const int* n_search, int max_search_tokens, void* o_out, float* lse_out, float* track,
+                               int track_ld, int cap, bool decode, int* worklist_out) {
   const fdl_config& c = ctx->cfg;
+  if (decode && B > kMaxDecodeB) return cudaErrorInvalidValue;
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) |
        reinterpret_cast<uintptr_t>(v_cache) | reinterpret_cast<uintptr_t>(o_out)) & 15)
     return cudaErrorMisalignedAddress;
@@ -952,7 +1060,13 @@ cudaError_t fdl_launch_attn_tc(fdl_ctx* ctx, const void* q, const void* k_cache,
       !map2d(&mv, v_cache, n_slots, c.d_model, kBN))
     return cudaErrorInvalidValue;
   TcAttnParams p;
-  p.wl = ctx->worklist;
+  p.wl = decode ? nullptr : ctx->worklist;
+  p.cu = cu_seqlens_q;
+  p.n_search = search_pos ? n_search : nullptr;
+  p.B = B;
+  p.max_seq = c.max_seq;
+  p.max_search_tokens = max_search_tokens;
+  p.wl_out = worklist_out;
   p.kv_len = kv_len;
   p.row_kind = row_kind;
   p.search_pos = search_pos;
