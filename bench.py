@@ -46,11 +46,11 @@ WORKLOAD = "llada8b_layer_bf16_b1_p512_g256_w32_t32"
 
 # DRAM traffic of one launch of the projection kernel on this workload
 # (dram__bytes_read.sum + dram__bytes_write.sum), from the ncu capture
-# summarised in profiles/qkv_tc_kernel_llada8b_layer.txt. It is reported only
+# summarised in profiles/hot_kernels_llada8b_layer.txt. It is reported only
 # while the sources it was taken from hash to the recorded value; after any
 # change to them the figure is stale and the line carries null.
-QKV_TRAFFIC = {"sources_sha256": "8cde7a8b83d38140f6768fb28c7f8d5a60665df2ef72dc38a55e328212816f52",
-               "bytes": 102134528 + 3614208}
+QKV_TRAFFIC = {"sources_sha256": "31bd0ac2c7ca4cb008037285501557a977d1aba319f7d87930b6a74f733af308",
+               "bytes": 102125824 + 3212800}
 QKV_SOURCES = ("kv_cache_attention_gb300/csrc/fdl_qkv_tc.cu", "kv_cache_attention_gb300/csrc/fdl_qkv.cu",
                "kv_cache_attention_gb300/csrc/tc_ptx.cuh", "kv_cache_attention_gb300/csrc/fdl_internal.cuh")
 
