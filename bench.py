@@ -274,13 +274,19 @@ def run_gpu(args, world, rank, local):
     o = torch.empty_like(q)
     lse = torch.empty((R, Hh), dtype=torch.float32, device="cuda")
     track = torch.zeros((1, N), dtype=torch.float32, device="cuda")
-    idx = torch.empty((1, k), dtype=torch.int32, device="cuda")
-    cnt = torch.empty((1,), dtype=torch.int32, device="cuda")
-    conf = torch.empty(Rw, dtype=torch.float32, device="cuda")
-    arg = torch.empty(Rw, dtype=torch.int32, device="cuda")
-    com = torch.empty(Rw, dtype=torch.uint8, device="cuda")
-    srows = torch.empty((1, ms), dtype=torch.int32, device="cuda")
-    nsr = torch.empty((1,), dtype=torch.int32, device="cuda")
+    # The step's results (decisions and tracked set) are views of one device
+    # buffer, so the end-to-end loop reads them back with one copy.
+    res_layout = [("conf", torch.float32, (Rw,)), ("arg", torch.int32, (Rw,)), ("com", torch.uint8, (Rw,)),
+                  ("srows", torch.int32, (1, ms)), ("nsr", torch.int32, (1,)), ("idx", torch.int32, (1, k)),
+                  ("cnt", torch.int32, (1,))]
+    res_off, off = {}, 0
+    for name, dt, shp in res_layout:
+        res_off[name] = off
+        off += (int(np.prod(shp)) * torch.empty((), dtype=dt).element_size() + 15) // 16 * 16
+    res_buf = torch.zeros(off, dtype=torch.uint8, device="cuda")
+    res = {name: res_buf[res_off[name]:res_off[name] + int(np.prod(shp)) * torch.empty((), dtype=dt).element_size()]
+           .view(dt).view(shp) for name, dt, shp in res_layout}
+    conf, arg, com, srows, nsr, idx, cnt = (res[n] for n in ("conf", "arg", "com", "srows", "nsr", "idx", "cnt"))
     launches_per_step = 4  # qkv, attention (finds its own work items), top-k, unmask (our kernels)
 
     def qkv_part(c, X=None):
@@ -353,21 +359,25 @@ def run_gpu(args, world, rank, local):
     qkv_timing = (f"CUDA events over {n_qkv * n_copies} back-to-back graph launches of the projection "
                   f"(rotating copies), right after the timed steps")
 
-    # end to end: pinned host inputs in, step results out, every step
-    x_pin = x_host.pin_memory()
-    l_pin = l_host.pin_memory()
-    out_pin = [t.new_empty(t.shape, device="cpu").pin_memory() for t in (conf, arg, com, srows, nsr, idx, cnt)]
-    xd, ld_ = torch.empty_like(Xs[0]), torch.empty_like(Ls[0])
+    # end to end: pinned host inputs in, step results out, every step. The
+    # step's inputs (hidden rows and logits) sit in one pinned host buffer and
+    # one device buffer, and its results in one device buffer, so each
+    # direction is one copy.
+    nx, nl = x_host.numel(), l_host.numel()
+    in_pin = torch.empty(nx + nl, dtype=torch.bfloat16).pin_memory()
+    in_pin[:nx].copy_(x_host.reshape(-1))
+    in_pin[nx:].copy_(l_host.reshape(-1))
+    in_dev = torch.empty_like(in_pin, device="cuda")
+    xd, ld_ = in_dev[:nx].view(x_host.shape), in_dev[nx:].view(l_host.shape)
+    out_pin = torch.empty_like(res_buf, device="cpu").pin_memory()
     K_e2e = min(K, 1000)
-    h2d = x_pin.numel() * 2 + l_pin.numel() * 2
-    d2h = sum(t.numel() * t.element_size() for t in out_pin)
+    h2d = in_pin.numel() * 2
+    d2h = out_pin.numel()
 
     def e2e_step(c):
-        xd.copy_(x_pin, non_blocking=True)
-        ld_.copy_(l_pin, non_blocking=True)
+        in_dev.copy_(in_pin, non_blocking=True)
         step(c, X=xd, L=ld_)
-        for src, dst in zip((conf, arg, com, srows, nsr, idx, cnt), out_pin):
-            dst.copy_(src, non_blocking=True)
+        out_pin.copy_(res_buf, non_blocking=True)
 
     for i in range(args.warmup):
         e2e_step(i % n_copies)

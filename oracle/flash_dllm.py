@@ -333,6 +333,33 @@ def unmask(logits, row_seq, row_pos, B: int, eps: float, force_progress: bool,
     return dict(conf=conf, argmax=arg, commit=commit, search_rows=search, n_search=n_search)
 
 
+def lm_head_logits(hidden, w_lm, chunk: int = 4096) -> np.ndarray:
+    """Window rows' logits over the vocabulary: l = h W_lm^T.
+
+    [FD "Method steps", step 2] takes c_i = max_x p(x_i | x^t) from the
+    model's output distribution over the vocabulary; p is the softmax of the
+    language-model head applied to the final hidden state of each masked
+    position. Reading: the head is a plain linear map [vocab, d_model] with
+    no bias (the LLaMA-style output layer of LLaDA), applied to the
+    already-normalised hidden state. float64 from the exactly widened
+    inputs, computed in vocabulary chunks only to bound memory.
+    """
+    h = np.asarray(hidden, np.float64)
+    V = w_lm.shape[0]
+    out = np.empty((h.shape[0], V))
+    for v0 in range(0, V, chunk):
+        out[:, v0:v0 + chunk] = h @ np.asarray(w_lm[v0:v0 + chunk], np.float64).T
+    return out
+
+
+def lm_head_unmask(hidden, w_lm, row_seq, row_pos, B: int, eps: float, force_progress: bool,
+                   max_search: int):
+    """Draft-step decisions straight from the hidden states: ``unmask`` of
+    ``lm_head_logits``, the composition the fused kernel computes without
+    storing the logits ([FD "Method steps", step 2])."""
+    return unmask(lm_head_logits(hidden, w_lm), row_seq, row_pos, B, eps, force_progress, max_search)
+
+
 def verify(mask_logits, draft_tok, n_search, gamma: float, B: int, max_search: int):
     """Flash-Verify prefix acceptance.
 

@@ -467,3 +467,37 @@ def projection_case(seed: int, d_model: int, n_heads: int, n_rows: int, batch: i
     kc, vc = _cache_fill(rng, geom.n_pages * geom.page_size, d_model, dtype)
     return Workload("projection_case", shape, batch, np.full(batch, seq_len, np.int32), seq_len, 0, geom,
                     dict(w=w, x=x, rows=rows, k_cache=kc, v_cache=vc))
+
+
+# --------------------------------------------------------------------------
+# Language-model head (the step after the path: hidden states -> decisions)
+# --------------------------------------------------------------------------
+def lm_head_case(seed: int = 1006, vocab: int = 126464, d: int = 4096, rows: int = 32,
+                 planted: float = 0.3, w_std: float = 0.02):
+    """Window rows' hidden states and an LM-head weight, bf16.
+
+    Hidden ~ N(0, 1), W_lm ~ N(0, w_std^2). For a seeded fraction ``planted``
+    of the rows, one vocabulary row of W_lm is replaced by a multiple of that
+    hidden row, so its logit stands far above the others and the row's
+    confidence lands between 0.5 and 0.999 (the multiple is solved from the
+    expected partition sum of the N(0, (w_std |h|)^2) logits, as in
+    ``targeted_logits``); the other rows keep confidences near 1 / vocab.
+    Returns (hidden Tensor [rows, d], W_lm Tensor [vocab, d], planted ids).
+    """
+    rng = np.random.default_rng(seed)
+    h = normal(rng, (rows, d))
+    w = normal(rng, (vocab, d), w_std)
+    n_plant = int(round(planted * rows))
+    plant_rows = np.sort(rng.choice(rows, size=n_plant, replace=False)) if n_plant else np.zeros(0, np.int64)
+    ids = np.full(rows, -1, dtype=np.int64)
+    free = rng.permutation(vocab)
+    for j, r in enumerate(plant_rows):
+        v = int(free[j])
+        hn = float(np.linalg.norm(h[r]))
+        sigma = w_std * hn
+        z_rest = (vocab - 1) * math.exp(sigma * sigma / 2)
+        target = float(rng.uniform(0.5, 0.999))
+        logit = math.log(target / (1 - target) * z_rest)
+        w[v] = (h[r] * (logit / (hn * hn))).astype(np.float32)
+        ids[r] = v
+    return make_tensor(h, "bf16"), make_tensor(w, "bf16"), ids

@@ -448,3 +448,57 @@ def test_flash_verify_recipe_rates():
     agree = float(np.mean(am == a))
     assert 0.55 <= agree <= 0.85
     assert 0.35 <= float(np.mean(cm >= e["gamma"])) <= 0.65
+
+
+# --------------------------------------------------------------------------- LM head (next-row f1)
+def test_lm_head_logits_brute_force_and_unit_rows():
+    # brute force: every logit as an explicit sum over the hidden dimension
+    rng = np.random.default_rng(21)
+    h = rng.standard_normal((3, 5))
+    w = rng.standard_normal((7, 5))
+    L = oracle.lm_head_logits(h, w, chunk=3)
+    for r in range(3):
+        for v in range(7):
+            assert abs(L[r, v] - sum(h[r, k] * w[v, k] for k in range(5))) < 1e-12
+    # unit vocabulary rows pick hidden components: W = I gives l = h exactly,
+    # a permutation of I permutes them (a transposed operand fails this)
+    assert np.array_equal(oracle.lm_head_logits(h, np.eye(5)), h)
+    perm = np.array([3, 0, 4, 1, 2])
+    assert np.array_equal(oracle.lm_head_logits(h, np.eye(5)[perm]), h[:, perm])
+    # chunking only bounds memory (the library product may reassociate)
+    np.testing.assert_allclose(oracle.lm_head_logits(h, w, chunk=1), oracle.lm_head_logits(h, w, chunk=100),
+                               rtol=1e-14, atol=1e-14)
+
+
+def test_lm_head_unmask_closed_form_and_composition():
+    # one vocabulary row aligned with the hidden state, all others zero: the
+    # logits are (a, 0, ..., 0) with a = 6 |h|^2, so c = e^a / (e^a + V - 1)
+    V, d = 50, 8
+    h = np.zeros((2, d))
+    h[0, :4] = 0.5
+    h[1, 6] = 1.0  # orthogonal to h[0]: all of row 1's logits are 0
+    w = np.zeros((V, d))
+    w[17] = 6.0 * h[0]
+    out = oracle.lm_head_unmask(h, w, np.array([0, 0]), np.array([10, 11]), 1, 0.5, False, 4)
+    a = 6.0 * float(h[0] @ h[0])
+    assert abs(out["conf"][0] - math.exp(a) / (math.exp(a) + V - 1)) < 1e-12
+    assert out["argmax"][0] == 17
+    assert abs(out["conf"][1] - 1.0 / V) < 1e-12 and out["argmax"][1] == 0  # all-zero row: lowest id
+    assert out["commit"].tolist() == [1, 0] and out["n_search"].tolist() == [1]
+    # the composition with explicit logits
+    hidden, wl, _ = synth.lm_head_case(seed=5, vocab=300, d=32, rows=6)
+    want = oracle.unmask(hidden.values() @ wl.values().T, np.zeros(6, np.int32), np.arange(6), 1, 0.9, True, 4)
+    got = oracle.lm_head_unmask(hidden.values(), wl.values(), np.zeros(6, np.int32), np.arange(6), 1, 0.9, True, 4)
+    for key in ("commit", "search_rows", "n_search", "argmax"):
+        assert np.array_equal(got[key], want[key])
+    np.testing.assert_allclose(got["conf"], want["conf"], rtol=1e-12)
+
+
+def test_lm_head_case_plants_confident_rows():
+    # the generator's recipe: planted rows are confident in their planted id
+    hidden, w, ids = synth.lm_head_case(seed=3, vocab=2048, d=128, rows=20)
+    c, a = oracle.row_confidence(oracle.lm_head_logits(hidden.values(), w.values()))
+    planted = ids >= 0
+    assert planted.sum() == 6
+    assert np.array_equal(a[planted], ids[planted])
+    assert (c[planted] > 0.3).all() and (c[~planted] < 0.05).all()
