@@ -14,6 +14,9 @@
  *   fdl_track_topk            top-k of the tracker scores (next tracked set)
  *   fdl_unmask_verify         confidence-threshold unmasking (search list) and
  *                             Flash-Verify prefix acceptance
+ *   fdl_lm_head_unmask        the unmasking decisions straight from the window
+ *                             rows' hidden states (LM head fused, logits never
+ *                             stored)
  *
  * Conventions shared by every entry point
  *   - All tensor arguments are DEVICE pointers owned by the caller (for
@@ -223,6 +226,26 @@ typedef struct {
 } fdl_unmask_args;
 
 fdl_status fdl_unmask_verify(fdl_ctx* ctx, const fdl_unmask_args* args);
+
+/* ------------------------------------------------------------------------
+ * Fused LM head + unmasking (paper digest, "Method steps in detail", step 2:
+ * c_i = max_x p(x_i | x^t) is taken over the model's output distribution,
+ * the softmax of the language-model head on each masked position's final
+ * hidden state). The logits are never stored:
+ *   logits[r] = hidden[r] . w_lm^T     (config.vocab entries, fp32 accumulation)
+ * and the unmask phase of fdl_unmask_verify is applied to them: conf,
+ * argmax, commit, search_rows and n_search exactly as documented above,
+ * from args' R_w, row_seq, row_pos, eps, force_progress, max_search and B.
+ * args->logits and args->mask_logits must be NULL (the verify phase runs
+ * through fdl_unmask_verify on explicit mask-view logits).
+ *
+ * hidden: [R_w, d_model] bf16, the window rows' final hidden states (16-byte
+ * aligned); w_lm: [vocab, d_model] bf16 row-major (16-byte aligned). bf16
+ * contexts only, 1 <= R_w <= 64 (one tile of window rows): otherwise
+ * FDL_ERR_UNSUPPORTED / FDL_ERR_INVALID_ARG. The reductions over the
+ * vocabulary run in a fixed order, so results do not depend on timing.
+ * ---------------------------------------------------------------------- */
+fdl_status fdl_lm_head_unmask(fdl_ctx* ctx, const void* hidden, const void* w_lm, const fdl_unmask_args* args);
 
 /* ------------------------------------------------------------------------
  * Scheduled attention without any device allocation. The paper has no

@@ -42,7 +42,7 @@ def FDL_KIND_MASK_VIEW(j: int) -> int:
 EXPORTS = (
     "fdl_create", "fdl_destroy", "fdl_set_stream", "fdl_last_error", "fdl_sync_status",
     "fdl_tile_m", "fdl_worklist_capacity", "fdl_qkv_rope_cache_write", "fdl_sched_attn",
-    "fdl_track_topk", "fdl_unmask_verify", "fdl_sched_attn_noalloc",
+    "fdl_track_topk", "fdl_unmask_verify", "fdl_sched_attn_noalloc", "fdl_lm_head_unmask",
 )
 
 
@@ -109,6 +109,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.fdl_track_topk.restype = i
     L.fdl_unmask_verify.argtypes = [p, ctypes.POINTER(fdl_unmask_args)]
     L.fdl_unmask_verify.restype = i
+    L.fdl_lm_head_unmask.argtypes = [p, p, p, ctypes.POINTER(fdl_unmask_args)]
+    L.fdl_lm_head_unmask.restype = i
     L.fdl_sched_attn_noalloc.argtypes = [ctypes.POINTER(fdl_config), p, p, p, p, p, i, p, p, i, i, p, p, i, p, p,
                                          p, p, i, p]
     L.fdl_sched_attn_noalloc.restype = i
@@ -207,6 +209,20 @@ class Context:
         a.mask_conf, a.mask_argmax = _ptr(mask_conf), _ptr(mask_argmax)
         self._check(load_library().fdl_unmask_verify(self.handle, ctypes.byref(a)), "fdl_unmask_verify")
 
+    def lm_head_unmask(self, hidden, w_lm, B: int, max_search: int, *, row_seq, row_pos, eps: float = 0.9,
+                       force_progress: bool = False, conf, argmax, commit, search_rows, n_search) -> None:
+        """Unmask-phase decisions straight from the window rows' hidden states
+        (hidden [R_w, d_model], w_lm [vocab, d_model], both bf16)."""
+        a = fdl_unmask_args()
+        a.B, a.max_search = int(B), int(max_search)
+        a.R_w = int(hidden.shape[0])
+        a.row_seq, a.row_pos = _ptr(row_seq), _ptr(row_pos)
+        a.eps, a.force_progress = float(eps), int(bool(force_progress))
+        a.conf, a.argmax, a.commit = _ptr(conf), _ptr(argmax), _ptr(commit)
+        a.search_rows, a.n_search = _ptr(search_rows), _ptr(n_search)
+        self._check(load_library().fdl_lm_head_unmask(self.handle, _ptr(hidden), _ptr(w_lm), ctypes.byref(a)),
+                    "fdl_lm_head_unmask")
+
 
 def _stream_handle(stream) -> int | None:
     if stream is None:
@@ -252,6 +268,10 @@ def fdl_track_topk(ctx: Context, *a, **k) -> None:
 
 def fdl_unmask_verify(ctx: Context, *a, **k) -> None:
     ctx.unmask_verify(*a, **k)
+
+
+def fdl_lm_head_unmask(ctx: Context, *a, **k) -> None:
+    ctx.lm_head_unmask(*a, **k)
 
 
 def fdl_sched_attn_noalloc(cfg: fdl_config, q, k_cache, v_cache, block_table, cu_seqlens_q, kv_len, row_kind,

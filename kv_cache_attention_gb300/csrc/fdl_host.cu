@@ -114,6 +114,7 @@ fdl_status fdl_create(const fdl_config* cfg, void* cuda_stream, fdl_ctx** out) {
     e = e ? e : cudaMalloc(&ctx->qkv_partials, ctx->qkv_partial_floats * sizeof(float));
     e = e ? e : cudaMalloc(&ctx->qkv_ticket_buf, ctx->qkv_tickets * sizeof(unsigned));
     e = e ? e : cudaMemset(ctx->qkv_ticket_buf, 0, ctx->qkv_tickets * sizeof(unsigned));
+    e = e ? e : cudaMalloc(&ctx->lm_part, fdl_lm_partial_floats(cfg->vocab) * sizeof(float));
   }
   e = e ? e : cudaMemcpy(ctx->rope_cos, hc.data(), n_tab * sizeof(float), cudaMemcpyHostToDevice);
   e = e ? e : cudaMemcpy(ctx->rope_sin, hs.data(), n_tab * sizeof(float), cudaMemcpyHostToDevice);
@@ -138,6 +139,7 @@ void fdl_destroy(fdl_ctx* ctx) {
   cudaFree(ctx->row_part);
   cudaFree(ctx->qkv_partials);
   cudaFree(ctx->qkv_ticket_buf);
+  cudaFree(ctx->lm_part);
   free(ctx);
 }
 
@@ -256,6 +258,28 @@ fdl_status fdl_unmask_verify(fdl_ctx* ctx, const fdl_unmask_args* a) {
   }
   if (!a->logits && !a->mask_logits) return FDL_OK;
   return launched(ctx, fdl_launch_unmask_verify(ctx, a), "unmask/verify launch");
+}
+
+fdl_status fdl_lm_head_unmask(fdl_ctx* ctx, const void* hidden, const void* w_lm, const fdl_unmask_args* a) {
+  if (!ctx) return FDL_ERR_INVALID_ARG;
+  if (!a || !hidden || !w_lm) return fail(ctx, FDL_ERR_INVALID_ARG, "fdl_lm_head_unmask: NULL argument");
+  if (a->logits || a->mask_logits)
+    return fail(ctx, FDL_ERR_INVALID_ARG, "fdl_lm_head_unmask: logits and mask_logits must be NULL");
+  if (ctx->cfg.dtype != FDL_BF16)
+    return fail(ctx, FDL_ERR_UNSUPPORTED, "fdl_lm_head_unmask: bf16 contexts only");
+  if (a->B < 1 || a->B > ctx->cfg.max_batch)
+    return fail(ctx, FDL_ERR_INVALID_ARG, "B=%d outside [1, max_batch=%d]", a->B, ctx->cfg.max_batch);
+  if (a->R_w < 1 || a->R_w > fdl_lm_head_max_rows())
+    return fail(ctx, FDL_ERR_UNSUPPORTED, "R_w=%d outside [1, %d]", a->R_w, fdl_lm_head_max_rows());
+  if (a->max_search < 0 || a->max_search > 1024)
+    return fail(ctx, FDL_ERR_INVALID_ARG, "max_search=%d outside [0, 1024]", a->max_search);
+  if (!a->row_seq || !a->row_pos || !a->conf || !a->argmax || !a->commit || !a->n_search ||
+      (a->max_search > 0 && !a->search_rows))
+    return fail(ctx, FDL_ERR_INVALID_ARG, "fdl_lm_head_unmask: NULL output or row argument");
+  if (!(a->eps >= 0.f && a->eps <= 1.f)) return fail(ctx, FDL_ERR_INVALID_ARG, "eps outside [0,1]");
+  if (ctx->cfg.d_model % 64 != 0)
+    return fail(ctx, FDL_ERR_UNSUPPORTED, "fdl_lm_head_unmask: d_model must be a multiple of 64");
+  return launched(ctx, fdl_launch_lm_head_unmask(ctx, hidden, w_lm, a), "LM-head unmask launch");
 }
 
 }  // extern "C"

@@ -36,6 +36,7 @@ struct fdl_ctx {
   size_t qkv_partial_floats;
   unsigned* qkv_ticket_buf;  // per-tile arrival counters (zero between calls)
   int qkv_tickets;
+  float* lm_part;       // per-vocabulary-tile statistics of the fused LM head (bf16 contexts)
   char last_error[512];
 };
 
@@ -152,6 +153,11 @@ cudaError_t fdl_launch_topk(fdl_ctx* ctx, const float* scores, const unsigned ch
                             const int* seq_len, int B, int k, int* idx_out, int* cnt_out);
 
 cudaError_t fdl_launch_unmask_verify(fdl_ctx* ctx, const fdl_unmask_args* a);
+
+cudaError_t fdl_launch_lm_head_unmask(fdl_ctx* ctx, const void* hidden, const void* w_lm, const fdl_unmask_args* a);
+// Window rows the fused LM head takes in one call, and its workspace floats.
+int fdl_lm_head_max_rows();
+size_t fdl_lm_partial_floats(int vocab);
 
 // Workspace floats the tensor-core projection needs for split-K partials.
 size_t fdl_qkv_partial_floats(int num_sms);

@@ -18,7 +18,10 @@
 // fixed xor tree, so the result does not depend on timing, and takes the
 // per-sequence decisions: one launch per phase, and nothing ever waits on
 // another CTA.
+#include <cudaTypedefs.h>
+
 #include "fdl_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace {
 
@@ -208,9 +211,9 @@ struct RowParams {
 // kStageRows rows), together with each sequence's row range (up to
 // kStageSeqs sequences), so no step waits on a chain of memory loads: the
 // ranking compares a sequence's rows in registers through warp shuffles.
-constexpr int kStageRows = 2048;
-constexpr int kStageSeqs = 1024;
-
+// (kStageRows and kStageSeqs are template arguments: the vocab reduction
+// stages up to 2048 rows of up to 1024 sequences, the fused LM head up to 64.)
+template <int kStageRows, int kStageSeqs>
 __device__ void decide_unmask(const RowParams& p, const int* st_seq, const int* st_pos, const float* st_conf) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   // parameters used inside loops, read once into registers
@@ -503,7 +506,7 @@ __global__ void __launch_bounds__(kThreads) row_reduce_kernel(RowParams p) {
       for (int r = threadIdx.x; r < n_rows_all; r += kThreads) pre_conf[r] = __ldcg(p.out_conf + r);
     }
     __syncthreads();
-    decide_unmask(p, pre ? pre_seq : nullptr, pre ? pre_pos : nullptr, pre ? pre_conf : nullptr);
+    decide_unmask<2048, 1024>(p, pre ? pre_seq : nullptr, pre ? pre_pos : nullptr, pre ? pre_conf : nullptr);
   } else {
     decide_verify(p);
   }
@@ -528,6 +531,241 @@ cudaError_t launch_phase(fdl_ctx* ctx, RowParams p) {
   p.vec_ok = ((reinterpret_cast<uintptr_t>(p.logits) & 15) == 0) && ((size_t)V * sizeof(T)) % 16 == 0;
   return fdl_launch_pdl(row_reduce_kernel<T>, dim3((unsigned)(p.n_rows * split)), dim3(kThreads), 0, ctx->stream, 1,
                         p);
+}
+
+
+// ---------------------------------------------------------------------------
+// Fused LM head + unmasking: logits = hidden . W_lm^T are reduced to each
+// window row's (max, argmax, sum of exponentials) tile by tile and never
+// stored. Same orientation as the projection ("swap AB"): one CTA takes 128
+// vocabulary rows (TMEM lanes) against all window rows (<= 64, TMEM
+// columns), with the weight streamed by TMA through a 4-stage ring into
+// tcgen05.mma (bf16 in, fp32 accumulate). The epilogue stages the fp32 tile
+// in shared memory and reduces every column (window row) over the tile's
+// vocabulary rows; the per-tile statistics go to the workspace, and the last
+// CTA to take the grid ticket merges them in tile order and takes the
+// decisions of the unmask phase (decide_unmask above).
+// ---------------------------------------------------------------------------
+constexpr int kLmBM = 128;  // vocabulary rows per tile
+constexpr int kLmBN = 64;   // window rows per tile (the whole call)
+constexpr int kLmBK = 64;
+constexpr int kLmStages = 4;
+constexpr int kLmThreads = 192;
+constexpr int kLmA = kLmBM * kLmBK * 2;
+constexpr int kLmB = kLmBN * kLmBK * 2;
+constexpr int kLmStage = kLmA + kLmB;
+constexpr int kLmPipe = kLmStages * kLmStage;
+constexpr int kLmSmem = 1024 + kLmPipe + 256;
+constexpr int kLmXs = kLmBM + 1;  // padded row of the fp32 tile: column-wise reads are conflict-free
+static_assert(kLmBN * kLmXs * 4 <= kLmPipe, "the fp32 tile fits in the drained ring");
+
+struct LmParams {
+  RowParams rp;  // decisions of the unmask phase; rp.part is the per-tile workspace
+  int vocab, nkb, n_tiles;
+};
+
+__global__ void __launch_bounds__(kLmThreads, 2)
+    lm_head_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_h,
+                   const LmParams p) {
+  extern __shared__ uint8_t lm_smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(lm_smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* pipe = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kLmPipe);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kLmStages;
+  uint64_t* tmem_full = bars + 2 * kLmStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tmem_full + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  __shared__ Stat half_stat[kLmBN];
+  __shared__ unsigned go;
+  __shared__ int pre_seq[kLmBN], pre_pos[kLmBN];
+  __shared__ float pre_conf[kLmBN];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile = blockIdx.x;
+  const int f0 = tile * kLmBM;
+  const int R = p.rp.n_rows;
+  const int pre = min(p.nkb, kLmStages);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kLmStages; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    tc::mbar_init(tmem_full, 1);
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+    tc::prefetch_tensormap(&tm_w);
+    tc::prefetch_tensormap(&tm_h);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_slot, kLmBN);
+    tc::tmem_relinquish();
+  }
+  fdl::grid_dep_wait();
+  fdl::grid_dep_launch();
+  if (threadIdx.x == 0) {
+    for (int it = 0; it < pre; ++it) {
+      uint8_t* a = pipe + it * kLmStage;
+      tc::mbar_arrive_expect_tx(&full[it], kLmStage);
+      tc::tma_load_2d(a, &tm_w, it * kLmBK, f0, &full[it]);
+      tc::tma_load_2d(a + kLmA, &tm_h, it * kLmBK, 0, &full[it]);
+    }
+  }
+  // every CTA may be the last: it stages the decision inputs at its start
+  if ((int)threadIdx.x < R) {
+    pre_seq[threadIdx.x] = p.rp.row_seq[threadIdx.x];
+    pre_pos[threadIdx.x] = p.rp.row_pos[threadIdx.x];
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int kb = pre; kb < p.nkb; ++kb) {
+        const int s = kb % kLmStages;
+        if (!tc::mbar_wait(&empty[s], ((uint32_t)(kb / kLmStages) & 1u) ^ 1u, abort_flag)) break;
+        uint8_t* a = pipe + s * kLmStage;
+        tc::mbar_arrive_expect_tx(&full[s], kLmStage);
+        tc::tma_load_2d(a, &tm_w, kb * kLmBK, f0, &full[s]);
+        tc::tma_load_2d(a + kLmA, &tm_h, kb * kLmBK, 0, &full[s]);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(kLmBM, kLmBN);
+      for (int kb = 0; kb < p.nkb; ++kb) {
+        const int s = kb % kLmStages;
+        if (!tc::mbar_wait(&full[s], (uint32_t)(kb / kLmStages) & 1u, abort_flag)) break;
+        tc::fence_after_sync();
+        const uint32_t a = tc::smem_addr(pipe + s * kLmStage);
+        const uint64_t ad = tc::desc_kmajor_sw128(a);
+        const uint64_t bd = tc::desc_kmajor_sw128(a + kLmA);
+#pragma unroll
+        for (int k = 0; k < kLmBK / 16; ++k)
+          tc::mma_bf16_ss(tmem, ad + 2 * k, bd + 2 * k, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+        tc::mma_commit(&empty[s]);
+      }
+      tc::mma_commit(tmem_full);
+    }
+    __syncwarp();
+  }
+
+  // ---- epilogue: the fp32 tile into shared memory, [window row][vocab row]
+  // (the ring has drained once every product finished)
+  float* xs = reinterpret_cast<float*>(pipe);
+  const int t = threadIdx.x - 64;  // epilogue thread = vocabulary row f0 + t
+  if (warp >= 2) {
+    tc::mbar_wait(tmem_full, 0, abort_flag);
+    tc::fence_after_sync();
+    const int q = warp & 3;
+    const uint32_t t_lane = tmem + ((uint32_t)(q * 32) << 16);
+    const int tq = q * 32 + lane;  // TMEM lane = vocabulary row f0 + tq
+    const bool live = f0 + tq < p.vocab;
+    for (int c0 = 0; c0 < kLmBN; c0 += 16) {
+      float v[16];
+      tc::tmem_ld_32x32b_x16(t_lane + c0, v);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) xs[(c0 + j) * kLmXs + tq] = live ? v[j] : -INFINITY;
+    }
+    tc::named_bar(1, 128);
+    // column c (window row) over the 128 vocabulary rows: two threads per
+    // column, 64 rows each, the maximum (first on ties) before any exponential
+    const int c = t & (kLmBN - 1), half = t >> 6;
+    Stat st{-INFINITY, 0.f, 0x7fffffff};
+    if (c < R) {
+      const float* col = xs + c * kLmXs + half * 64;
+      float m = -INFINITY;
+      int mi = 0;
+      for (int r = 0; r < 64; ++r)
+        if (col[r] > m) {
+          m = col[r];
+          mi = r;
+        }
+      if (m != -INFINITY) {
+        const float mb = m * kLog2e;
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        for (int r = 0; r < 64; r += 4) {
+          a0 += ex2(fmaf(col[r], kLog2e, -mb));
+          a1 += ex2(fmaf(col[r + 1], kLog2e, -mb));
+          a2 += ex2(fmaf(col[r + 2], kLog2e, -mb));
+          a3 += ex2(fmaf(col[r + 3], kLog2e, -mb));
+        }
+        st = Stat{m, (a0 + a1) + (a2 + a3), f0 + half * 64 + mi};
+      }
+    }
+    if (half == 1) half_stat[c] = st;
+    tc::named_bar(1, 128);
+    if (half == 0 && c < R) {
+      const Stat m = merge(st, half_stat[c]);  // rows of half 0 come first: ties keep the lower index
+      float* slot = p.rp.part + ((size_t)tile * R + c) * 3;
+      __stcg(slot, m.m);
+      __stcg(slot + 1, m.s);
+      __stcg(slot + 2, __int_as_float(m.i));
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) tc::tmem_dealloc(tmem, kLmBN);
+  if (threadIdx.x == 0) {
+    if (*abort_flag) fdl::raise_error(p.rp.err, FDL_DEVERR_TIMEOUT);
+    // every CTA's statistics are released by its own add; the last arrival
+    // acquires all of them (and passes them on with the barrier below)
+    unsigned tk;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(tk) : "l"(p.rp.ticket) : "memory");
+    go = tk == gridDim.x - 1u ? 1u : 0u;
+  }
+  __syncthreads();
+  if (!go) return;
+  // ---- last CTA: each window row's statistics over all tiles, merged in a
+  // fixed order (lane l takes tiles l, l + 32, ... in order, then a fixed
+  // xor tree), then the decisions
+  const Stat none{-INFINITY, 0.f, 0x7fffffff};
+  for (int c = warp; c < R; c += kLmThreads / 32) {
+    Stat acc = none;
+    for (int tt = lane; tt < p.n_tiles; tt += 32) {
+      const float* o = p.rp.part + ((size_t)tt * R + c) * 3;
+      acc = merge(acc, Stat{__ldcg(o), __ldcg(o + 1), __float_as_int(__ldcg(o + 2))});
+    }
+    for (int off = 16; off; off >>= 1) acc = shfl_merge(acc, off);
+    if (lane == 0) {
+      const float conf = acc.s > 0.f ? 1.f / acc.s : 0.f;
+      p.rp.out_conf[c] = conf;
+      p.rp.out_arg[c] = acc.i;
+      pre_conf[c] = conf;
+    }
+  }
+  __syncthreads();
+  decide_unmask<kLmBN, kLmBN>(p.rp, pre_seq, pre_pos, pre_conf);
+  if (threadIdx.x == 0) *p.rp.ticket = 0u;  // ready for the next call
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 lm_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+// bf16 row-major [rows, cols], box kLmBK columns x box_rows rows, 128-byte swizzle
+bool lm_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto enc = lm_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kLmBK, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -583,4 +821,45 @@ cudaError_t fdl_launch_unmask_verify(fdl_ctx* ctx, const fdl_unmask_args* a) {
     e = bf16 ? launch_phase<__nv_bfloat16>(ctx, p) : launch_phase<float>(ctx, p);
   }
   return e;
+}
+
+int fdl_lm_head_max_rows() { return kLmBN; }
+
+size_t fdl_lm_partial_floats(int vocab) { return (size_t)((vocab + kLmBM - 1) / kLmBM) * kLmBN * 3; }
+
+cudaError_t fdl_launch_lm_head_unmask(fdl_ctx* ctx, const void* hidden, const void* w_lm, const fdl_unmask_args* a) {
+  const fdl_config& c = ctx->cfg;
+  if (c.dtype != FDL_BF16 || a->R_w < 1 || a->R_w > kLmBN || c.d_model % kLmBK != 0 || !ctx->lm_part)
+    return cudaErrorNotSupported;
+  if ((reinterpret_cast<uintptr_t>(hidden) | reinterpret_cast<uintptr_t>(w_lm)) & 15) return cudaErrorMisalignedAddress;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(lm_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kLmSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  CUtensorMap mw, mh;
+  if (!lm_map(&mw, w_lm, (uint64_t)c.vocab, c.d_model, kLmBM) || !lm_map(&mh, hidden, a->R_w, c.d_model, kLmBN))
+    return cudaErrorInvalidValue;
+  LmParams p = {};
+  p.rp.n_rows = a->R_w;
+  p.rp.out_conf = a->conf;
+  p.rp.out_arg = a->argmax;
+  p.rp.part = ctx->lm_part;
+  p.rp.ticket = ctx->tickets + 2;
+  p.rp.err = ctx->err_word;
+  p.rp.phase = 0;
+  p.rp.B = a->B;
+  p.rp.row_seq = a->row_seq;
+  p.rp.row_pos = a->row_pos;
+  p.rp.eps = a->eps;
+  p.rp.force_progress = a->force_progress;
+  p.rp.commit = a->commit;
+  p.rp.search_rows = a->search_rows;
+  p.rp.n_search_out = a->n_search;
+  p.rp.max_search = a->max_search;
+  p.vocab = c.vocab;
+  p.nkb = c.d_model / kLmBK;
+  p.n_tiles = (c.vocab + kLmBM - 1) / kLmBM;
+  return fdl_launch_pdl(lm_head_kernel, dim3((unsigned)p.n_tiles), dim3(kLmThreads), kLmSmem, ctx->stream, 1, mw, mh, p);
 }
