@@ -114,7 +114,7 @@ fdl_status fdl_create(const fdl_config* cfg, void* cuda_stream, fdl_ctx** out) {
     e = e ? e : cudaMalloc(&ctx->qkv_partials, ctx->qkv_partial_floats * sizeof(float));
     e = e ? e : cudaMalloc(&ctx->qkv_ticket_buf, ctx->qkv_tickets * sizeof(unsigned));
     e = e ? e : cudaMemset(ctx->qkv_ticket_buf, 0, ctx->qkv_tickets * sizeof(unsigned));
-    e = e ? e : cudaMalloc(&ctx->lm_part, fdl_lm_partial_floats(cfg->vocab) * sizeof(float));
+    e = e ? e : cudaMalloc(&ctx->lm_part, fdl_lm_partial_floats(ctx->num_sms) * sizeof(float));
   }
   e = e ? e : cudaMemcpy(ctx->rope_cos, hc.data(), n_tab * sizeof(float), cudaMemcpyHostToDevice);
   e = e ? e : cudaMemcpy(ctx->rope_sin, hs.data(), n_tab * sizeof(float), cudaMemcpyHostToDevice);

@@ -537,44 +537,50 @@ cudaError_t launch_phase(fdl_ctx* ctx, RowParams p) {
 // ---------------------------------------------------------------------------
 // Fused LM head + unmasking: logits = hidden . W_lm^T are reduced to each
 // window row's (max, argmax, sum of exponentials) tile by tile and never
-// stored. Same orientation as the projection ("swap AB"): one CTA takes 128
-// vocabulary rows (TMEM lanes) against all window rows (<= 64, TMEM
-// columns), with the weight streamed by TMA through a 4-stage ring into
-// tcgen05.mma (bf16 in, fp32 accumulate). The epilogue stages the fp32 tile
-// in shared memory and reduces every column (window row) over the tile's
-// vocabulary rows; the per-tile statistics go to the workspace, and the last
-// CTA to take the grid ticket merges them in tile order and takes the
-// decisions of the unmask phase (decide_unmask above).
+// stored. Same orientation as the projection ("swap AB"): a vocabulary tile
+// of 128 rows (TMEM lanes) against all window rows (<= 64, TMEM columns),
+// bf16 in, fp32 accumulate (tcgen05.mma). The kernel is persistent: one CTA
+// per SM loops over the tiles t = blockIdx.x + k * gridDim.x, its TMA ring
+// streams the weight across tile boundaries, and two TMEM accumulators let
+// the epilogue of tile k overlap the products of tile k + 1. The epilogue
+// stages each fp32 tile in shared memory, reduces every column (window row)
+// over the tile's vocabulary rows and merges it into the CTA's running
+// statistics in tile order; the CTA publishes them, and the last CTA to take
+// the grid ticket merges the CTAs' statistics in CTA order and takes the
+// unmask decisions (decide_unmask above). Every merge is in a fixed order.
 // ---------------------------------------------------------------------------
 constexpr int kLmBM = 128;  // vocabulary rows per tile
-constexpr int kLmBN = 64;   // window rows per tile (the whole call)
+constexpr int kLmBN = 64;   // window rows (the whole call)
 constexpr int kLmBK = 64;
-constexpr int kLmStages = 4;
+constexpr int kLmStages = 6;
 constexpr int kLmThreads = 192;
 constexpr int kLmA = kLmBM * kLmBK * 2;
 constexpr int kLmB = kLmBN * kLmBK * 2;
 constexpr int kLmStage = kLmA + kLmB;
 constexpr int kLmPipe = kLmStages * kLmStage;
-constexpr int kLmSmem = 1024 + kLmPipe + 256;
 constexpr int kLmXs = kLmBM + 1;  // padded row of the fp32 tile: column-wise reads are conflict-free
-static_assert(kLmBN * kLmXs * 4 <= kLmPipe, "the fp32 tile fits in the drained ring");
+constexpr int kLmXsBytes = kLmBN * kLmXs * 4;
+constexpr int kLmSmem = 1024 + kLmPipe + kLmXsBytes + 256;
+static_assert(kLmSmem <= 227 * 1024, "shared memory budget");
 
 struct LmParams {
-  RowParams rp;  // decisions of the unmask phase; rp.part is the per-tile workspace
+  RowParams rp;  // decisions of the unmask phase; rp.part holds the CTAs' statistics
   int vocab, nkb, n_tiles;
 };
 
-__global__ void __launch_bounds__(kLmThreads, 2)
+__global__ void __launch_bounds__(kLmThreads, 1)
     lm_head_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_h,
                    const LmParams p) {
   extern __shared__ uint8_t lm_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(lm_smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* pipe = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kLmPipe);
+  float* xs = reinterpret_cast<float*>(smem + kLmPipe);  // [window row][vocab row], padded
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kLmPipe + kLmXsBytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + kLmStages;
-  uint64_t* tmem_full = bars + 2 * kLmStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tmem_full + 1);
+  uint64_t* tmem_full = bars + 2 * kLmStages;   // [2]
+  uint64_t* tmem_empty = tmem_full + 2;         // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tmem_empty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   __shared__ Stat half_stat[kLmBN];
   __shared__ unsigned go;
@@ -582,35 +588,40 @@ __global__ void __launch_bounds__(kLmThreads, 2)
   __shared__ float pre_conf[kLmBN];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile = blockIdx.x;
-  const int f0 = tile * kLmBM;
   const int R = p.rp.n_rows;
-  const int pre = min(p.nkb, kLmStages);
+  const int n_mine = (p.n_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;  // tiles of this CTA
+  const int n_it = n_mine * p.nkb;                                                          // k-blocks of this CTA
+  auto tile_of = [&](int j) { return (int)blockIdx.x + j * (int)gridDim.x; };
+  const int pre = min(n_it, kLmStages);
   if (threadIdx.x == 0) {
     for (int s = 0; s < kLmStages; ++s) {
       tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], 1);
     }
-    tc::mbar_init(tmem_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(&tmem_full[s], 1);
+      tc::mbar_init(&tmem_empty[s], 4);  // the four epilogue warps
+    }
     *abort_flag = 0;
     tc::fence_mbar_init();
     tc::prefetch_tensormap(&tm_w);
     tc::prefetch_tensormap(&tm_h);
   }
   if (warp == 1) {
-    tc::tmem_alloc(tmem_slot, kLmBN);
+    tc::tmem_alloc(tmem_slot, 2 * kLmBN);
     tc::tmem_relinquish();
   }
   fdl::grid_dep_wait();
   fdl::grid_dep_launch();
-  if (threadIdx.x == 0) {
-    for (int it = 0; it < pre; ++it) {
-      uint8_t* a = pipe + it * kLmStage;
-      tc::mbar_arrive_expect_tx(&full[it], kLmStage);
-      tc::tma_load_2d(a, &tm_w, it * kLmBK, f0, &full[it]);
-      tc::tma_load_2d(a + kLmA, &tm_h, it * kLmBK, 0, &full[it]);
-    }
-  }
+  auto issue = [&](int it, int s) {
+    const int j = it / p.nkb, kb = it % p.nkb;
+    uint8_t* a = pipe + s * kLmStage;
+    tc::mbar_arrive_expect_tx(&full[s], kLmStage);
+    tc::tma_load_2d(a, &tm_w, kb * kLmBK, tile_of(j) * kLmBM, &full[s]);
+    tc::tma_load_2d(a + kLmA, &tm_h, kb * kLmBK, 0, &full[s]);
+  };
+  if (threadIdx.x == 0)
+    for (int it = 0; it < pre; ++it) issue(it, it);
   // every CTA may be the last: it stages the decision inputs at its start
   if ((int)threadIdx.x < R) {
     pre_seq[threadIdx.x] = p.rp.row_seq[threadIdx.x];
@@ -622,93 +633,109 @@ __global__ void __launch_bounds__(kLmThreads, 2)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
+    // ------------------------------------------------------------ producer
     if (lane == 0) {
-      for (int kb = pre; kb < p.nkb; ++kb) {
-        const int s = kb % kLmStages;
-        if (!tc::mbar_wait(&empty[s], ((uint32_t)(kb / kLmStages) & 1u) ^ 1u, abort_flag)) break;
-        uint8_t* a = pipe + s * kLmStage;
-        tc::mbar_arrive_expect_tx(&full[s], kLmStage);
-        tc::tma_load_2d(a, &tm_w, kb * kLmBK, f0, &full[s]);
-        tc::tma_load_2d(a + kLmA, &tm_h, kb * kLmBK, 0, &full[s]);
+      for (int it = pre; it < n_it; ++it) {
+        const int s = it % kLmStages;
+        if (!tc::mbar_wait(&empty[s], ((uint32_t)(it / kLmStages) & 1u) ^ 1u, abort_flag)) break;
+        issue(it, s);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_bf16_f32(kLmBM, kLmBN);
-      for (int kb = 0; kb < p.nkb; ++kb) {
-        const int s = kb % kLmStages;
-        if (!tc::mbar_wait(&full[s], (uint32_t)(kb / kLmStages) & 1u, abort_flag)) break;
+      int it = 0;
+      bool ok = true;
+      for (int j = 0; ok && j < n_mine; ++j) {
+        const int buf = j & 1;
+        // the epilogue has read this accumulator's previous tile (j - 2)
+        if (j >= 2 && !tc::mbar_wait(&tmem_empty[buf], (uint32_t)((j - 2) >> 1) & 1u, abort_flag)) break;
         tc::fence_after_sync();
-        const uint32_t a = tc::smem_addr(pipe + s * kLmStage);
-        const uint64_t ad = tc::desc_kmajor_sw128(a);
-        const uint64_t bd = tc::desc_kmajor_sw128(a + kLmA);
+        for (int kb = 0; kb < p.nkb; ++kb, ++it) {
+          const int s = it % kLmStages;
+          if (!tc::mbar_wait(&full[s], (uint32_t)(it / kLmStages) & 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t a = tc::smem_addr(pipe + s * kLmStage);
+          const uint64_t ad = tc::desc_kmajor_sw128(a);
+          const uint64_t bd = tc::desc_kmajor_sw128(a + kLmA);
 #pragma unroll
-        for (int k = 0; k < kLmBK / 16; ++k)
-          tc::mma_bf16_ss(tmem, ad + 2 * k, bd + 2 * k, idesc, (kb > 0 || k > 0) ? 1u : 0u);
-        tc::mma_commit(&empty[s]);
+          for (int k = 0; k < kLmBK / 16; ++k)
+            tc::mma_bf16_ss(tmem + buf * kLmBN, ad + 2 * k, bd + 2 * k, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+          tc::mma_commit(&empty[s]);
+        }
+        if (ok) tc::mma_commit(&tmem_full[buf]);
       }
-      tc::mma_commit(tmem_full);
     }
     __syncwarp();
-  }
-
-  // ---- epilogue: the fp32 tile into shared memory, [window row][vocab row]
-  // (the ring has drained once every product finished)
-  float* xs = reinterpret_cast<float*>(pipe);
-  const int t = threadIdx.x - 64;  // epilogue thread = vocabulary row f0 + t
-  if (warp >= 2) {
-    tc::mbar_wait(tmem_full, 0, abort_flag);
-    tc::fence_after_sync();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int t = threadIdx.x - 64;  // 0..127
     const int q = warp & 3;
+    const int tq = q * 32 + lane;    // TMEM lane = vocabulary row tile * 128 + tq
     const uint32_t t_lane = tmem + ((uint32_t)(q * 32) << 16);
-    const int tq = q * 32 + lane;  // TMEM lane = vocabulary row f0 + tq
-    const bool live = f0 + tq < p.vocab;
-    for (int c0 = 0; c0 < kLmBN; c0 += 16) {
-      float v[16];
-      tc::tmem_ld_32x32b_x16(t_lane + c0, v);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) xs[(c0 + j) * kLmXs + tq] = live ? v[j] : -INFINITY;
-    }
-    tc::named_bar(1, 128);
-    // column c (window row) over the 128 vocabulary rows: two threads per
-    // column, 64 rows each, the maximum (first on ties) before any exponential
     const int c = t & (kLmBN - 1), half = t >> 6;
-    Stat st{-INFINITY, 0.f, 0x7fffffff};
-    if (c < R) {
-      const float* col = xs + c * kLmXs + half * 64;
-      float m = -INFINITY;
-      int mi = 0;
-      for (int r = 0; r < 64; ++r)
-        if (col[r] > m) {
-          m = col[r];
-          mi = r;
-        }
-      if (m != -INFINITY) {
-        const float mb = m * kLog2e;
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-        for (int r = 0; r < 64; r += 4) {
-          a0 += ex2(fmaf(col[r], kLog2e, -mb));
-          a1 += ex2(fmaf(col[r + 1], kLog2e, -mb));
-          a2 += ex2(fmaf(col[r + 2], kLog2e, -mb));
-          a3 += ex2(fmaf(col[r + 3], kLog2e, -mb));
-        }
-        st = Stat{m, (a0 + a1) + (a2 + a3), f0 + half * 64 + mi};
+    Stat run{-INFINITY, 0.f, 0x7fffffff};  // half 0: column c's statistics over this CTA's tiles so far
+    for (int j = 0; j < n_mine; ++j) {
+      const int buf = j & 1;
+      const int f0 = tile_of(j) * kLmBM;
+      const bool got = __all_sync(0xffffffffu, tc::mbar_wait(&tmem_full[buf], (uint32_t)(j >> 1) & 1u, abort_flag));
+      tc::fence_after_sync();
+      tc::named_bar(1, 128);  // the previous tile's column reads of xs are done
+      const bool live = f0 + tq < p.vocab;
+#pragma unroll 1
+      for (int c0 = 0; c0 < kLmBN; c0 += 16) {
+        float v[16];
+        if (got) tc::tmem_ld_32x32b_x16(t_lane + buf * kLmBN + c0, v);
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) xs[(c0 + jj) * kLmXs + tq] = (got && live) ? v[jj] : -INFINITY;
       }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&tmem_empty[buf]);  // the accumulator may take tile j + 2
+      tc::named_bar(1, 128);
+      // column c over the tile's 128 vocabulary rows: two threads per column,
+      // 64 rows each, the maximum (first on ties) before any exponential
+      Stat st{-INFINITY, 0.f, 0x7fffffff};
+      if (c < R) {
+        const float* col = xs + c * kLmXs + half * 64;
+        float m = -INFINITY;
+        int mi = 0;
+        for (int r = 0; r < 64; ++r)
+          if (col[r] > m) {
+            m = col[r];
+            mi = r;
+          }
+        if (m != -INFINITY) {
+          const float mb = m * kLog2e;
+          float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+          for (int r = 0; r < 64; r += 4) {
+            a0 += ex2(fmaf(col[r], kLog2e, -mb));
+            a1 += ex2(fmaf(col[r + 1], kLog2e, -mb));
+            a2 += ex2(fmaf(col[r + 2], kLog2e, -mb));
+            a3 += ex2(fmaf(col[r + 3], kLog2e, -mb));
+          }
+          st = Stat{m, (a0 + a1) + (a2 + a3), f0 + half * 64 + mi};
+        }
+      }
+      if (half == 1) half_stat[c] = st;
+      tc::named_bar(1, 128);
+      if (half == 0 && c < R) run = merge(run, merge(st, half_stat[c]));  // tile order; lower rows first
     }
-    if (half == 1) half_stat[c] = st;
-    tc::named_bar(1, 128);
     if (half == 0 && c < R) {
-      const Stat m = merge(st, half_stat[c]);  // rows of half 0 come first: ties keep the lower index
-      float* slot = p.rp.part + ((size_t)tile * R + c) * 3;
-      __stcg(slot, m.m);
-      __stcg(slot + 1, m.s);
-      __stcg(slot + 2, __int_as_float(m.i));
+      float* slot = p.rp.part + ((size_t)blockIdx.x * R + c) * 3;
+      __stcg(slot, run.m);
+      __stcg(slot + 1, run.s);
+      __stcg(slot + 2, __int_as_float(run.i));
     }
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 1) tc::tmem_dealloc(tmem, kLmBN);
+  if (warp == 1) tc::tmem_dealloc(tmem, 2 * kLmBN);
   if (threadIdx.x == 0) {
     if (*abort_flag) fdl::raise_error(p.rp.err, FDL_DEVERR_TIMEOUT);
     // every CTA's statistics are released by its own add; the last arrival
@@ -719,14 +746,14 @@ __global__ void __launch_bounds__(kLmThreads, 2)
   }
   __syncthreads();
   if (!go) return;
-  // ---- last CTA: each window row's statistics over all tiles, merged in a
-  // fixed order (lane l takes tiles l, l + 32, ... in order, then a fixed
-  // xor tree), then the decisions
+  // ---- last CTA: each window row's statistics over all CTAs, merged in a
+  // fixed order (lane l takes CTAs l, l + 32, ... in order, then a fixed xor
+  // tree), then the decisions
   const Stat none{-INFINITY, 0.f, 0x7fffffff};
   for (int c = warp; c < R; c += kLmThreads / 32) {
     Stat acc = none;
-    for (int tt = lane; tt < p.n_tiles; tt += 32) {
-      const float* o = p.rp.part + ((size_t)tt * R + c) * 3;
+    for (int cta = lane; cta < (int)gridDim.x; cta += 32) {
+      const float* o = p.rp.part + ((size_t)cta * R + c) * 3;
       acc = merge(acc, Stat{__ldcg(o), __ldcg(o + 1), __float_as_int(__ldcg(o + 2))});
     }
     for (int off = 16; off; off >>= 1) acc = shfl_merge(acc, off);
@@ -825,7 +852,7 @@ cudaError_t fdl_launch_unmask_verify(fdl_ctx* ctx, const fdl_unmask_args* a) {
 
 int fdl_lm_head_max_rows() { return kLmBN; }
 
-size_t fdl_lm_partial_floats(int vocab) { return (size_t)((vocab + kLmBM - 1) / kLmBM) * kLmBN * 3; }
+size_t fdl_lm_partial_floats(int num_sms) { return (size_t)num_sms * kLmBN * 3; }
 
 cudaError_t fdl_launch_lm_head_unmask(fdl_ctx* ctx, const void* hidden, const void* w_lm, const fdl_unmask_args* a) {
   const fdl_config& c = ctx->cfg;
@@ -861,5 +888,7 @@ cudaError_t fdl_launch_lm_head_unmask(fdl_ctx* ctx, const void* hidden, const vo
   p.vocab = c.vocab;
   p.nkb = c.d_model / kLmBK;
   p.n_tiles = (c.vocab + kLmBM - 1) / kLmBM;
-  return fdl_launch_pdl(lm_head_kernel, dim3((unsigned)p.n_tiles), dim3(kLmThreads), kLmSmem, ctx->stream, 1, mw, mh, p);
+  // persistent: one CTA per SM (or per tile when there are fewer tiles)
+  const int grid = min(p.n_tiles, ctx->num_sms);
+  return fdl_launch_pdl(lm_head_kernel, dim3((unsigned)grid), dim3(kLmThreads), kLmSmem, ctx->stream, 1, mw, mh, p);
 }
