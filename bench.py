@@ -428,9 +428,10 @@ def run_gpu(args, world, rank, local):
 # ---------------------------------------------------------------------------
 def run_configs(args):
     """Times each kernel of the path on the ragged batch, one layer of the
-    32-layer chain and the Flash-Verify stress workload: CUDA-graph replays
-    of one call, µs per call, and algorithmic TFLOP/s or GB/s against the
-    measured peaks. Prints one JSON line per configuration."""
+    32-layer chain and the Flash-Verify stress workload, and the fused LM
+    head + unmasking over the LLaDA vocabulary: CUDA-graph replays of one
+    call, µs per call, and algorithmic TFLOP/s or GB/s against the measured
+    peaks. Prints one JSON line per configuration."""
     import torch
 
     import kv_cache_attention_gb300 as fdl
@@ -582,6 +583,29 @@ def run_configs(args):
     ctx.sync_status()
     results.append({"config": "flash_verify_b32", **res})
     ctx.close()
+
+    # fused LM head + eps unmasking (the step after the layers): the LLaDA
+    # vocabulary and width against the 32 window rows; the weight (1.04 GB,
+    # two seeded copies) is the algorithmic traffic
+    d, V, Rw = 4096, 126464, 32
+    ctx = fdl.fdl_create(d, 32, 128, 5e5, 1, 64, 0, 64, 1, 64, V, "bf16", stream=stream)
+    gen = torch.Generator(device="cuda").manual_seed(1009)
+    W_lm = [(torch.randn((V, d), device="cuda", generator=gen) * 0.02).bfloat16() for _ in range(2)]
+    hid = torch.randn((Rw, d), device="cuda", generator=gen).bfloat16()
+    rs, rp = i32(np.zeros(Rw)), i32(512 + np.arange(Rw))
+    conf = torch.empty(Rw, dtype=torch.float32, device="cuda")
+    arg = torch.empty(Rw, dtype=torch.int32, device="cuda")
+    com = torch.empty(Rw, dtype=torch.uint8, device="cuda")
+    srows = torch.empty((1, 16), dtype=torch.int32, device="cuda")
+    nsr = torch.empty((1,), dtype=torch.int32, device="cuda")
+    lm = [lambda W=W: ctx.lm_head_unmask(hid, W, 1, 16, row_seq=rs, row_pos=rp, eps=0.9, force_progress=True,
+                                         conf=conf, argmax=arg, commit=com, search_rows=srows, n_search=nsr)
+          for W in W_lm]
+    res = {"lm_head_unmask": entry(timed(lm, 50), 2.0 * Rw * V * d, 2.0 * (V * d + Rw * d))}
+    ctx.sync_status()
+    results.append({"config": "lm_head_llada_vocab_w32", "rows": Rw, **res})
+    ctx.close()
+    del W_lm
     for r in results:
         r.update({"peaks": {"hbm_gbs": hbm, "bf16_tflops": tc, "source": src},
                   "timing": "CUDA-graph replays of one call on the dedicated stream; algorithmic work"})
@@ -597,7 +621,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--configs", action="store_true",
-                    help="time each kernel on the ragged-batch, 32-layer-chain and Flash-Verify workloads")
+                    help="time each kernel on the ragged-batch, 32-layer-chain and Flash-Verify workloads, "
+                         "and the fused LM head")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.configs:
