@@ -18,14 +18,18 @@ Every function cites the passage it follows. Pages cited:
         Eq. (2)), "Reproduction" (hyper-parameters).
   [FA]  "What is Flash-dLLM? ..." article: section "How does Flash-Verify let
         the model draft and verify itself?".
-  [FAST] Fast-dLLM news piece: section "Confidence-aware parallel decoding".
+  [FAST] Fast-dLLM news piece: sections "Confidence-aware parallel decoding"
+        and the key-value cache for block-wise decoding (PrefixCache,
+        DualCache; oracle/refresh.py).
+  [FREE] FlashDLM note: key design 1, FreeCache (oracle/refresh.py).
 
 Readings of silent or conflicting points (RoPE convention, view-visibility
 rule, acceptance order, tie-breaks, ...) are listed in the repository's
 design notes; each function states the reading it uses.
 
 Parity status: every function below is pinned by tests/test_oracle_pins.py
-(closed forms, hand-worked golden fixtures, invariants, brute force). The
+(closed forms, hand-worked golden fixtures, invariants, brute force), and the
+refresh policies of oracle/refresh.py by tests/test_refresh_pins.py. The
 accuracy effect of the selective refresh itself is out of scope and not
 modelled.
 """
