@@ -431,7 +431,9 @@ def run_configs(args):
     32-layer chain and the Flash-Verify stress workload, and the fused LM
     head + unmasking over the LLaDA vocabulary: CUDA-graph replays of one
     call, µs per call, and algorithmic TFLOP/s or GB/s against the measured
-    peaks. Prints one JSON line per configuration."""
+    peaks. Then one layer's projection + attention over a whole scripted
+    decode under each KV-cache refresh policy, against the sum of the
+    per-kernel roofline floors. Prints one JSON line per configuration."""
     import torch
 
     import kv_cache_attention_gb300 as fdl
@@ -606,6 +608,81 @@ def run_configs(args):
     results.append({"config": "lm_head_llada_vocab_w32", "rows": Rw, **res})
     ctx.close()
     del W_lm
+
+    # KV-cache refresh policies over one scripted decode of one layer: LLaDA
+    # layer shape, batch 1, prompt 512 + gen 256, block (window) 32, two
+    # positions unmasked per step (128 steps). Each step is the projection
+    # and the attention of the rows the policy chooses, one graph per step,
+    # replayed in order; the two weight copies alternate between steps
+    # (200 MB > L2).
+    d, Hh, hd, P, G, blk = 4096, 32, 128, 512, 256, 32
+    N = P + G
+    ctx = fdl.fdl_create(d, Hh, hd, 5e5, 1, N, 0, N, 1, N, 16, "bf16", stream=stream)
+    gen = torch.Generator(device="cuda").manual_seed(1011)
+    Ws = [(torch.randn((3 * d, d), device="cuda", generator=gen) * 0.02).bfloat16() for _ in range(2)]
+    X = torch.randn((N, d), device="cuda", generator=gen).bfloat16()
+    kc = torch.zeros((N, d), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    q = torch.empty((N, Hh, hd), dtype=torch.bfloat16, device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty((N, Hh), dtype=torch.float32, device="cuda")
+    track = torch.zeros((1, N), dtype=torch.float32, device="cuda")
+    bt, kvl = i32([[0]]), i32([N])
+    names = {fdl.FDL_REFRESH_FULL: "full_recompute", fdl.FDL_REFRESH_PREFIX: "fastdllm_prefix_cache",
+             fdl.FDL_REFRESH_DUAL: "fastdllm_dual_cache", fdl.FDL_REFRESH_FREECACHE: "freecache",
+             fdl.FDL_REFRESH_FLASH_DRAFT: "flash_dllm_draft_forward_only"}
+    for policy, name in names.items():
+        rng = np.random.default_rng([1011, policy])
+        masked = np.zeros((1, N), np.uint8)
+        masked[0, P:] = 1
+        state = np.full(1, -1, np.int32)
+        steps = []
+        while masked.any():
+            tracked = n_tracked = None
+            if policy == fdl.FDL_REFRESH_FLASH_DRAFT:
+                tracked = rng.permutation(np.nonzero(masked[0] == 0)[0])[:32].astype(np.int32)[None]
+                n_tracked = np.array([tracked.shape[1]], np.int32)
+            rows = fdl.fdl_refresh_rows(policy, [P], [N], masked, blk, state, tracked, n_tracked)
+            steps.append(rows)
+            masked[0, synth.trace_unmask(rng, rows.row_rope_pos[rows.row_kind == 1], 2, 2)] = 0
+        graphs, keep, n_rows, floor_us = [], [], 0, 0.0
+        for t, rows in enumerate(steps):
+            R = rows.n_rows
+            args_t = (i32(rows.row_seq), i32(rows.row_rope_pos), i32(rows.row_kind), i32(rows.cu_seqlens))
+            keep.append(args_t)
+            rs, rp, rk, cu = args_t
+            tr = track if policy == fdl.FDL_REFRESH_FLASH_DRAFT else None
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                ctx.qkv_rope_cache_write(X[:R], Ws[t % 2], rs, rp, rp, bt, kc, vc, q[:R])
+                ctx.sched_attn(q[:R], kc, vc, bt, cu, kvl, rk, o[:R], lse_out=lse[:R], track_scores=tr)
+            graphs.append(g)
+            n_rows += R
+            qkv_fl, qkv_by = 2.0 * R * 3 * d * d, 2.0 * (3 * d * d + 4 * R * d)
+            att_fl, att_by = 4.0 * d * R * N, 2.0 * (2 * d * N + 2 * R * d)
+            floor_us += max(qkv_by / hbm * 1e-3, qkv_fl / tc * 1e-6) + max(att_by / hbm * 1e-3, att_fl / tc * 1e-6)
+        for _ in range(2):
+            for g in graphs:
+                g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        passes = 5
+        a.record(stream)
+        for _ in range(passes):
+            for g in graphs:
+                g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ctx.sync_status()
+        us = a.elapsed_time(b) / passes * 1e3
+        results.append({"config": f"refresh_{name}_llada_b1_p512_g256_blk32", "steps": len(steps),
+                        "rows": n_rows, "us_per_decode_layer": round(us, 1),
+                        "us_per_step": round(us / len(steps), 2),
+                        "rows_per_s": round(n_rows / us * 1e6, 1),
+                        "roofline_floor_us": round(floor_us, 1), "frac_roofline": round(floor_us / us, 3)})
+        del graphs, keep
+    ctx.close()
+    del Ws
     for r in results:
         r.update({"peaks": {"hbm_gbs": hbm, "bf16_tflops": tc, "source": src},
                   "timing": "CUDA-graph replays of one call on the dedicated stream; algorithmic work"})
@@ -622,7 +699,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--configs", action="store_true",
                     help="time each kernel on the ragged-batch, 32-layer-chain and Flash-Verify workloads, "
-                         "and the fused LM head")
+                         "the fused LM head, and one layer's decode under each KV-cache refresh policy")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.configs:

@@ -17,8 +17,13 @@
  *   fdl_lm_head_unmask        the unmasking decisions straight from the window
  *                             rows' hidden states (LM head fused, logits never
  *                             stored)
+ *   fdl_refresh_rows          (host) the query rows of a step under a KV-cache
+ *                             refresh policy: Fast-dLLM PrefixCache and
+ *                             DualCache, FlashDLM FreeCache, the Flash-dLLM
+ *                             draft forward
+ *   fdl_verify_rows           (host) the query rows of a Flash-Verify forward
  *
- * Conventions shared by every entry point
+ * Conventions shared by every entry point (but the two host row builders)
  *   - All tensor arguments are DEVICE pointers owned by the caller (for
  *     example PyTorch allocations); the library never frees them.
  *   - Every call is asynchronous on the context's CUDA stream.
@@ -281,6 +286,111 @@ fdl_status fdl_sched_attn_noalloc(const fdl_config* cfg, void* cuda_stream, cons
                                   const int* row_kind, const int* search_pos, int search_ld,
                                   const int* n_search, void* o_out, float* lse_out, float* track_scores,
                                   int track_ld, unsigned* device_error);
+
+/* ------------------------------------------------------------------------
+ * Row descriptors of one step under a KV-cache refresh policy (HOST code:
+ * every pointer below is a host pointer; no context, no GPU work).
+ *
+ * A refresh policy only chooses which positions a step recomputes. Each
+ * chosen row gets rope position = cache position = its position (its K/V
+ * overwrite the cache there) and attends over the whole cache (kv_len of its
+ * sequence = seq_len). Positions not chosen keep the K/V last written.
+ * Blocks start at the end of the prompt: block i of sequence b covers
+ * [prompt_len[b] + i*block, min(prompt_len[b] + (i+1)*block, seq_len[b])).
+ * The current block is the first one still holding a masked position.
+ *
+ *   FDL_REFRESH_FULL       every position, every step (no cache reuse).
+ *   FDL_REFRESH_PREFIX     Fast-dLLM PrefixCache (Fast-dLLM news piece, the
+ *                          key-value cache for block-wise decoding): the
+ *                          current block and everything after it; at the
+ *                          first step of every block (state != current
+ *                          block) every position, which is how the cache of
+ *                          all tokens is recomputed once a block is decoded.
+ *   FDL_REFRESH_DUAL       Fast-dLLM DualCache: the current block only (the
+ *                          masked suffix stays cached); every position at the
+ *                          first step of every block.
+ *   FDL_REFRESH_FREECACHE  FlashDLM FreeCache (FlashDLM note, key design 1):
+ *                          every position at the first step (state == -1),
+ *                          then the current block and every later block;
+ *                          finished blocks and the prompt stay frozen.
+ *   FDL_REFRESH_FLASH_DRAFT  Flash-dLLM (paper digest, Algorithm 2 steps 1
+ *                          and 2): every position at the first step (state
+ *                          == -1, the initial full forward), then the draft
+ *                          forward's query: the window (the first `block` still-
+ *                          masked positions at or after the prompt, in
+ *                          position order) followed by the tracked positions
+ *                          in the order given.
+ *
+ * Row kinds: FDL_KIND_WINDOW for the rows whose predictions are decoded (the
+ * still-masked positions of the current block; for FLASH_DRAFT the window),
+ * FDL_KIND_NORMAL for every other row. Rows of a sequence are contiguous
+ * (cu_seqlens) and, except for FLASH_DRAFT, in ascending position order. A
+ * sequence with no masked position left takes no rows and keeps its state.
+ *
+ * state[b] carries the policy's memory between steps: set it to -1 before a
+ * sequence's first step; the call updates it (the block refreshed in full
+ * last; 0 for FLASH_DRAFT after its first step).
+ *
+ * Errors (FDL_ERR_INVALID_ARG; nothing written, state untouched): a NULL
+ * pointer the policy needs, B < 1, block < 1, an unknown policy, prompt_len
+ * or seq_len outside 0 <= prompt_len <= seq_len <= max_seq, state < -1,
+ * n_tracked outside [0, tracked_ld], a tracked position outside the sequence,
+ * masked or repeated, or more rows than max_rows.
+ * ---------------------------------------------------------------------- */
+typedef enum {
+  FDL_REFRESH_FULL = 0,
+  FDL_REFRESH_PREFIX = 1,
+  FDL_REFRESH_DUAL = 2,
+  FDL_REFRESH_FREECACHE = 3,
+  FDL_REFRESH_FLASH_DRAFT = 4
+} fdl_refresh_policy;
+
+typedef struct {
+  int policy;                  /* fdl_refresh_policy                                */
+  int B;                       /* sequences                                         */
+  int max_seq;                 /* row stride of masked                              */
+  int block;                   /* block size; the window size for FLASH_DRAFT       */
+  const int* prompt_len;       /* [B]                                               */
+  const int* seq_len;          /* [B] N_b                                           */
+  const unsigned char* masked; /* [B*max_seq] 1 = position still masked             */
+  int* state;                  /* [B] in/out, -1 before the first step              */
+  const int* tracked;          /* FLASH_DRAFT only: [B*tracked_ld] positions        */
+  int tracked_ld;
+  const int* n_tracked;        /* FLASH_DRAFT only: [B]                             */
+  int max_rows;                /* capacity of the four row arrays                   */
+  int* row_seq;                /* [max_rows] out                                    */
+  int* row_rope_pos;           /* [max_rows] out                                    */
+  int* row_cache_pos;          /* [max_rows] out                                    */
+  int* row_kind;               /* [max_rows] out                                    */
+  int* cu_seqlens;             /* [B+1] out                                         */
+  int* n_rows;                 /* [1] out: total rows                               */
+} fdl_refresh_args;
+
+fdl_status fdl_refresh_rows(const fdl_refresh_args* args);
+
+/* ------------------------------------------------------------------------
+ * Row descriptors of a Flash-dLLM verify forward (HOST code, host pointers;
+ * paper digest, Algorithm 2 step 3, and the aiposthub article's Flash-Verify
+ * section). For sequence b with m = n_search[b] search tokens s_0..s_{m-1}
+ * (search_pos[b*search_ld + j], in acceptance order):
+ *   - the first max(0, query_budget - 2m) tracked positions (tracked[b*
+ *     tracked_ld ...], ordered by score, n_tracked[b] of them) as
+ *     FDL_KIND_NORMAL rows at their own positions;
+ *   - then s_j's draft view: rope position s_j, cache position seq_len[b] + j,
+ *     kind FDL_KIND_DRAFT_VIEW(j);
+ *   - then s_j's mask view: rope position s_j, cache position seq_len[b] + m
+ *     + j, kind FDL_KIND_MASK_VIEW(j).
+ * The attention of this forward takes kv_len = seq_len and search_pos /
+ * n_search as given here. Errors (FDL_ERR_INVALID_ARG, nothing written): a
+ * NULL pointer, B < 1, query_budget < 0, n_tracked or n_search outside
+ * [0, ld], a tracked or search position outside [0, seq_len[b]), a repeated
+ * search position, or more rows than max_rows.
+ * ---------------------------------------------------------------------- */
+fdl_status fdl_verify_rows(int B, const int* seq_len, const int* tracked, int tracked_ld,
+                           const int* n_tracked, const int* search_pos, int search_ld,
+                           const int* n_search, int query_budget, int max_rows, int* row_seq,
+                           int* row_rope_pos, int* row_cache_pos, int* row_kind, int* cu_seqlens,
+                           int* n_rows);
 
 #ifdef __cplusplus
 }

@@ -43,7 +43,14 @@ EXPORTS = (
     "fdl_create", "fdl_destroy", "fdl_set_stream", "fdl_last_error", "fdl_sync_status",
     "fdl_tile_m", "fdl_worklist_capacity", "fdl_qkv_rope_cache_write", "fdl_sched_attn",
     "fdl_track_topk", "fdl_unmask_verify", "fdl_sched_attn_noalloc", "fdl_lm_head_unmask",
+    "fdl_refresh_rows", "fdl_verify_rows",
 )
+
+FDL_REFRESH_FULL = 0
+FDL_REFRESH_PREFIX = 1
+FDL_REFRESH_DUAL = 2
+FDL_REFRESH_FREECACHE = 3
+FDL_REFRESH_FLASH_DRAFT = 4
 
 
 class FdlError(RuntimeError):
@@ -72,6 +79,16 @@ class fdl_unmask_args(ctypes.Structure):
         ("conf", _P), ("argmax", _P), ("commit", _P), ("search_rows", _P), ("n_search", _P),
         ("mask_logits", _P), ("draft_tok", _P), ("gamma", ctypes.c_float),
         ("accept", _P), ("n_accept", _P), ("mask_conf", _P), ("mask_argmax", _P),
+    ]
+
+
+class fdl_refresh_args(ctypes.Structure):
+    _fields_ = [
+        ("policy", ctypes.c_int), ("B", ctypes.c_int), ("max_seq", ctypes.c_int), ("block", ctypes.c_int),
+        ("prompt_len", _P), ("seq_len", _P), ("masked", _P), ("state", _P),
+        ("tracked", _P), ("tracked_ld", ctypes.c_int), ("n_tracked", _P), ("max_rows", ctypes.c_int),
+        ("row_seq", _P), ("row_rope_pos", _P), ("row_cache_pos", _P), ("row_kind", _P),
+        ("cu_seqlens", _P), ("n_rows", _P),
     ]
 
 
@@ -114,6 +131,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.fdl_sched_attn_noalloc.argtypes = [ctypes.POINTER(fdl_config), p, p, p, p, p, i, p, p, i, i, p, p, i, p, p,
                                          p, p, i, p]
     L.fdl_sched_attn_noalloc.restype = i
+    L.fdl_refresh_rows.argtypes = [ctypes.POINTER(fdl_refresh_args)]
+    L.fdl_refresh_rows.restype = i
+    L.fdl_verify_rows.argtypes = [i, p, p, i, p, p, i, p, i, i, p, p, p, p, p, p]
+    L.fdl_verify_rows.restype = i
     _lib = L
     return L
 
@@ -292,3 +313,89 @@ def fdl_sched_attn_noalloc(cfg: fdl_config, q, k_cache, v_cache, block_table, cu
         search_ld, _ptr(n_search), _ptr(o_out), _ptr(lse_out), _ptr(track_scores), track_ld, _ptr(device_error))
     if st != FDL_OK:
         raise FdlError(st, "fdl_sched_attn_noalloc (reason on stderr)")
+
+
+# Host row builders (numpy arrays in and out; no GPU involved).
+class Rows:
+    """Row descriptors of one call (int32 numpy arrays)."""
+
+    def __init__(self, row_seq, row_rope_pos, row_cache_pos, row_kind, cu_seqlens):
+        self.row_seq, self.row_rope_pos, self.row_cache_pos = row_seq, row_rope_pos, row_cache_pos
+        self.row_kind, self.cu_seqlens = row_kind, cu_seqlens
+
+    @property
+    def n_rows(self) -> int:
+        return int(self.row_seq.shape[0])
+
+
+def _host(a, dtype, name: str, writable: bool = False):
+    """Contiguous host array of ``dtype`` and its address (None stays NULL)."""
+    import numpy as np
+    if a is None:
+        return None, None
+    if writable:
+        if not (isinstance(a, np.ndarray) and a.dtype == dtype and a.flags.c_contiguous):
+            raise FdlError(FDL_ERR_INVALID_ARG, f"{name} must be a contiguous {np.dtype(dtype).name} numpy array")
+        arr = a
+    else:
+        arr = np.ascontiguousarray(a, dtype=dtype)
+    return arr, arr.ctypes.data
+
+
+def fdl_refresh_rows(policy: int, prompt_len, seq_len, masked, block: int, state, tracked=None,
+                     n_tracked=None, max_rows: int | None = None) -> Rows:
+    """Rows of one step under a refresh policy (see include/fdl.h).
+
+    ``masked`` is uint8 [B, max_seq]; ``state`` an int32 numpy array [B]
+    (-1 before the first step) that the call updates in place; ``tracked``
+    int32 [B, ld] and ``n_tracked`` [B] for FDL_REFRESH_FLASH_DRAFT.
+    """
+    import numpy as np
+    m, mp = _host(masked, np.uint8, "masked")
+    pl, plp = _host(prompt_len, np.int32, "prompt_len")
+    sl, slp = _host(seq_len, np.int32, "seq_len")
+    _, stp = _host(state, np.int32, "state", writable=True)
+    tr, trp = _host(tracked, np.int32, "tracked")
+    _, ntp = _host(n_tracked, np.int32, "n_tracked")
+    B, max_seq = int(m.shape[0]), int(m.shape[1])
+    if max_rows is None:
+        max_rows = int(sl.sum()) + (int(tr.size) if tr is not None else 0)
+    out = [np.empty(max(max_rows, 1), np.int32) for _ in range(4)]
+    cu = np.empty(B + 1, np.int32)
+    n = np.zeros(1, np.int32)
+    a = fdl_refresh_args()
+    a.policy, a.B, a.max_seq, a.block = int(policy), B, max_seq, int(block)
+    a.prompt_len, a.seq_len, a.masked, a.state = plp, slp, mp, stp
+    a.tracked, a.tracked_ld = trp, int(tr.shape[-1]) if tr is not None else 0
+    a.n_tracked, a.max_rows = ntp, int(max_rows)
+    a.row_seq, a.row_rope_pos, a.row_cache_pos, a.row_kind = (o.ctypes.data for o in out)
+    a.cu_seqlens, a.n_rows = cu.ctypes.data, n.ctypes.data
+    st = load_library().fdl_refresh_rows(ctypes.byref(a))
+    if st != FDL_OK:
+        raise FdlError(st, "fdl_refresh_rows rejected its arguments")
+    r = int(n[0])
+    return Rows(*(o[:r] for o in out), cu)
+
+
+def fdl_verify_rows(seq_len, tracked, n_tracked, search_pos, n_search, query_budget: int,
+                    max_rows: int | None = None) -> Rows:
+    """Rows of a Flash-Verify forward (see include/fdl.h); int32 host arrays."""
+    import numpy as np
+    sl, slp = _host(seq_len, np.int32, "seq_len")
+    tr, trp = _host(tracked, np.int32, "tracked")
+    _, ntp = _host(n_tracked, np.int32, "n_tracked")
+    sp, spp = _host(search_pos, np.int32, "search_pos")
+    _, nsp = _host(n_search, np.int32, "n_search")
+    B = int(sl.shape[0])
+    if max_rows is None:
+        max_rows = int(tr.size) + 2 * int(sp.size)
+    out = [np.empty(max(max_rows, 1), np.int32) for _ in range(4)]
+    cu = np.empty(B + 1, np.int32)
+    n = np.zeros(1, np.int32)
+    st = load_library().fdl_verify_rows(B, slp, trp, int(tr.shape[-1]), ntp, spp, int(sp.shape[-1]), nsp,
+                                        int(query_budget), int(max_rows), *(o.ctypes.data for o in out),
+                                        cu.ctypes.data, n.ctypes.data)
+    if st != FDL_OK:
+        raise FdlError(st, "fdl_verify_rows rejected its arguments")
+    r = int(n[0])
+    return Rows(*(o[:r] for o in out), cu)

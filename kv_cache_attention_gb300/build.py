@@ -1,7 +1,8 @@
 """Builds libfdl.so in-tree with nvcc for sm_103a (GB300) only.
 
-Each ``csrc/*.cu`` translation unit is compiled in parallel to an object under
-``_build/`` and the objects are linked into ``libfdl.so`` next to this file.
+Each ``csrc/*.cu`` translation unit (and each host-only ``csrc/*.cpp`` one) is
+compiled in parallel to an object under ``_build/`` and the objects are linked
+into ``libfdl.so`` next to this file.
 The CUDA runtime is linked statically, so the library depends only on the
 driver at run time (the tensor-map encoder is fetched through the runtime's
 driver entry-point query rather than by linking libcuda).
@@ -40,15 +41,19 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
+def _obj(src: str) -> str:
+    return os.path.join(OBJDIR, os.path.splitext(os.path.basename(src))[0] + ".o")
+
+
 def build(verbose: bool = False, extra_flags=None) -> str:
     """Compiles (if needed) and returns the path of libfdl.so."""
     os.makedirs(OBJDIR, exist_ok=True)
-    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
     headers = sorted(glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h")))
     flags = FLAGS + list(extra_flags or [])
     jobs = []
     for s in srcs:
-        obj = os.path.join(OBJDIR, os.path.basename(s)[:-3] + ".o")
+        obj = _obj(s)
         if _stale(obj, [s, __file__] + headers):
             jobs.append((s, obj))
 
@@ -64,7 +69,7 @@ def build(verbose: bool = False, extra_flags=None) -> str:
         for s, err in ex.map(compile_one, jobs):
             if verbose and err.strip():
                 print(f"[{os.path.basename(s)}]\n{err}")
-    objs = [os.path.join(OBJDIR, os.path.basename(s)[:-3] + ".o") for s in srcs]
+    objs = [_obj(s) for s in srcs]
     if jobs or _stale(LIB, objs):
         cmd = [nvcc()] + ARCH + ["-shared", "-o", LIB] + objs
         r = subprocess.run(cmd, capture_output=True, text=True)

@@ -470,6 +470,38 @@ def projection_case(seed: int, d_model: int, n_heads: int, n_rows: int, batch: i
 
 
 # --------------------------------------------------------------------------
+# Decode traces for the KV-cache refresh policies
+# --------------------------------------------------------------------------
+def refresh_trace(seed: int = 1010) -> Workload:
+    """Small multi-step decode for the refresh policies: bf16, d_model 512,
+    4 heads of 128, theta 1e4; 3 sequences with prompts 37, 64, 5 and gen 70,
+    48, 90 (ragged last blocks), block 16; paged cache of 64-slot pages
+    randomly permuted in one pool, zero-filled. W ~ N(0, 0.02^2)."""
+    rng = np.random.default_rng(seed)
+    shape = LayerShape(512, 4, 128, 1.0e4, "bf16")
+    prompts = np.array([37, 64, 5], np.int32)
+    lengths = (prompts + np.array([70, 48, 90])).astype(np.int32)
+    geom = paged_geometry(rng, lengths, 64)
+    w = make_tensor(normal(rng, (3 * shape.d_model, shape.d_model), 0.02), "bf16")
+    return Workload("refresh_trace", shape, 3, lengths, int(lengths.max()), 0, geom,
+                    dict(w=w, prompts=prompts, block=16, seed=seed))
+
+
+def trace_hidden(seed: int, step: int, rows: int, d: int, dtype: str = "bf16") -> Tensor:
+    """Hidden inputs of one step's rows, N(0, 1)."""
+    rng = np.random.default_rng([seed, 2, step])
+    return make_tensor(normal(rng, (rows, d)), dtype)
+
+
+def trace_unmask(rng: np.random.Generator, decoded_pos, lo: int = 1, hi: int = 4):
+    """Positions a scripted step unmasks: lo..hi of the decoded rows, at random."""
+    decoded_pos = np.asarray(decoded_pos)
+    if decoded_pos.size == 0:
+        return decoded_pos
+    return rng.permutation(decoded_pos)[:int(rng.integers(lo, hi + 1))]
+
+
+# --------------------------------------------------------------------------
 # Language-model head (the step after the path: hidden states -> decisions)
 # --------------------------------------------------------------------------
 def lm_head_case(seed: int = 1006, vocab: int = 126464, d: int = 4096, rows: int = 32,
