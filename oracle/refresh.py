@@ -20,10 +20,11 @@ Pages followed:
          whole sequence; while B_i is generated the active window is B_i and
          every block after it, and the prompt and the frozen blocks only give
          KV; when B_i is fully unmasked its KV is frozen and the window shrinks.
-  [FD]   Flash-dLLM paper digest, Algorithm 2 step 1 (the draft forward
-         recomputes the masked window and the tracked set) and the verify
-         forward (the tracked rows kept, A11, then the two views of each
-         search token).
+  [FD]   Flash-dLLM paper digest, Algorithm 2: step 1 (one full forward at
+         initialisation), step 2 (each step's query is the tracked set plus
+         the sliding masked window) and step 3 (the verify forward: the
+         tracked set shrunk to free query slots, then the draft view and the
+         mask view of each search token).
 
 Readings (where the pages leave a step open):
   * Blocks start at the end of the prompt: block i covers positions
