@@ -37,5 +37,5 @@ from .flash_dllm import (  # noqa: F401
     KIND_NORMAL, KIND_WINDOW, store_round, slot_of, slot_map, work_list,
     project_qkv, rope, qkv_rope_cache_write, visible_positions, visible_keys,
     sched_attn, track_topk, row_confidence, unmask, verify, tv_point_mass,
-    lm_head_logits, lm_head_unmask,
+    lm_head_logits, lm_head_unmask, lm_head_verify,
 )

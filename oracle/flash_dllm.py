@@ -360,6 +360,14 @@ def lm_head_unmask(hidden, w_lm, row_seq, row_pos, B: int, eps: float, force_pro
     return unmask(lm_head_logits(hidden, w_lm), row_seq, row_pos, B, eps, force_progress, max_search)
 
 
+def lm_head_verify(mask_hidden, w_lm, draft_tok, n_search, gamma: float, B: int, max_search: int):
+    """Verify-step acceptance straight from the mask views' hidden states:
+    ``verify`` of ``lm_head_logits`` ([FD "Method steps", step 3]: the mask
+    view's x_tilde and c_tilde come from the model's output distribution at
+    that view, the softmax of the same linear head as in step 2)."""
+    return verify(lm_head_logits(mask_hidden, w_lm), draft_tok, n_search, gamma, B, max_search)
+
+
 def verify(mask_logits, draft_tok, n_search, gamma: float, B: int, max_search: int):
     """Flash-Verify prefix acceptance.
 

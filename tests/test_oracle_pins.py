@@ -494,6 +494,44 @@ def test_lm_head_unmask_closed_form_and_composition():
     np.testing.assert_allclose(got["conf"], want["conf"], rtol=1e-12)
 
 
+def test_lm_head_verify_closed_form_walk():
+    # two sequences, three mask views each, orthogonal unit hidden rows: row r's
+    # logits are 0 except a_r at its aligned vocabulary row, so its confidence
+    # is e^a / (e^a + V - 1) and its argmax that row (or 0 when a_r = 0)
+    V, d, gamma = 40, 8, 0.8
+    h = np.eye(d)[:6]
+    a_r = [9.0, 9.0, 2.0, 9.0, 0.0, 9.0]            # e^9/(e^9+39) = 0.9952, e^2/(e^2+39) = 0.159
+    w = np.zeros((V, d))
+    ids = [5, 11, 23, 7, 0, 30]
+    for r, (a, v) in enumerate(zip(a_r, ids)):
+        w[v] += a * h[r]
+    conf = [math.exp(a) / (math.exp(a) + V - 1) for a in a_r]
+    # sequence 0: both confident rows agree, then row 2 is below gamma -> 2
+    # sequence 1 (two search tokens): row 3 agrees, row 4 is flat (conf 1/V) -> 1
+    draft = np.array([5, 11, 23, 7, 0, 30])
+    out = oracle.lm_head_verify(h, w, draft, np.array([3, 2]), gamma, 2, 3)
+    assert out["n_accept"].tolist() == [2, 1]
+    assert out["accept"].tolist() == [1, 1, 0, 1, 0, 0]
+    np.testing.assert_allclose(out["mask_conf"][:4], conf[:4], rtol=1e-12)
+    assert abs(out["mask_conf"][4] - 1.0 / V) < 1e-12
+    assert out["mask_argmax"].tolist()[:5] == ids[:5]
+    # a draft mismatch at the first token stops the walk at once
+    draft[0] = 6
+    assert oracle.lm_head_verify(h, w, draft, np.array([3, 2]), gamma, 2, 3)["n_accept"].tolist() == [0, 1]
+    # views past n_search never count: row 1 would be accepted, but sequence 0
+    # has one search token
+    draft[0] = 5
+    assert oracle.lm_head_verify(h, w, draft, np.array([1, 1]), gamma, 2, 3)["n_accept"].tolist() == [1, 1]
+    # composition with explicit logits
+    hidden, wl, _ = synth.lm_head_case(seed=6, vocab=300, d=32, rows=6, planted=1.0)
+    logits = hidden.values() @ wl.values().T
+    tok = np.argmax(logits, axis=1)
+    want = oracle.verify(logits, tok, np.array([3, 3]), 0.6, 2, 3)
+    got = oracle.lm_head_verify(hidden.values(), wl.values(), tok, np.array([3, 3]), 0.6, 2, 3)
+    for key in ("accept", "n_accept", "mask_argmax"):
+        assert np.array_equal(got[key], want[key])
+
+
 def test_lm_head_case_plants_confident_rows():
     # the generator's recipe: planted rows are confident in their planted id
     hidden, w, ids = synth.lm_head_case(seed=3, vocab=2048, d=128, rows=20)
