@@ -249,6 +249,14 @@ def run_gpu(args, world, rank, local):
     torch.cuda.set_stream(stream)
     ctx = fdl.fdl_create(d, Hh, hd, s.rope_theta, 1, N, wl.max_views, g.page_size, g.n_pages, R, V, "bf16",
                          stream=stream)
+    # The step's decisions run on a second stream with a context of their own
+    # (one context per stream): the unmasking needs only the step's logits
+    # and the top-k only the layer's tracker, so once the layer is done the
+    # two run concurrently.
+    dec_stream = torch.cuda.Stream()
+    ctx_dec = fdl.fdl_create(d, Hh, hd, s.rope_theta, 1, N, wl.max_views, g.page_size, g.n_pages, R, V, "bf16",
+                             stream=dec_stream)
+    layer_done, dec_done = torch.cuda.Event(), torch.cuda.Event()
 
     def bf(t):
         return torch.from_numpy(np.ascontiguousarray(t.data).view(np.int16)).view(torch.bfloat16)
@@ -296,9 +304,17 @@ def run_gpu(args, world, rank, local):
     def rest_part(c, L=None):
         L = Ls[c] if L is None else L
         ctx.sched_attn(q, KC[c], VC[c], bt, cu, kv_len, row_kind, o, lse_out=lse, track_scores=track)
+        # fork: the top-k on the layer's stream, the unmasking on the
+        # decisions' stream (it waits for the layer, as it would for the LM
+        # head's logits after the last layer); join before the next step
+        layer_done.record(stream)
         ctx.track_topk(track, elig, seq_len, k, idx, cnt)
-        ctx.unmask_verify(1, ms, logits=L, row_seq=win_seq, row_pos=win_pos, eps=e["eps"], force_progress=False,
-                          conf=conf, argmax=arg, commit=com, search_rows=srows, n_search=nsr)
+        dec_stream.wait_event(layer_done)
+        ctx_dec.unmask_verify(1, ms, logits=L, row_seq=win_seq, row_pos=win_pos, eps=e["eps"],
+                              force_progress=False, conf=conf, argmax=arg, commit=com, search_rows=srows,
+                              n_search=nsr)
+        dec_done.record(dec_stream)
+        stream.wait_event(dec_done)
 
     def step(c, X=None, L=None):
         # the tracker accumulates over a step's layers: zeroed once per step,
@@ -310,6 +326,7 @@ def run_gpu(args, world, rank, local):
     for i in range(args.warmup):
         step(i % n_copies)
     ctx.sync_status()
+    ctx_dec.sync_status()
     # The device-resident step is replayed from CUDA graphs (one per rotating
     # input copy) so host launch cost does not stand in for GPU time; the
     # graphs hold exactly the kernels a direct call launches. Nothing else is
@@ -332,6 +349,7 @@ def run_gpu(args, world, rank, local):
         step_graphs[i % n_copies].replay()
     qkv_graph.replay()
     ctx.sync_status()
+    ctx_dec.sync_status()
     K = args.steps
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
@@ -344,6 +362,7 @@ def run_gpu(args, world, rank, local):
         torch.cuda.synchronize()
     barrier(world)
     ctx.sync_status()
+    ctx_dec.sync_status()
     ms_total = t0.elapsed_time(t1)
     ms_total = max_over_ranks(ms_total, world)
     ms_step = ms_total / K
@@ -403,7 +422,7 @@ def run_gpu(args, world, rank, local):
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "global_batch": world, "seq_len": N, "rows_per_step": R,
-                   "parallelism": f"replicas{world}", "launch": "one CUDA graph replay per step",
+                   "parallelism": f"replicas{world}", "launch": "one CUDA graph replay per step; top-k and unmasking concurrent on two streams",
                    "l2_hygiene": f"{n_copies} rotating copies of W/X/cache/logits "
                    f"({per_copy * n_copies / 1e9:.2f} GB > 4x L2 {l2 / 1e6:.0f} MB)"},
         "e2e": {"value": e2e_value, "unit": "query-rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

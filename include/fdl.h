@@ -17,6 +17,8 @@
  *   fdl_lm_head_unmask        the unmasking decisions straight from the window
  *                             rows' hidden states (LM head fused, logits never
  *                             stored)
+ *   fdl_lm_head_verify        the verify acceptance straight from the mask
+ *                             views' hidden states (LM head fused)
  *   fdl_refresh_rows          (host) the query rows of a step under a KV-cache
  *                             refresh policy: Fast-dLLM PrefixCache and
  *                             DualCache, FlashDLM FreeCache, the Flash-dLLM
@@ -251,6 +253,25 @@ fdl_status fdl_unmask_verify(fdl_ctx* ctx, const fdl_unmask_args* args);
  * vocabulary run in a fixed order, so results do not depend on timing.
  * ---------------------------------------------------------------------- */
 fdl_status fdl_lm_head_unmask(fdl_ctx* ctx, const void* hidden, const void* w_lm, const fdl_unmask_args* args);
+
+/* ------------------------------------------------------------------------
+ * Fused LM head + Flash-Verify acceptance (paper digest, "Method steps in
+ * detail", step 3: the mask view's prediction x~ and confidence c~ are the
+ * argmax and the maximum of the model's output distribution at that view).
+ * The logits are never stored:
+ *   logits[r] = mask_hidden[r] . w_lm^T   for r = b*max_search + j, j < n_search[b]
+ * and the verify phase of fdl_unmask_verify is applied to them: mask_conf,
+ * mask_argmax (written for those rows only), accept and n_accept exactly as
+ * documented above, from args' B, max_search, n_search (input), draft_tok
+ * and gamma. args->logits and args->mask_logits must be NULL.
+ *
+ * mask_hidden: [B*max_search, d_model] bf16, the mask-view rows' final hidden
+ * states in the verify forward's layout (rows j >= n_search[b] are read but
+ * ignored); w_lm as for fdl_lm_head_unmask. bf16 contexts only,
+ * 1 <= B*max_search <= 64: otherwise FDL_ERR_UNSUPPORTED / FDL_ERR_INVALID_ARG.
+ * ---------------------------------------------------------------------- */
+fdl_status fdl_lm_head_verify(fdl_ctx* ctx, const void* mask_hidden, const void* w_lm,
+                              const fdl_unmask_args* args);
 
 /* ------------------------------------------------------------------------
  * Scheduled attention without any device allocation. The paper has no

@@ -43,7 +43,7 @@ EXPORTS = (
     "fdl_create", "fdl_destroy", "fdl_set_stream", "fdl_last_error", "fdl_sync_status",
     "fdl_tile_m", "fdl_worklist_capacity", "fdl_qkv_rope_cache_write", "fdl_sched_attn",
     "fdl_track_topk", "fdl_unmask_verify", "fdl_sched_attn_noalloc", "fdl_lm_head_unmask",
-    "fdl_refresh_rows", "fdl_verify_rows",
+    "fdl_refresh_rows", "fdl_verify_rows", "fdl_lm_head_verify",
 )
 
 FDL_REFRESH_FULL = 0
@@ -128,6 +128,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.fdl_unmask_verify.restype = i
     L.fdl_lm_head_unmask.argtypes = [p, p, p, ctypes.POINTER(fdl_unmask_args)]
     L.fdl_lm_head_unmask.restype = i
+    L.fdl_lm_head_verify.argtypes = [p, p, p, ctypes.POINTER(fdl_unmask_args)]
+    L.fdl_lm_head_verify.restype = i
     L.fdl_sched_attn_noalloc.argtypes = [ctypes.POINTER(fdl_config), p, p, p, p, p, i, p, p, i, i, p, p, i, p, p,
                                          p, p, i, p]
     L.fdl_sched_attn_noalloc.restype = i
@@ -244,6 +246,18 @@ class Context:
         self._check(load_library().fdl_lm_head_unmask(self.handle, _ptr(hidden), _ptr(w_lm), ctypes.byref(a)),
                     "fdl_lm_head_unmask")
 
+    def lm_head_verify(self, mask_hidden, w_lm, B: int, max_search: int, *, n_search, draft_tok,
+                       gamma: float = 0.8, accept, n_accept, mask_conf, mask_argmax) -> None:
+        """Verify acceptance straight from the mask views' hidden states
+        (mask_hidden [B*max_search, d_model], w_lm [vocab, d_model], both bf16)."""
+        a = fdl_unmask_args()
+        a.B, a.max_search = int(B), int(max_search)
+        a.n_search, a.draft_tok, a.gamma = _ptr(n_search), _ptr(draft_tok), float(gamma)
+        a.accept, a.n_accept = _ptr(accept), _ptr(n_accept)
+        a.mask_conf, a.mask_argmax = _ptr(mask_conf), _ptr(mask_argmax)
+        self._check(load_library().fdl_lm_head_verify(self.handle, _ptr(mask_hidden), _ptr(w_lm), ctypes.byref(a)),
+                    "fdl_lm_head_verify")
+
 
 def _stream_handle(stream) -> int | None:
     if stream is None:
@@ -293,6 +307,10 @@ def fdl_unmask_verify(ctx: Context, *a, **k) -> None:
 
 def fdl_lm_head_unmask(ctx: Context, *a, **k) -> None:
     ctx.lm_head_unmask(*a, **k)
+
+
+def fdl_lm_head_verify(ctx: Context, *a, **k) -> None:
+    ctx.lm_head_verify(*a, **k)
 
 
 def fdl_sched_attn_noalloc(cfg: fdl_config, q, k_cache, v_cache, block_table, cu_seqlens_q, kv_len, row_kind,

@@ -279,7 +279,29 @@ fdl_status fdl_lm_head_unmask(fdl_ctx* ctx, const void* hidden, const void* w_lm
   if (!(a->eps >= 0.f && a->eps <= 1.f)) return fail(ctx, FDL_ERR_INVALID_ARG, "eps outside [0,1]");
   if (ctx->cfg.d_model % 64 != 0)
     return fail(ctx, FDL_ERR_UNSUPPORTED, "fdl_lm_head_unmask: d_model must be a multiple of 64");
-  return launched(ctx, fdl_launch_lm_head_unmask(ctx, hidden, w_lm, a), "LM-head unmask launch");
+  return launched(ctx, fdl_launch_lm_head(ctx, hidden, w_lm, a, false), "LM-head unmask launch");
+}
+
+fdl_status fdl_lm_head_verify(fdl_ctx* ctx, const void* mask_hidden, const void* w_lm, const fdl_unmask_args* a) {
+  if (!ctx) return FDL_ERR_INVALID_ARG;
+  if (!a || !mask_hidden || !w_lm) return fail(ctx, FDL_ERR_INVALID_ARG, "fdl_lm_head_verify: NULL argument");
+  if (a->logits || a->mask_logits)
+    return fail(ctx, FDL_ERR_INVALID_ARG, "fdl_lm_head_verify: logits and mask_logits must be NULL");
+  if (ctx->cfg.dtype != FDL_BF16)
+    return fail(ctx, FDL_ERR_UNSUPPORTED, "fdl_lm_head_verify: bf16 contexts only");
+  if (a->B < 1 || a->B > ctx->cfg.max_batch)
+    return fail(ctx, FDL_ERR_INVALID_ARG, "B=%d outside [1, max_batch=%d]", a->B, ctx->cfg.max_batch);
+  if (a->max_search < 1 || a->max_search > 1024)
+    return fail(ctx, FDL_ERR_INVALID_ARG, "max_search=%d outside [1, 1024]", a->max_search);
+  if ((long long)a->B * a->max_search > fdl_lm_head_max_rows())
+    return fail(ctx, FDL_ERR_UNSUPPORTED, "B*max_search=%lld above %d mask-view rows",
+                (long long)a->B * a->max_search, fdl_lm_head_max_rows());
+  if (!a->n_search || !a->draft_tok || !a->accept || !a->n_accept || !a->mask_conf || !a->mask_argmax)
+    return fail(ctx, FDL_ERR_INVALID_ARG, "fdl_lm_head_verify: NULL output or input argument");
+  if (!(a->gamma >= 0.f && a->gamma <= 1.f)) return fail(ctx, FDL_ERR_INVALID_ARG, "gamma outside [0,1]");
+  if (ctx->cfg.d_model % 64 != 0)
+    return fail(ctx, FDL_ERR_UNSUPPORTED, "fdl_lm_head_verify: d_model must be a multiple of 64");
+  return launched(ctx, fdl_launch_lm_head(ctx, mask_hidden, w_lm, a, true), "LM-head verify launch");
 }
 
 }  // extern "C"

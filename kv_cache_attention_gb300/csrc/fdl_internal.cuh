@@ -154,8 +154,11 @@ cudaError_t fdl_launch_topk(fdl_ctx* ctx, const float* scores, const unsigned ch
 
 cudaError_t fdl_launch_unmask_verify(fdl_ctx* ctx, const fdl_unmask_args* a);
 
-cudaError_t fdl_launch_lm_head_unmask(fdl_ctx* ctx, const void* hidden, const void* w_lm, const fdl_unmask_args* a);
-// Window rows the fused LM head takes in one call, and its workspace floats
+// The fused LM head: unmask decisions from the window rows' hidden states
+// (verify == false) or verify acceptance from the mask views' (verify == true).
+cudaError_t fdl_launch_lm_head(fdl_ctx* ctx, const void* hidden, const void* w_lm, const fdl_unmask_args* a,
+                               bool verify);
+// Rows the fused LM head takes in one call, and its workspace floats
 // (one set of per-row statistics per CTA of its persistent grid).
 int fdl_lm_head_max_rows();
 size_t fdl_lm_partial_floats(int num_sms);

@@ -622,8 +622,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   };
   if (threadIdx.x == 0)
     for (int it = 0; it < pre; ++it) issue(it, it);
-  // every CTA may be the last: it stages the decision inputs at its start
-  if ((int)threadIdx.x < R) {
+  // every CTA may be the last: it stages the unmask decisions' inputs at its start
+  if (p.rp.phase == 0 && (int)threadIdx.x < R) {
     pre_seq[threadIdx.x] = p.rp.row_seq[threadIdx.x];
     pre_pos[threadIdx.x] = p.rp.row_pos[threadIdx.x];
   }
@@ -759,13 +759,20 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     for (int off = 16; off; off >>= 1) acc = shfl_merge(acc, off);
     if (lane == 0) {
       const float conf = acc.s > 0.f ? 1.f / acc.s : 0.f;
-      p.rp.out_conf[c] = conf;
-      p.rp.out_arg[c] = acc.i;
+      // verify: row b*max_search + j holds a mask view only for j < n_search[b]
+      const bool real = p.rp.phase == 0 || c % p.rp.max_search < __ldg(p.rp.n_search + c / p.rp.max_search);
+      if (real) {
+        p.rp.out_conf[c] = conf;
+        p.rp.out_arg[c] = acc.i;
+      }
       pre_conf[c] = conf;
     }
   }
   __syncthreads();
-  decide_unmask<kLmBN, kLmBN>(p.rp, pre_seq, pre_pos, pre_conf);
+  if (p.rp.phase == 0)
+    decide_unmask<kLmBN, kLmBN>(p.rp, pre_seq, pre_pos, pre_conf);
+  else
+    decide_verify(p.rp);
   if (threadIdx.x == 0) *p.rp.ticket = 0u;  // ready for the next call
 }
 
@@ -854,9 +861,11 @@ int fdl_lm_head_max_rows() { return kLmBN; }
 
 size_t fdl_lm_partial_floats(int num_sms) { return (size_t)num_sms * kLmBN * 3; }
 
-cudaError_t fdl_launch_lm_head_unmask(fdl_ctx* ctx, const void* hidden, const void* w_lm, const fdl_unmask_args* a) {
+cudaError_t fdl_launch_lm_head(fdl_ctx* ctx, const void* hidden, const void* w_lm, const fdl_unmask_args* a,
+                               bool verify) {
   const fdl_config& c = ctx->cfg;
-  if (c.dtype != FDL_BF16 || a->R_w < 1 || a->R_w > kLmBN || c.d_model % kLmBK != 0 || !ctx->lm_part)
+  const int R = verify ? a->B * a->max_search : a->R_w;
+  if (c.dtype != FDL_BF16 || R < 1 || R > kLmBN || c.d_model % kLmBK != 0 || !ctx->lm_part)
     return cudaErrorNotSupported;
   if ((reinterpret_cast<uintptr_t>(hidden) | reinterpret_cast<uintptr_t>(w_lm)) & 15) return cudaErrorMisalignedAddress;
   static bool attr_set = false;
@@ -866,25 +875,36 @@ cudaError_t fdl_launch_lm_head_unmask(fdl_ctx* ctx, const void* hidden, const vo
     attr_set = true;
   }
   CUtensorMap mw, mh;
-  if (!lm_map(&mw, w_lm, (uint64_t)c.vocab, c.d_model, kLmBM) || !lm_map(&mh, hidden, a->R_w, c.d_model, kLmBN))
+  if (!lm_map(&mw, w_lm, (uint64_t)c.vocab, c.d_model, kLmBM) || !lm_map(&mh, hidden, R, c.d_model, kLmBN))
     return cudaErrorInvalidValue;
   LmParams p = {};
-  p.rp.n_rows = a->R_w;
-  p.rp.out_conf = a->conf;
-  p.rp.out_arg = a->argmax;
+  p.rp.n_rows = R;
   p.rp.part = ctx->lm_part;
   p.rp.ticket = ctx->tickets + 2;
   p.rp.err = ctx->err_word;
-  p.rp.phase = 0;
   p.rp.B = a->B;
-  p.rp.row_seq = a->row_seq;
-  p.rp.row_pos = a->row_pos;
-  p.rp.eps = a->eps;
-  p.rp.force_progress = a->force_progress;
-  p.rp.commit = a->commit;
-  p.rp.search_rows = a->search_rows;
-  p.rp.n_search_out = a->n_search;
   p.rp.max_search = a->max_search;
+  if (!verify) {
+    p.rp.phase = 0;
+    p.rp.out_conf = a->conf;
+    p.rp.out_arg = a->argmax;
+    p.rp.row_seq = a->row_seq;
+    p.rp.row_pos = a->row_pos;
+    p.rp.eps = a->eps;
+    p.rp.force_progress = a->force_progress;
+    p.rp.commit = a->commit;
+    p.rp.search_rows = a->search_rows;
+    p.rp.n_search_out = a->n_search;
+  } else {
+    p.rp.phase = 1;
+    p.rp.out_conf = a->mask_conf;
+    p.rp.out_arg = a->mask_argmax;
+    p.rp.n_search = a->n_search;
+    p.rp.draft_tok = a->draft_tok;
+    p.rp.gamma = a->gamma;
+    p.rp.accept = a->accept;
+    p.rp.n_accept = a->n_accept;
+  }
   p.vocab = c.vocab;
   p.nkb = c.d_model / kLmBK;
   p.n_tiles = (c.vocab + kLmBM - 1) / kLmBM;

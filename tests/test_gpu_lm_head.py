@@ -132,3 +132,88 @@ def test_lm_head_unmask_limits():
     assert got[1].tolist() == [0] * 64
     assert got[4].tolist() == [8] and got[3][0].tolist() == list(range(8))
     ctx.close()
+
+
+def _verify_rule(mask_conf, mask_arg, draft, n_search, gamma, B, ms):
+    """The verify rule on given (c~, x~): float32 confidences compared as
+    float64 against float32(gamma), the comparison the kernel makes."""
+    accept = np.zeros(B * ms, np.uint8)
+    n_accept = np.zeros(B, np.int64)
+    g = np.float64(np.float32(gamma))
+    for b in range(B):
+        for j in range(int(n_search[b])):
+            r = b * ms + j
+            if int(draft[r]) != int(mask_arg[r]) or np.float64(mask_conf[r]) < g:
+                break
+            accept[r] = 1
+            n_accept[b] += 1
+    return accept, n_accept
+
+
+def test_lm_head_verify_ragged_vocab():
+    torch = H.torch_mod()
+    d, V, B, ms, gamma = 4096, 16384 + 77, 3, 5, 0.8
+    R = B * ms
+    hidden, w, _ = synth.lm_head_case(seed=1012, vocab=V, d=d, rows=R, planted=1.0)
+    c0, _ = oracle.row_confidence(oracle.lm_head_logits(hidden.values(), w.values()))
+    # the most confident mask views first, so sequence 0's walk runs several tokens
+    hidden = synth.make_tensor(hidden.values()[np.argsort(-c0, kind="stable")], "bf16")
+    logits = oracle.lm_head_logits(hidden.values(), w.values())
+    n_search = np.array([5, 2, 0], np.int32)
+    _, a_o = oracle.row_confidence(logits)
+    draft = a_o.astype(np.int32).copy()                 # drafts agree with the mask views' argmax,
+    draft[3] = (draft[3] + 1) % V                       # except one inside sequence 0's walk
+    want = oracle.verify(logits, draft, n_search, gamma, B, ms)
+    ctx = _ctx(d, V, B, R)
+    mc = torch.full((R,), -5.0, dtype=torch.float32, device="cuda")
+    ma = torch.full((R,), -5, dtype=torch.int32, device="cuda")
+    acc = torch.full((R,), 7, dtype=torch.uint8, device="cuda")
+    nacc = torch.full((B,), -1, dtype=torch.int32, device="cuda")
+    ctx.lm_head_verify(H.dev(hidden), H.dev(w), B, ms, n_search=H.ints(n_search), draft_tok=H.ints(draft),
+                       gamma=gamma, accept=acc, n_accept=nacc, mask_conf=mc, mask_argmax=ma)
+    ctx.sync_status()
+    mc, ma, acc, nacc = H.host(mc), H.host(ma), H.host(acc), H.host(nacc)
+    valid = np.array([b * ms + j for b in range(B) for j in range(n_search[b])])
+    rest = np.setdiff1d(np.arange(R), valid)
+    assert (mc[rest] == -5.0).all() and (ma[rest] == -5).all()      # views past n_search are not written
+    np.testing.assert_allclose(mc[valid], want["mask_conf"][valid], atol=H.F32_TOL, rtol=0)
+    top2 = np.sort(logits[valid], axis=1)[:, -2:]
+    clear = (top2[:, 1] - top2[:, 0]) > 1e-3
+    assert np.array_equal(ma[valid][clear], want["mask_argmax"][valid][clear])
+    # the decisions are exactly the rule applied to the kernel's own values ...
+    rule_acc, rule_n = _verify_rule(mc, ma, draft, n_search, gamma, B, ms)
+    assert acc.tolist() == rule_acc.tolist() and nacc.tolist() == rule_n.tolist()
+    # ... and the oracle's wherever no walked confidence sits within 1e-3 of gamma
+    for b in range(B):
+        rows = valid[valid // ms == b]
+        if not (np.abs(want["mask_conf"][rows] - gamma) < 1e-3).any():
+            assert nacc[b] == want["n_accept"][b]
+            assert acc[b * ms:(b + 1) * ms].tolist() == want["accept"][b * ms:(b + 1) * ms].tolist()
+    assert nacc[0] == 3 and nacc[2] == 0
+    ctx.close()
+
+
+def test_lm_head_verify_limits():
+    import kv_cache_attention_gb300 as fdl
+    torch = H.torch_mod()
+    d, V = 4096, 1024
+    ctx = _ctx(d, V, 16, 64)
+    w = torch.zeros((V, d), dtype=torch.bfloat16, device="cuda")
+    h = torch.zeros((80, d), dtype=torch.bfloat16, device="cuda")
+    z = torch.zeros(80, dtype=torch.int32, device="cuda")
+    f = torch.zeros(80, dtype=torch.float32, device="cuda")
+    u = torch.zeros(80, dtype=torch.uint8, device="cuda")
+    for B, ms, status in ((13, 5, fdl.FDL_ERR_UNSUPPORTED), (1, 0, fdl.FDL_ERR_INVALID_ARG)):
+        with pytest.raises(fdl.FdlError) as ei:
+            ctx.lm_head_verify(h, w, B, ms, n_search=z, draft_tok=z, gamma=0.8, accept=u, n_accept=z,
+                               mask_conf=f, mask_argmax=z)
+        assert ei.value.status == status
+    # 64 mask views of zero logits: c~ = 1/V < gamma, so nothing is accepted
+    ns = torch.full((16,), 4, dtype=torch.int32, device="cuda")
+    nacc = torch.full((16,), -1, dtype=torch.int32, device="cuda")
+    ctx.lm_head_verify(h[:64], w, 16, 4, n_search=ns, draft_tok=z[:64], gamma=0.8, accept=u[:64], n_accept=nacc,
+                       mask_conf=f[:64], mask_argmax=z[:64])
+    ctx.sync_status()
+    assert (H.host(nacc) == 0).all() and (H.host(u[:64]) == 0).all()
+    np.testing.assert_allclose(H.host(f[:64]), 1.0 / V, rtol=1e-6)
+    ctx.close()
