@@ -502,6 +502,45 @@ def trace_unmask(rng: np.random.Generator, decoded_pos, lo: int = 1, hi: int = 4
 
 
 # --------------------------------------------------------------------------
+# A whole masked-diffusion transformer with random weights
+# --------------------------------------------------------------------------
+def model_case(seed: int = 1013, d: int = 512, n_heads: int = 4, n_layers: int = 2, ffn: int = 1024,
+               vocab: int = 2048 + 40, theta: float = 1.0e4, dtype: str = "bf16") -> dict:
+    """LLaMA-style weights (no biases), bf16: embedding ~ N(0, 1); W_qkv, W_o,
+    W_gate/W_up (stacked: gate rows, then up rows) and W_down ~ N(0, 0.02^2);
+    RMSNorm gains 1 + U(-0.2, 0.2); LM head ~ N(0, 0.02^2). The last
+    vocabulary id is the [MASK] token. Returns a dict of Tensors and sizes."""
+    rng = np.random.default_rng(seed)
+    hd = d // n_heads
+
+    def gain():
+        return make_tensor(1.0 + rng.uniform(-0.2, 0.2, size=d), dtype)
+
+    layers = []
+    for _ in range(n_layers):
+        layers.append(dict(g_attn=gain(), w_qkv=make_tensor(normal(rng, (3 * d, d), 0.02), dtype),
+                           w_o=make_tensor(normal(rng, (d, d), 0.02), dtype), g_mlp=gain(),
+                           w_gu=make_tensor(normal(rng, (2 * ffn, d), 0.02), dtype),
+                           w_down=make_tensor(normal(rng, (d, ffn), 0.02), dtype)))
+    return dict(n_heads=n_heads, head_dim=hd, d_model=d, ffn=ffn, vocab=vocab, theta=theta, eps=1e-5,
+                mask_id=vocab - 1, embed=make_tensor(normal(rng, (vocab, d)), dtype), layers=layers,
+                g_final=gain(), w_lm=make_tensor(normal(rng, (vocab, d), 0.02), dtype))
+
+
+def model_values(m: dict) -> dict:
+    """The same dict with every Tensor replaced by its float64 values."""
+    out = {}
+    for k, v in m.items():
+        if isinstance(v, Tensor):
+            out[k] = v.values()
+        elif k == "layers":
+            out[k] = [{kk: vv.values() for kk, vv in layer.items()} for layer in v]
+        else:
+            out[k] = v
+    return out
+
+
+# --------------------------------------------------------------------------
 # Language-model head (the step after the path: hidden states -> decisions)
 # --------------------------------------------------------------------------
 def lm_head_case(seed: int = 1006, vocab: int = 126464, d: int = 4096, rows: int = 32,
