@@ -19,6 +19,10 @@
  *                             stored)
  *   fdl_lm_head_verify        the verify acceptance straight from the mask
  *                             views' hidden states (LM head fused)
+ *   fdl_model_forward         the whole transformer forward over a step's
+ *                             refresh rows (embedding, every layer's norm,
+ *                             projection, attention, W_o and SwiGLU FFN, the
+ *                             final norm)
  *   fdl_refresh_rows          (host) the query rows of a step under a KV-cache
  *                             refresh policy: Fast-dLLM PrefixCache and
  *                             DualCache, FlashDLM FreeCache, the Flash-dLLM
@@ -44,6 +48,8 @@
  */
 #ifndef FDL_H_
 #define FDL_H_
+
+#include <stddef.h>
 
 #ifdef __cplusplus
 extern "C" {
@@ -307,6 +313,59 @@ fdl_status fdl_sched_attn_noalloc(const fdl_config* cfg, void* cuda_stream, cons
                                   const int* row_kind, const int* search_pos, int search_ld,
                                   const int* n_search, void* o_out, float* lse_out, float* track_scores,
                                   int track_ld, unsigned* device_error);
+
+/* ------------------------------------------------------------------------
+ * Whole-model forward over one step's refresh rows (the dLLM the path sits
+ * in: paper digest, "Background", a bidirectional transformer such as LLaDA;
+ * "Method steps in detail", Algorithm 2 step 2, each step's query rows go
+ * through every layer against the full cache). The pages are silent on the
+ * block's internals; it is LLaMA-style (LLaDA's), with no biases:
+ *   h = embed[tokens[r]]                                  (fp32)
+ *   per layer l:
+ *     a  = RMSNorm(h) * g_attn[l]                         (bf16)
+ *     fdl_qkv_rope_cache_write(a, w_qkv[l], ...) into k_caches[l], v_caches[l]
+ *     o  = fdl_sched_attn(...)  (with track_scores: Eq. (2) summed over layers)
+ *     h += o . w_o[l]^T
+ *     m  = RMSNorm(h) * g_mlp[l]                          (bf16)
+ *     h += (SiLU(m . W_gate^T) * (m . W_up^T)) . w_down[l]^T
+ *   final_out = RMSNorm(h) * g_final                      (bf16 [R, d_model])
+ * with RMSNorm(x) = x / sqrt(mean(x^2) + rms_eps). The rows, cu_seqlens,
+ * kv_len, block table, views and tracker arguments are those of
+ * fdl_qkv_rope_cache_write and fdl_sched_attn (same meaning, same checks);
+ * tokens [R] are the rows' input token ids (the [MASK] id for a masked
+ * position). k_caches / v_caches are HOST arrays of n_layers DEVICE pointers,
+ * one cache pair per layer. workspace is caller-owned device memory of at
+ * least fdl_model_workspace_bytes(ctx, ffn, R) bytes, 256-byte aligned
+ * (the fp32 residual stream and the bf16 intermediates).
+ *
+ * bf16 contexts only, d_model a multiple of 128, ffn a multiple of 64:
+ * otherwise FDL_ERR_UNSUPPORTED. A token id outside [0, vocab) gives a zero
+ * input row and sets the device error word (FDL_ERR_DEVICE_INDEX).
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  int n_layers;
+  int ffn;                    /* SwiGLU hidden size F                              */
+  float rms_eps;
+  const void* embed;          /* [vocab, d_model] bf16                             */
+  const void* const* g_attn;  /* host array [n_layers] of [d_model] bf16 gains     */
+  const void* const* w_qkv;   /* host array [n_layers] of [3 d_model, d_model] bf16 */
+  const void* const* w_o;     /* host array [n_layers] of [d_model, d_model] bf16   */
+  const void* const* g_mlp;   /* host array [n_layers] of [d_model] bf16 gains     */
+  const void* const* w_gu;    /* host array [n_layers] of [2 ffn, d_model] bf16:
+                                 the gate rows, then the up rows                   */
+  const void* const* w_down;  /* host array [n_layers] of [d_model, ffn] bf16      */
+  const void* g_final;        /* [d_model] bf16                                    */
+} fdl_model;
+
+size_t fdl_model_workspace_bytes(const fdl_ctx* ctx, int ffn, int R);
+
+fdl_status fdl_model_forward(fdl_ctx* ctx, const fdl_model* model, const int* tokens, int R,
+                             const int* row_seq, const int* row_rope_pos, const int* row_cache_pos,
+                             const int* row_kind, const int* cu_seqlens_q, const int* kv_len, int B,
+                             const int* block_table, int bt_stride, void* const* k_caches,
+                             void* const* v_caches, const int* search_pos, int search_ld,
+                             const int* n_search, float* track_scores, int track_ld, void* workspace,
+                             size_t workspace_bytes, void* final_out);
 
 /* ------------------------------------------------------------------------
  * Row descriptors of one step under a KV-cache refresh policy (HOST code:

@@ -43,7 +43,8 @@ EXPORTS = (
     "fdl_create", "fdl_destroy", "fdl_set_stream", "fdl_last_error", "fdl_sync_status",
     "fdl_tile_m", "fdl_worklist_capacity", "fdl_qkv_rope_cache_write", "fdl_sched_attn",
     "fdl_track_topk", "fdl_unmask_verify", "fdl_sched_attn_noalloc", "fdl_lm_head_unmask",
-    "fdl_refresh_rows", "fdl_verify_rows", "fdl_lm_head_verify",
+    "fdl_refresh_rows", "fdl_verify_rows", "fdl_lm_head_verify", "fdl_model_workspace_bytes",
+    "fdl_model_forward",
 )
 
 FDL_REFRESH_FULL = 0
@@ -79,6 +80,17 @@ class fdl_unmask_args(ctypes.Structure):
         ("conf", _P), ("argmax", _P), ("commit", _P), ("search_rows", _P), ("n_search", _P),
         ("mask_logits", _P), ("draft_tok", _P), ("gamma", ctypes.c_float),
         ("accept", _P), ("n_accept", _P), ("mask_conf", _P), ("mask_argmax", _P),
+    ]
+
+
+_PP = ctypes.POINTER(ctypes.c_void_p)
+
+
+class fdl_model(ctypes.Structure):
+    _fields_ = [
+        ("n_layers", ctypes.c_int), ("ffn", ctypes.c_int), ("rms_eps", ctypes.c_float), ("embed", _P),
+        ("g_attn", _PP), ("w_qkv", _PP), ("w_o", _PP), ("g_mlp", _PP), ("w_gu", _PP), ("w_down", _PP),
+        ("g_final", _P),
     ]
 
 
@@ -133,6 +145,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.fdl_sched_attn_noalloc.argtypes = [ctypes.POINTER(fdl_config), p, p, p, p, p, i, p, p, i, i, p, p, i, p, p,
                                          p, p, i, p]
     L.fdl_sched_attn_noalloc.restype = i
+    L.fdl_model_workspace_bytes.argtypes = [p, i, i]
+    L.fdl_model_workspace_bytes.restype = ctypes.c_size_t
+    L.fdl_model_forward.argtypes = [p, ctypes.POINTER(fdl_model), p, i, p, p, p, p, p, p, i, p, i, _PP, _PP, p, i, p,
+                                    p, i, p, ctypes.c_size_t, p]
+    L.fdl_model_forward.restype = i
     L.fdl_refresh_rows.argtypes = [ctypes.POINTER(fdl_refresh_args)]
     L.fdl_refresh_rows.restype = i
     L.fdl_verify_rows.argtypes = [i, p, p, i, p, p, i, p, i, i, p, p, p, p, p, p]
@@ -246,6 +263,41 @@ class Context:
         self._check(load_library().fdl_lm_head_unmask(self.handle, _ptr(hidden), _ptr(w_lm), ctypes.byref(a)),
                     "fdl_lm_head_unmask")
 
+    def model_workspace_bytes(self, ffn: int, R: int) -> int:
+        return int(load_library().fdl_model_workspace_bytes(self.handle, int(ffn), int(R)))
+
+    def model_forward(self, model: dict, tokens, row_seq, row_rope_pos, row_cache_pos, row_kind, cu_seqlens_q,
+                      kv_len, block_table, k_caches, v_caches, workspace, final_out, search_pos=None,
+                      n_search=None, track_scores=None) -> None:
+        """Whole-model forward over the rows. ``model``: dict with ffn, eps,
+        embed, g_final and layers (dicts with g_attn, w_qkv, w_o, g_mlp, w_gu,
+        w_down), all bf16 device tensors; k_caches / v_caches: one tensor per
+        layer; workspace: a uint8 device tensor of model_workspace_bytes."""
+        layers = model["layers"]
+        n = len(layers)
+
+        def arr(ts):
+            return (ctypes.c_void_p * n)(*[_ptr(t) for t in ts])
+
+        keep = {k: arr([w[k] for w in layers]) for k in ("g_attn", "w_qkv", "w_o", "g_mlp", "w_gu", "w_down")}
+        kc, vc = arr(k_caches), arr(v_caches)
+        m = fdl_model()
+        m.n_layers, m.ffn, m.rms_eps = n, int(model["ffn"]), float(model["eps"])
+        m.embed, m.g_final = _ptr(model["embed"]), _ptr(model["g_final"])
+        for k, a in keep.items():
+            setattr(m, k, ctypes.cast(a, _PP))
+        B = int(kv_len.shape[0])
+        R = int(tokens.shape[0])
+        search_ld = int(search_pos.shape[-1]) if search_pos is not None else 0
+        track_ld = int(track_scores.shape[-1]) if track_scores is not None else 0
+        st = load_library().fdl_model_forward(
+            self.handle, ctypes.byref(m), _ptr(tokens), R, _ptr(row_seq), _ptr(row_rope_pos), _ptr(row_cache_pos),
+            _ptr(row_kind), _ptr(cu_seqlens_q), _ptr(kv_len), B, _ptr(block_table), int(block_table.shape[-1]),
+            ctypes.cast(kc, _PP), ctypes.cast(vc, _PP), _ptr(search_pos), search_ld, _ptr(n_search),
+            _ptr(track_scores), track_ld, _ptr(workspace), int(workspace.numel() * workspace.element_size()),
+            _ptr(final_out))
+        self._check(st, "fdl_model_forward")
+
     def lm_head_verify(self, mask_hidden, w_lm, B: int, max_search: int, *, n_search, draft_tok,
                        gamma: float = 0.8, accept, n_accept, mask_conf, mask_argmax) -> None:
         """Verify acceptance straight from the mask views' hidden states
@@ -311,6 +363,14 @@ def fdl_lm_head_unmask(ctx: Context, *a, **k) -> None:
 
 def fdl_lm_head_verify(ctx: Context, *a, **k) -> None:
     ctx.lm_head_verify(*a, **k)
+
+
+def fdl_model_workspace_bytes(ctx: Context, ffn: int, R: int) -> int:
+    return ctx.model_workspace_bytes(ffn, R)
+
+
+def fdl_model_forward(ctx: Context, *a, **k) -> None:
+    ctx.model_forward(*a, **k)
 
 
 def fdl_sched_attn_noalloc(cfg: fdl_config, q, k_cache, v_cache, block_table, cu_seqlens_q, kv_len, row_kind,
