@@ -505,11 +505,14 @@ def trace_unmask(rng: np.random.Generator, decoded_pos, lo: int = 1, hi: int = 4
 # A whole masked-diffusion transformer with random weights
 # --------------------------------------------------------------------------
 def model_case(seed: int = 1013, d: int = 512, n_heads: int = 4, n_layers: int = 2, ffn: int = 1024,
-               vocab: int = 2048 + 40, theta: float = 1.0e4, dtype: str = "bf16") -> dict:
-    """LLaMA-style weights (no biases), bf16: embedding ~ N(0, 1); W_qkv, W_o,
-    W_gate/W_up (stacked: gate rows, then up rows) and W_down ~ N(0, 0.02^2);
-    RMSNorm gains 1 + U(-0.2, 0.2); LM head ~ N(0, 0.02^2). The last
-    vocabulary id is the [MASK] token. Returns a dict of Tensors and sizes."""
+               vocab: int = 2048 + 40, theta: float = 1.0e4, dtype: str = "bf16", out_std: float = 0.02,
+               lm_std: float = 0.02) -> dict:
+    """LLaMA-style weights (no biases), bf16: embedding ~ N(0, 1); W_qkv and
+    W_gate/W_up (stacked: gate rows, then up rows) ~ N(0, 0.02^2); W_o and
+    W_down ~ N(0, out_std^2) (larger values let attention and the FFN move
+    the residual stream further from the embeddings); RMSNorm gains
+    1 + U(-0.2, 0.2); LM head ~ N(0, lm_std^2). The last vocabulary id is the
+    [MASK] token. Returns a dict of Tensors and sizes."""
     rng = np.random.default_rng(seed)
     hd = d // n_heads
 
@@ -519,12 +522,12 @@ def model_case(seed: int = 1013, d: int = 512, n_heads: int = 4, n_layers: int =
     layers = []
     for _ in range(n_layers):
         layers.append(dict(g_attn=gain(), w_qkv=make_tensor(normal(rng, (3 * d, d), 0.02), dtype),
-                           w_o=make_tensor(normal(rng, (d, d), 0.02), dtype), g_mlp=gain(),
+                           w_o=make_tensor(normal(rng, (d, d), out_std), dtype), g_mlp=gain(),
                            w_gu=make_tensor(normal(rng, (2 * ffn, d), 0.02), dtype),
-                           w_down=make_tensor(normal(rng, (d, ffn), 0.02), dtype)))
+                           w_down=make_tensor(normal(rng, (d, ffn), out_std), dtype)))
     return dict(n_heads=n_heads, head_dim=hd, d_model=d, ffn=ffn, vocab=vocab, theta=theta, eps=1e-5,
                 mask_id=vocab - 1, embed=make_tensor(normal(rng, (vocab, d)), dtype), layers=layers,
-                g_final=gain(), w_lm=make_tensor(normal(rng, (vocab, d), 0.02), dtype))
+                g_final=gain(), w_lm=make_tensor(normal(rng, (vocab, d), lm_std), dtype))
 
 
 def model_values(m: dict) -> dict:
