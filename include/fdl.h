@@ -23,6 +23,9 @@
  *                             refresh rows (embedding, every layer's norm,
  *                             projection, attention, W_o and SwiGLU FFN, the
  *                             final norm)
+ *   fdl_flash_step            one Flash-dLLM denoising step of a whole model
+ *                             (draft forward, unmasking, verify forward,
+ *                             acceptance, next tracked set)
  *   fdl_refresh_rows          (host) the query rows of a step under a KV-cache
  *                             refresh policy: Fast-dLLM PrefixCache and
  *                             DualCache, FlashDLM FreeCache, the Flash-dLLM
@@ -471,6 +474,82 @@ fdl_status fdl_verify_rows(int B, const int* seq_len, const int* tracked, int tr
                            const int* n_search, int query_budget, int max_rows, int* row_seq,
                            int* row_rope_pos, int* row_cache_pos, int* row_kind, int* cu_seqlens,
                            int* n_rows);
+
+/* ------------------------------------------------------------------------
+ * One Flash-dLLM denoising step of a whole model on a batch of sequences
+ * (paper digest, "Method steps in detail", Algorithm 2 steps 2-4):
+ *   1. draft forward (fdl_model_forward with the tracker) over the rows
+ *      fdl_refresh_rows gives for FDL_REFRESH_FLASH_DRAFT: the tracked set
+ *      and the window of the first `window` masked positions; at a
+ *      sequence's first step (state -1) every position, which fills the
+ *      caches (Algorithm 2 step 1);
+ *   2. fdl_lm_head_unmask on the window rows: c >= eps is decoded, the
+ *      uncommitted rows, most confident first, form the search list;
+ *   3. if any sequence has search tokens, the verify forward over the rows
+ *      of fdl_verify_rows (query budget track_budget + window; draft views
+ *      hold their draft tokens, mask views mask_token), then
+ *      fdl_lm_head_verify on the mask views: the accepted prefix is decoded;
+ *   4. the committed, then the accepted tokens (each in position order) are
+ *      written into tokens / masked; the next tracked set is those newly
+ *      decoded positions, then the top (track_budget - their number) of the
+ *      other decoded positions (prompt included) by the draft forward's
+ *      tracker scores (fdl_track_topk), at most track_budget in all.
+ * The sequences' state is HOST memory and is updated in place; the caches
+ * (host array of per-layer device pointers, as in fdl_model_forward) and the
+ * device block table must hold seq_len + 2*max_search slots per sequence
+ * (the view keys). The call synchronises the context's stream (it reads the
+ * decisions back three times). workspace: device memory of at least
+ * fdl_flash_workspace_bytes bytes, 256-byte aligned. Limits: B*window and
+ * B*max_search <= 64 (the fused LM head), 2*max_search <= config.max_views,
+ * the first step's rows (every position of every sequence) <= max_rows.
+ * A step on sequences with nothing left masked returns FDL_OK and does
+ * nothing.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  int window;         /* beta_m: masked-window rows per sequence          */
+  int track_budget;   /* beta_t: tracked rows per sequence                 */
+  int max_search;     /* search tokens per sequence (0: no verify forward) */
+  float eps;          /* unmask threshold                                  */
+  float gamma;        /* acceptance threshold                              */
+  int force_progress; /* commit the most confident row when none reaches eps */
+  int mask_token;     /* the [MASK] id                                     */
+} fdl_flash_params;
+
+typedef struct {
+  int B;
+  int max_seq;                 /* row stride of tokens / masked (and of the tracker) */
+  const int* prompt_len;       /* host [B]                                           */
+  const int* seq_len;          /* host [B] N_b <= max_seq                            */
+  int* tokens;                 /* host [B*max_seq] in/out: current token ids         */
+  unsigned char* masked;       /* host [B*max_seq] in/out: 1 = still masked          */
+  int* tracked;                /* host [B*track_budget] in/out: tracked positions     */
+  int* n_tracked;              /* host [B] in/out                                     */
+  int* state;                  /* host [B] in/out: -1 before the first step           */
+} fdl_flash_seqs;
+
+typedef struct {               /* optional record of one step; host pointers, any may be NULL */
+  int* n_rows;                 /* [2]: draft-forward rows, verify-forward rows (0 when none) */
+  int* n_window;               /* [1]: window rows R_w                               */
+  int* window_seq;             /* [B*window]: each window row's sequence             */
+  int* window_pos;             /* [B*window]: and position                           */
+  float* conf;                 /* [B*window]: confidence of each window row          */
+  int* argmax;                 /* [B*window]: its prediction (the draft token)       */
+  unsigned char* commit;       /* [B*window]                                         */
+  int* search_rows;            /* [B*max_search]: window-row indices, -1 pad          */
+  int* n_search;               /* [B]                                                */
+  float* mask_conf;            /* [B*max_search]: the mask views' confidence          */
+  int* mask_argmax;            /* [B*max_search]: and prediction                      */
+  int* n_accept;               /* [B]                                                */
+  float* track;                /* [B*max_seq]: the draft forward's tracker scores     */
+} fdl_flash_trace;
+
+size_t fdl_flash_workspace_bytes(const fdl_ctx* ctx, int ffn, const fdl_flash_params* params, int B,
+                                 int max_seq);
+
+fdl_status fdl_flash_step(fdl_ctx* ctx, const fdl_model* model, const void* w_lm, void* const* k_caches,
+                          void* const* v_caches, const int* block_table, int bt_stride,
+                          const fdl_flash_params* params, fdl_flash_seqs* seqs, fdl_flash_trace* trace,
+                          void* workspace, size_t workspace_bytes);
 
 #ifdef __cplusplus
 }

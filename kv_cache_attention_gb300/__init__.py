@@ -44,7 +44,7 @@ EXPORTS = (
     "fdl_tile_m", "fdl_worklist_capacity", "fdl_qkv_rope_cache_write", "fdl_sched_attn",
     "fdl_track_topk", "fdl_unmask_verify", "fdl_sched_attn_noalloc", "fdl_lm_head_unmask",
     "fdl_refresh_rows", "fdl_verify_rows", "fdl_lm_head_verify", "fdl_model_workspace_bytes",
-    "fdl_model_forward",
+    "fdl_model_forward", "fdl_flash_workspace_bytes", "fdl_flash_step",
 )
 
 FDL_REFRESH_FULL = 0
@@ -92,6 +92,26 @@ class fdl_model(ctypes.Structure):
         ("g_attn", _PP), ("w_qkv", _PP), ("w_o", _PP), ("g_mlp", _PP), ("w_gu", _PP), ("w_down", _PP),
         ("g_final", _P),
     ]
+
+
+class fdl_flash_params(ctypes.Structure):
+    _fields_ = [
+        ("window", ctypes.c_int), ("track_budget", ctypes.c_int), ("max_search", ctypes.c_int),
+        ("eps", ctypes.c_float), ("gamma", ctypes.c_float), ("force_progress", ctypes.c_int),
+        ("mask_token", ctypes.c_int),
+    ]
+
+
+class fdl_flash_seqs(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int), ("max_seq", ctypes.c_int), ("prompt_len", _P), ("seq_len", _P), ("tokens", _P),
+        ("masked", _P), ("tracked", _P), ("n_tracked", _P), ("state", _P),
+    ]
+
+
+class fdl_flash_trace(ctypes.Structure):
+    _fields_ = [(n, _P) for n in ("n_rows", "n_window", "window_seq", "window_pos", "conf", "argmax", "commit",
+                                  "search_rows", "n_search", "mask_conf", "mask_argmax", "n_accept", "track")]
 
 
 class fdl_refresh_args(ctypes.Structure):
@@ -150,6 +170,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.fdl_model_forward.argtypes = [p, ctypes.POINTER(fdl_model), p, i, p, p, p, p, p, p, i, p, i, _PP, _PP, p, i, p,
                                     p, i, p, ctypes.c_size_t, p]
     L.fdl_model_forward.restype = i
+    L.fdl_flash_workspace_bytes.argtypes = [p, i, ctypes.POINTER(fdl_flash_params), i, i]
+    L.fdl_flash_workspace_bytes.restype = ctypes.c_size_t
+    L.fdl_flash_step.argtypes = [p, ctypes.POINTER(fdl_model), p, _PP, _PP, p, i, ctypes.POINTER(fdl_flash_params),
+                                 ctypes.POINTER(fdl_flash_seqs), ctypes.POINTER(fdl_flash_trace), p, ctypes.c_size_t]
+    L.fdl_flash_step.restype = i
     L.fdl_refresh_rows.argtypes = [ctypes.POINTER(fdl_refresh_args)]
     L.fdl_refresh_rows.restype = i
     L.fdl_verify_rows.argtypes = [i, p, p, i, p, p, i, p, i, i, p, p, p, p, p, p]
@@ -266,6 +291,47 @@ class Context:
     def model_workspace_bytes(self, ffn: int, R: int) -> int:
         return int(load_library().fdl_model_workspace_bytes(self.handle, int(ffn), int(R)))
 
+    def flash_workspace_bytes(self, ffn: int, params: dict, B: int, max_seq: int) -> int:
+        return int(load_library().fdl_flash_workspace_bytes(self.handle, int(ffn), ctypes.byref(_flash_params(params)),
+                                                            int(B), int(max_seq)))
+
+    def flash_step(self, model: dict, w_lm, k_caches, v_caches, block_table, params: dict, seqs: dict, workspace,
+                   trace: bool = True):
+        """One denoising step (see include/fdl.h). ``seqs``: dict of host numpy
+        arrays prompt_len, seq_len (int32 [B]), tokens (int32 [B, max_seq]),
+        masked (uint8 [B, max_seq]), tracked (int32 [B, track_budget]),
+        n_tracked and state (int32 [B]); the last five are updated in place.
+        Returns the step's record as a dict of numpy arrays (or None)."""
+        import numpy as np
+        m, keep = _model_struct(model)
+        kc, vc = _ptr_array(k_caches), _ptr_array(v_caches)
+        pr = _flash_params(params)
+        B, N = int(seqs["tokens"].shape[0]), int(seqs["tokens"].shape[1])
+        sq = fdl_flash_seqs()
+        sq.B, sq.max_seq = B, N
+        for name, dt in (("prompt_len", np.int32), ("seq_len", np.int32), ("tokens", np.int32), ("masked", np.uint8),
+                         ("tracked", np.int32), ("n_tracked", np.int32), ("state", np.int32)):
+            _, ptr = _host(seqs[name], dt, name, writable=True)
+            setattr(sq, name, ptr)
+        rec, tr = None, None
+        if trace:
+            W, MS = int(params["window"]), max(1, int(params["max_search"]))
+            rec = dict(n_rows=np.zeros(2, np.int32), n_window=np.zeros(1, np.int32),
+                       window_seq=np.zeros(B * W, np.int32), window_pos=np.zeros(B * W, np.int32),
+                       conf=np.zeros(B * W, np.float32), argmax=np.zeros(B * W, np.int32),
+                       commit=np.zeros(B * W, np.uint8), search_rows=np.full(B * MS, -1, np.int32),
+                       n_search=np.zeros(B, np.int32), mask_conf=np.zeros(B * MS, np.float32),
+                       mask_argmax=np.zeros(B * MS, np.int32), n_accept=np.zeros(B, np.int32),
+                       track=np.zeros(B * N, np.float32))
+            tr = fdl_flash_trace(**{k: v.ctypes.data for k, v in rec.items()})
+        st = load_library().fdl_flash_step(
+            self.handle, ctypes.byref(m), _ptr(w_lm), kc, vc, _ptr(block_table), int(block_table.shape[-1]),
+            ctypes.byref(pr), ctypes.byref(sq), ctypes.byref(tr) if tr is not None else None, _ptr(workspace),
+            int(workspace.numel() * workspace.element_size()))
+        del keep
+        self._check(st, "fdl_flash_step")
+        return rec
+
     def model_forward(self, model: dict, tokens, row_seq, row_rope_pos, row_cache_pos, row_kind, cu_seqlens_q,
                       kv_len, block_table, k_caches, v_caches, workspace, final_out, search_pos=None,
                       n_search=None, track_scores=None) -> None:
@@ -273,19 +339,8 @@ class Context:
         embed, g_final and layers (dicts with g_attn, w_qkv, w_o, g_mlp, w_gu,
         w_down), all bf16 device tensors; k_caches / v_caches: one tensor per
         layer; workspace: a uint8 device tensor of model_workspace_bytes."""
-        layers = model["layers"]
-        n = len(layers)
-
-        def arr(ts):
-            return (ctypes.c_void_p * n)(*[_ptr(t) for t in ts])
-
-        keep = {k: arr([w[k] for w in layers]) for k in ("g_attn", "w_qkv", "w_o", "g_mlp", "w_gu", "w_down")}
-        kc, vc = arr(k_caches), arr(v_caches)
-        m = fdl_model()
-        m.n_layers, m.ffn, m.rms_eps = n, int(model["ffn"]), float(model["eps"])
-        m.embed, m.g_final = _ptr(model["embed"]), _ptr(model["g_final"])
-        for k, a in keep.items():
-            setattr(m, k, ctypes.cast(a, _PP))
+        m, keep = _model_struct(model)
+        kc, vc = _ptr_array(k_caches), _ptr_array(v_caches)
         B = int(kv_len.shape[0])
         R = int(tokens.shape[0])
         search_ld = int(search_pos.shape[-1]) if search_pos is not None else 0
@@ -293,7 +348,7 @@ class Context:
         st = load_library().fdl_model_forward(
             self.handle, ctypes.byref(m), _ptr(tokens), R, _ptr(row_seq), _ptr(row_rope_pos), _ptr(row_cache_pos),
             _ptr(row_kind), _ptr(cu_seqlens_q), _ptr(kv_len), B, _ptr(block_table), int(block_table.shape[-1]),
-            ctypes.cast(kc, _PP), ctypes.cast(vc, _PP), _ptr(search_pos), search_ld, _ptr(n_search),
+            kc, vc, _ptr(search_pos), search_ld, _ptr(n_search),
             _ptr(track_scores), track_ld, _ptr(workspace), int(workspace.numel() * workspace.element_size()),
             _ptr(final_out))
         self._check(st, "fdl_model_forward")
@@ -309,6 +364,34 @@ class Context:
         a.mask_conf, a.mask_argmax = _ptr(mask_conf), _ptr(mask_argmax)
         self._check(load_library().fdl_lm_head_verify(self.handle, _ptr(mask_hidden), _ptr(w_lm), ctypes.byref(a)),
                     "fdl_lm_head_verify")
+
+
+def _ptr_array(tensors):
+    """Host array of device pointers (kept alive by the caller)."""
+    arr = (ctypes.c_void_p * len(tensors))(*[_ptr(t) for t in tensors])
+    return ctypes.cast(arr, _PP)
+
+
+def _model_struct(model: dict):
+    """fdl_model for a dict of device tensors, and the pointer arrays it references."""
+    layers = model["layers"]
+    keep = {k: (ctypes.c_void_p * len(layers))(*[_ptr(w[k]) for w in layers])
+            for k in ("g_attn", "w_qkv", "w_o", "g_mlp", "w_gu", "w_down")}
+    m = fdl_model()
+    m.n_layers, m.ffn, m.rms_eps = len(layers), int(model["ffn"]), float(model["eps"])
+    m.embed, m.g_final = _ptr(model["embed"]), _ptr(model["g_final"])
+    for k, a in keep.items():
+        setattr(m, k, ctypes.cast(a, _PP))
+    return m, keep
+
+
+def _flash_params(params: dict) -> fdl_flash_params:
+    pr = fdl_flash_params()
+    pr.window, pr.track_budget, pr.max_search = int(params["window"]), int(params["track_budget"]), \
+        int(params["max_search"])
+    pr.eps, pr.gamma = float(params["eps"]), float(params["gamma"])
+    pr.force_progress, pr.mask_token = int(bool(params["force_progress"])), int(params["mask_id"])
+    return pr
 
 
 def _stream_handle(stream) -> int | None:
@@ -371,6 +454,14 @@ def fdl_model_workspace_bytes(ctx: Context, ffn: int, R: int) -> int:
 
 def fdl_model_forward(ctx: Context, *a, **k) -> None:
     ctx.model_forward(*a, **k)
+
+
+def fdl_flash_workspace_bytes(ctx: Context, *a, **k) -> int:
+    return ctx.flash_workspace_bytes(*a, **k)
+
+
+def fdl_flash_step(ctx: Context, *a, **k):
+    return ctx.flash_step(*a, **k)
 
 
 def fdl_sched_attn_noalloc(cfg: fdl_config, q, k_cache, v_cache, block_table, cu_seqlens_q, kv_len, row_kind,

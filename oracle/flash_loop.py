@@ -48,8 +48,9 @@ def flash_step(model: dict, w_lm, seqs: dict, params: dict, caches, geom, dtype:
     max_search, eps, gamma, force_progress, mask_id, max_views.
 
     ``force`` (optional) replaces this oracle's own decisions with given ones
-    so that a step can follow another implementation's path: keys 'commit'
-    [R_w], 'search_rows' [B, max_search], 'n_search' [B], 'n_accept' [B].
+    so that a step can follow another implementation's path: keys 'argmax'
+    (the draft tokens) and 'commit' [R_w], 'search_rows' [B, max_search],
+    'n_search' [B], 'n_accept' [B].
 
     Returns (new seqs, new caches, trace dict).
     """
@@ -84,10 +85,11 @@ def flash_step(model: dict, w_lm, seqs: dict, params: dict, caches, geom, dtype:
     logits = lm_head_logits(final[wsel], w_lm)
     dec = unmask(logits, w_seq, w_pos, B, params["eps"], bool(params["force_progress"]), ms)
     trace["window_pos"], trace["window_seq"], trace["unmask"] = w_pos, w_seq, dec
+    trace["window_rows"], trace["window_logits"] = wsel, logits
     commit = dec["commit"] if force is None else np.asarray(force["commit"])
     search_rows = dec["search_rows"] if force is None else np.asarray(force["search_rows"])
     n_search = dec["n_search"] if force is None else np.asarray(force["n_search"])
-    draft_tok = np.asarray(dec["argmax"], np.int64)
+    draft_tok = np.asarray(dec["argmax"] if force is None else force["argmax"], np.int64)
 
     committed = [[] for _ in range(B)]
     for r in np.nonzero(commit)[0]:
@@ -131,8 +133,10 @@ def flash_step(model: dict, w_lm, seqs: dict, params: dict, caches, geom, dtype:
         for b in range(B):
             for j, r in enumerate(search[b]):
                 dtok[b * ms + j] = draft_tok[r]
-        ver = verify(lm_head_logits(hv, w_lm), dtok, np.array([len(s) for s in search]), params["gamma"], B, ms)
-        trace["verify"] = dict(ver, s_pos=s_pos, draft_tok=dtok, final=final_v, mask_rows=mask_rows)
+        mask_logits = lm_head_logits(hv, w_lm)
+        ver = verify(mask_logits, dtok, np.array([len(s) for s in search]), params["gamma"], B, ms)
+        trace["verify"] = dict(ver, s_pos=s_pos, draft_tok=dtok, final=final_v, mask_rows=mask_rows,
+                               mask_logits=mask_logits)
         n_acc = ver["n_accept"] if force is None else np.asarray(force["n_accept"])
         for b in range(B):
             accepted[b] = [(int(w_pos[r]), int(draft_tok[r])) for r in search[b][:int(n_acc[b])]]
