@@ -527,7 +527,7 @@ typedef struct {
   int* state;                  /* host [B] in/out: -1 before the first step           */
 } fdl_flash_seqs;
 
-typedef struct {               /* optional record of one step; host pointers, any may be NULL */
+typedef struct {               /* optional record of one step; any pointer may be NULL */
   int* n_rows;                 /* [2]: draft-forward rows, verify-forward rows (0 when none) */
   int* n_window;               /* [1]: window rows R_w                               */
   int* window_seq;             /* [B*window]: each window row's sequence             */
@@ -541,6 +541,9 @@ typedef struct {               /* optional record of one step; host pointers, an
   int* mask_argmax;            /* [B*max_search]: and prediction                      */
   int* n_accept;               /* [B]                                                */
   float* track;                /* [B*max_seq]: the draft forward's tracker scores     */
+  void* draft_final;           /* DEVICE [max_rows, d_model] bf16: the draft forward's
+                                  final normed rows, in row order                    */
+  void* verify_final;          /* DEVICE [max_rows, d_model] bf16: the verify forward's */
 } fdl_flash_trace;
 
 size_t fdl_flash_workspace_bytes(const fdl_ctx* ctx, int ffn, const fdl_flash_params* params, int B,

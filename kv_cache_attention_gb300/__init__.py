@@ -111,7 +111,8 @@ class fdl_flash_seqs(ctypes.Structure):
 
 class fdl_flash_trace(ctypes.Structure):
     _fields_ = [(n, _P) for n in ("n_rows", "n_window", "window_seq", "window_pos", "conf", "argmax", "commit",
-                                  "search_rows", "n_search", "mask_conf", "mask_argmax", "n_accept", "track")]
+                                  "search_rows", "n_search", "mask_conf", "mask_argmax", "n_accept", "track",
+                                  "draft_final", "verify_final")]
 
 
 class fdl_refresh_args(ctypes.Structure):
@@ -324,12 +325,20 @@ class Context:
                        mask_argmax=np.zeros(B * MS, np.int32), n_accept=np.zeros(B, np.int32),
                        track=np.zeros(B * N, np.float32))
             tr = fdl_flash_trace(**{k: v.ctypes.data for k, v in rec.items()})
+            import torch
+            finals = [torch.empty((self.cfg.max_rows, self.cfg.d_model), dtype=torch.bfloat16, device="cuda")
+                      for _ in range(2)]
+            tr.draft_final, tr.verify_final = finals[0].data_ptr(), finals[1].data_ptr()
         st = load_library().fdl_flash_step(
             self.handle, ctypes.byref(m), _ptr(w_lm), kc, vc, _ptr(block_table), int(block_table.shape[-1]),
             ctypes.byref(pr), ctypes.byref(sq), ctypes.byref(tr) if tr is not None else None, _ptr(workspace),
             int(workspace.numel() * workspace.element_size()))
         del keep
         self._check(st, "fdl_flash_step")
+        if rec is not None:
+            n0, n1 = int(rec["n_rows"][0]), int(rec["n_rows"][1])
+            rec["draft_final"] = finals[0][:n0].float().cpu().numpy()
+            rec["verify_final"] = finals[1][:n1].float().cpu().numpy()
         return rec
 
     def model_forward(self, model: dict, tokens, row_seq, row_rope_pos, row_cache_pos, row_kind, cu_seqlens_q,

@@ -195,6 +195,8 @@ extern "C" fdl_status fdl_flash_step(fdl_ctx* ctx, const fdl_model* m, const voi
   FDL_TRY(fdl_model_forward(ctx, m, d.tok, rw.n, d.seq, d.rope, d.rope, d.kind, d.cu, d.kv_len, B, block_table,
                             bt_stride, k_caches, v_caches, nullptr, 0, nullptr, d.track, N, d.model_ws,
                             d.model_ws_bytes, d.final_rows));
+  if (trace && trace->draft_final)
+    FDL_CU(cudaMemcpyAsync(trace->draft_final, d.final_rows, (size_t)rw.n * dm * 2, cudaMemcpyDeviceToDevice, st));
   FDL_CU(fdl_launch_pdl(gather_rows_kernel, dim3(RW), dim3(kGatherThreads), 0, st, 1,
                         (const __nv_bfloat16*)d.final_rows, (const int*)d.gidx, dm, d.gathered));
 
@@ -273,6 +275,8 @@ extern "C" fdl_status fdl_flash_step(fdl_ctx* ctx, const fdl_model* m, const voi
     FDL_TRY(fdl_model_forward(ctx, m, d.tok, vr.n, d.seq, d.rope, d.cache, d.kind, d.cu, d.kv_len, B, block_table,
                               bt_stride, k_caches, v_caches, d.spos, MS, d.nsearch, nullptr, 0, d.model_ws,
                               d.model_ws_bytes, d.final_rows));
+    if (trace && trace->verify_final)
+      FDL_CU(cudaMemcpyAsync(trace->verify_final, d.final_rows, (size_t)vr.n * dm * 2, cudaMemcpyDeviceToDevice, st));
     FDL_CU(fdl_launch_pdl(gather_rows_kernel, dim3(B * MS), dim3(kGatherThreads), 0, st, 1,
                           (const __nv_bfloat16*)d.final_rows, (const int*)d.gidx, dm, d.gathered));
     fdl_unmask_args va = {};

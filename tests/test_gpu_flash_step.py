@@ -76,10 +76,13 @@ def test_flash_steps_teacher_forced():
         assert int(rec["n_rows"][0]) == len(tr["draft_pos"]), step
         assert rec["window_pos"][:RW].tolist() == tr["window_pos"].tolist()
         assert rec["window_seq"][:RW].tolist() == tr["window_seq"].tolist()
-        # window rows: confidences and predictions
+        # the draft forward's final rows, then the window rows' confidences and
+        # predictions (the logits have a standard deviation near 4.5 here, so a
+        # relative difference r in a hidden row moves a logit by about 4.5 r)
+        _rows_close(rec["draft_final"], tr["draft_final"], f"draft rows, step {step}")
         dec = tr["unmask"]
-        np.testing.assert_allclose(rec["conf"][:RW], dec["conf"], atol=2e-3, rtol=2e-2)
-        clear = _top2_gap(tr["window_logits"]) > 5e-2
+        np.testing.assert_allclose(rec["conf"][:RW], dec["conf"], atol=1e-2, rtol=5e-2)
+        clear = _top2_gap(tr["window_logits"]) > 0.2
         assert np.array_equal(rec["argmax"][:RW][clear], dec["argmax"][clear])
         # the GPU's decisions are the rule applied to its own confidences
         want = _decide(rec["conf"][:RW], tr["window_seq"], tr["window_pos"], B, params["eps"], True, MS)
@@ -93,10 +96,11 @@ def test_flash_steps_teacher_forced():
             saw["verify_steps"] += 1
             assert int(rec["n_rows"][1]) == len(tr["verify"]["final"])
             ver = tr["verify"]
+            _rows_close(rec["verify_final"], ver["final"], f"verify rows, step {step}")
             valid = np.array([b * MS + j for b in range(B) for j in range(int(rec["n_search"][b]))])
-            np.testing.assert_allclose(rec["mask_conf"][valid], ver["mask_conf"][valid], atol=2e-3, rtol=2e-2)
+            np.testing.assert_allclose(rec["mask_conf"][valid], ver["mask_conf"][valid], atol=1e-2, rtol=5e-2)
             mgap = _top2_gap(ver["mask_logits"])[valid]
-            assert np.array_equal(rec["mask_argmax"][valid][mgap > 5e-2], ver["mask_argmax"][valid][mgap > 5e-2])
+            assert np.array_equal(rec["mask_argmax"][valid][mgap > 0.2], ver["mask_argmax"][valid][mgap > 0.2])
             acc, n_acc = _verify_rule(rec["mask_conf"], rec["mask_argmax"], ver["draft_tok"], rec["n_search"],
                                       params["gamma"], B, MS)
             assert rec["n_accept"].tolist() == n_acc.tolist()
@@ -128,3 +132,15 @@ def _top2_gap(logits):
     """Gap between the two largest float64 logits of each row."""
     top = np.sort(logits, axis=1)[:, -2:]
     return top[:, 1] - top[:, 0]
+
+
+def _rows_close(gpu, ref, what):
+    """Each final row (unit RMS times the gains) within 1e-2 relative RMS of
+    the oracle's: bf16 roundings of the intermediates on both sides, carried
+    through two layers whose W_o and W_down are large. A row taken from the
+    wrong position or sequence would be off by about sqrt(2)."""
+    gpu = np.asarray(gpu, np.float64)
+    assert gpu.shape == ref.shape, (what, gpu.shape, ref.shape)
+    rel = np.sqrt(((gpu - ref) ** 2).mean(1) / (ref ** 2).mean(1))
+    assert (rel < 1e-2).all(), f"{what}: worst row relative RMS difference {rel.max():.3e}"
+
