@@ -445,6 +445,9 @@ def run_gpu(args, world, rank, local):
 # ---------------------------------------------------------------------------
 # Per-configuration kernel measurements (--configs)
 # ---------------------------------------------------------------------------
+CONFIG_SECTIONS = ("ragged", "chain", "flash_verify", "lm_head", "refresh", "flash_step")
+
+
 def run_configs(args):
     """Times each kernel of the path on the ragged batch, one layer of the
     32-layer chain and the Flash-Verify stress workload, and the fused LM
@@ -529,245 +532,258 @@ def run_configs(args):
         return out
 
     results = []
-    # ragged batch of 16 (paged cache, half full refresh)
-    wl = synth.ragged_batch()
-    e, s, g = wl.extra, wl.shape, wl.geom
-    rows = e["rows"]
-    ctx = fdl.fdl_create(s.d_model, s.n_heads, s.head_dim, s.rope_theta, wl.batch, wl.max_seq, 0, g.page_size,
-                         g.n_pages, rows.n_rows, 16, "bf16", stream=stream)
-    Ws = [bf(e["w"]), bf(e["w"])]
-    res = layer_kernels("ragged_batch", wl, rows, bf(e["x"]), Ws, bf(e["k_cache"]), bf(e["v_cache"]), ctx, reps=20)
-    results.append({"config": "ragged_batch_b16_p64", **res})
-    ctx.close()
-    del Ws
+    only = args.configs if args.configs != "all" else None
 
-    # one layer of the 32-layer chain: 8 sequences x (32 window + 32 tracked)
-    wl = synth.layer_chain()
-    e, s, g = wl.extra, wl.shape, wl.geom
-    d = s.d_model
-    rng = np.random.default_rng(7)
-    per_seq = [synth.draft_rows(e["window_pos"], np.sort(rng.choice(e["prompt"], 32, replace=False)))
-               for _ in range(wl.batch)]
-    rows = synth.build_rows(per_seq)
-    ctx = fdl.fdl_create(d, s.n_heads, s.head_dim, s.rope_theta, wl.batch, wl.max_seq, 0, g.page_size,
-                         g.n_pages, rows.n_rows, 16, "bf16", stream=stream)
-    n_slots = g.n_pages * g.page_size
-    kc = torch.randn((n_slots, d), device="cuda").mul_(0.02 * d ** 0.5).bfloat16()
-    vc = torch.randn((n_slots, d), device="cuda").mul_(0.02 * d ** 0.5).bfloat16()
-    Ws = [bf(synth.chain_weight(e["seed"], l, d)) for l in range(2)]
-    x = bf(synth.chain_hidden(e["seed"], 1, 0, rows.n_rows, d))
-    res = layer_kernels("layer_chain", wl, rows, x, Ws, kc, vc, ctx)
-    results.append({"config": "layer_chain_b8_one_layer", **res})
-    ctx.close()
-    del Ws, kc, vc
+    def want(name):
+        return only is None or only == name
 
-    # Flash-Verify stress: draft forward, eps unmasking, verify acceptance, top-k
-    wl = synth.flash_verify()
-    e, s, g = wl.extra, wl.shape, wl.geom
-    rows = e["rows"]
-    B, ms, V = wl.batch, e["max_search"], e["vocab"]
-    ctx = fdl.fdl_create(s.d_model, s.n_heads, s.head_dim, s.rope_theta, B, wl.max_seq, wl.max_views,
-                         g.page_size, g.n_pages, rows.n_rows, V, "bf16", stream=stream)
-    Ws = [bf(e["w"]), bf(e["w"])]
-    res = layer_kernels("flash_verify", wl, rows, bf(e["x"]), Ws, bf(e["k_cache"]), bf(e["v_cache"]), ctx)
-    del Ws
-    logits = bf(e["logits"])
-    Rw = logits.shape[0]
-    wseq, wpos = i32(e["window_row_seq"]), i32(e["window_row_pos"])
-    conf = torch.empty(Rw, dtype=torch.float32, device="cuda")
-    arg = torch.empty(Rw, dtype=torch.int32, device="cuda")
-    com = torch.empty(Rw, dtype=torch.uint8, device="cuda")
-    srows = torch.empty((B, ms), dtype=torch.int32, device="cuda")
-    nsr = torch.empty((B,), dtype=torch.int32, device="cuda")
-    um = lambda: ctx.unmask_verify(B, ms, logits=logits, row_seq=wseq, row_pos=wpos, eps=e["eps"],
-                                   force_progress=False, conf=conf, argmax=arg, commit=com, search_rows=srows,
-                                   n_search=nsr)
-    res["unmask (eps rule)"] = entry(timed([um], 50), None, 2.0 * Rw * V)
-    um()
-    torch.cuda.synchronize()
-    ns_host = nsr.cpu().numpy()
-    mask_logits = torch.empty((B * ms, V), dtype=torch.bfloat16, device="cuda")
-    mask_logits.copy_(logits[: B * ms])
-    draft = arg[: B * ms].clone()
-    acc = torch.empty(B * ms, dtype=torch.uint8, device="cuda")
-    nacc = torch.empty(B, dtype=torch.int32, device="cuda")
-    mconf = torch.empty(B * ms, dtype=torch.float32, device="cuda")
-    marg = torch.empty(B * ms, dtype=torch.int32, device="cuda")
-    vf = lambda: ctx.unmask_verify(B, ms, mask_logits=mask_logits, draft_tok=draft, gamma=e["gamma"], n_search=nsr,
-                                   accept=acc, n_accept=nacc, mask_conf=mconf, mask_argmax=marg)
-    res["verify (acceptance)"] = entry(timed([vf], 50), None, 2.0 * float(ns_host.sum()) * V)
-    res["verify (acceptance)"]["valid_rows"] = int(ns_host.sum())
-    track = torch.rand((B, wl.max_seq), device="cuda")
-    elig, sl = torch.as_tensor(e["eligible"]).cuda(), i32(wl.seq_len)
-    idx = torch.empty((B, 32), dtype=torch.int32, device="cuda")
-    cnt = torch.empty((B,), dtype=torch.int32, device="cuda")
-    res["track_topk"] = entry(timed([lambda: ctx.track_topk(track, elig, sl, 32, idx, cnt)], 200))
-    ctx.sync_status()
-    results.append({"config": "flash_verify_b32", **res})
-    ctx.close()
+    if want("ragged"):
+        # ragged batch of 16 (paged cache, half full refresh)
+        wl = synth.ragged_batch()
+        e, s, g = wl.extra, wl.shape, wl.geom
+        rows = e["rows"]
+        ctx = fdl.fdl_create(s.d_model, s.n_heads, s.head_dim, s.rope_theta, wl.batch, wl.max_seq, 0, g.page_size,
+                             g.n_pages, rows.n_rows, 16, "bf16", stream=stream)
+        Ws = [bf(e["w"]), bf(e["w"])]
+        res = layer_kernels("ragged_batch", wl, rows, bf(e["x"]), Ws, bf(e["k_cache"]), bf(e["v_cache"]), ctx, reps=20)
+        results.append({"config": "ragged_batch_b16_p64", **res})
+        ctx.close()
+        del Ws
 
-    # fused LM head + eps unmasking (the step after the layers): the LLaDA
-    # vocabulary and width against the 32 window rows; the weight (1.04 GB,
-    # two seeded copies) is the algorithmic traffic
-    d, V, Rw = 4096, 126464, 32
-    ctx = fdl.fdl_create(d, 32, 128, 5e5, 1, 64, 0, 64, 1, 64, V, "bf16", stream=stream)
-    gen = torch.Generator(device="cuda").manual_seed(1009)
-    W_lm = [(torch.randn((V, d), device="cuda", generator=gen) * 0.02).bfloat16() for _ in range(2)]
-    hid = torch.randn((Rw, d), device="cuda", generator=gen).bfloat16()
-    rs, rp = i32(np.zeros(Rw)), i32(512 + np.arange(Rw))
-    conf = torch.empty(Rw, dtype=torch.float32, device="cuda")
-    arg = torch.empty(Rw, dtype=torch.int32, device="cuda")
-    com = torch.empty(Rw, dtype=torch.uint8, device="cuda")
-    srows = torch.empty((1, 16), dtype=torch.int32, device="cuda")
-    nsr = torch.empty((1,), dtype=torch.int32, device="cuda")
-    lm = [lambda W=W: ctx.lm_head_unmask(hid, W, 1, 16, row_seq=rs, row_pos=rp, eps=0.9, force_progress=True,
-                                         conf=conf, argmax=arg, commit=com, search_rows=srows, n_search=nsr)
-          for W in W_lm]
-    res = {"lm_head_unmask": entry(timed(lm, 50), 2.0 * Rw * V * d, 2.0 * (V * d + Rw * d))}
-    ctx.sync_status()
-    results.append({"config": "lm_head_llada_vocab_w32", "rows": Rw, **res})
-    ctx.close()
-    del W_lm
+    if want("chain"):
+        # one layer of the 32-layer chain: 8 sequences x (32 window + 32 tracked)
+        wl = synth.layer_chain()
+        e, s, g = wl.extra, wl.shape, wl.geom
+        d = s.d_model
+        rng = np.random.default_rng(7)
+        per_seq = [synth.draft_rows(e["window_pos"], np.sort(rng.choice(e["prompt"], 32, replace=False)))
+                   for _ in range(wl.batch)]
+        rows = synth.build_rows(per_seq)
+        ctx = fdl.fdl_create(d, s.n_heads, s.head_dim, s.rope_theta, wl.batch, wl.max_seq, 0, g.page_size,
+                             g.n_pages, rows.n_rows, 16, "bf16", stream=stream)
+        n_slots = g.n_pages * g.page_size
+        kc = torch.randn((n_slots, d), device="cuda").mul_(0.02 * d ** 0.5).bfloat16()
+        vc = torch.randn((n_slots, d), device="cuda").mul_(0.02 * d ** 0.5).bfloat16()
+        Ws = [bf(synth.chain_weight(e["seed"], l, d)) for l in range(2)]
+        x = bf(synth.chain_hidden(e["seed"], 1, 0, rows.n_rows, d))
+        res = layer_kernels("layer_chain", wl, rows, x, Ws, kc, vc, ctx)
+        results.append({"config": "layer_chain_b8_one_layer", **res})
+        ctx.close()
+        del Ws, kc, vc
 
-    # KV-cache refresh policies over one scripted decode of one layer: LLaDA
-    # layer shape, batch 1, prompt 512 + gen 256, block (window) 32, two
-    # positions unmasked per step (128 steps). Each step is the projection
-    # and the attention of the rows the policy chooses, one graph per step,
-    # replayed in order; the two weight copies alternate between steps
-    # (200 MB > L2).
-    d, Hh, hd, P, G, blk = 4096, 32, 128, 512, 256, 32
-    N = P + G
-    ctx = fdl.fdl_create(d, Hh, hd, 5e5, 1, N, 0, N, 1, N, 16, "bf16", stream=stream)
-    gen = torch.Generator(device="cuda").manual_seed(1011)
-    Ws = [(torch.randn((3 * d, d), device="cuda", generator=gen) * 0.02).bfloat16() for _ in range(2)]
-    X = torch.randn((N, d), device="cuda", generator=gen).bfloat16()
-    kc = torch.zeros((N, d), dtype=torch.bfloat16, device="cuda")
-    vc = torch.zeros_like(kc)
-    q = torch.empty((N, Hh, hd), dtype=torch.bfloat16, device="cuda")
-    o = torch.empty_like(q)
-    lse = torch.empty((N, Hh), dtype=torch.float32, device="cuda")
-    track = torch.zeros((1, N), dtype=torch.float32, device="cuda")
-    bt, kvl = i32([[0]]), i32([N])
-    names = {fdl.FDL_REFRESH_FULL: "full_recompute", fdl.FDL_REFRESH_PREFIX: "fastdllm_prefix_cache",
-             fdl.FDL_REFRESH_DUAL: "fastdllm_dual_cache", fdl.FDL_REFRESH_FREECACHE: "freecache",
-             fdl.FDL_REFRESH_FLASH_DRAFT: "flash_dllm_draft_forward_only"}
-    for policy, name in names.items():
-        rng = np.random.default_rng([1011, policy])
-        masked = np.zeros((1, N), np.uint8)
-        masked[0, P:] = 1
-        state = np.full(1, -1, np.int32)
-        steps = []
-        while masked.any():
-            tracked = n_tracked = None
-            if policy == fdl.FDL_REFRESH_FLASH_DRAFT:
-                tracked = rng.permutation(np.nonzero(masked[0] == 0)[0])[:32].astype(np.int32)[None]
-                n_tracked = np.array([tracked.shape[1]], np.int32)
-            rows = fdl.fdl_refresh_rows(policy, [P], [N], masked, blk, state, tracked, n_tracked)
-            steps.append(rows)
-            masked[0, synth.trace_unmask(rng, rows.row_rope_pos[rows.row_kind == 1], 2, 2)] = 0
-        graphs, keep, n_rows, floor_us = [], [], 0, 0.0
-        for t, rows in enumerate(steps):
-            R = rows.n_rows
-            args_t = (i32(rows.row_seq), i32(rows.row_rope_pos), i32(rows.row_kind), i32(rows.cu_seqlens))
-            keep.append(args_t)
-            rs, rp, rk, cu = args_t
-            tr = track if policy == fdl.FDL_REFRESH_FLASH_DRAFT else None
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                ctx.qkv_rope_cache_write(X[:R], Ws[t % 2], rs, rp, rp, bt, kc, vc, q[:R])
-                ctx.sched_attn(q[:R], kc, vc, bt, cu, kvl, rk, o[:R], lse_out=lse[:R], track_scores=tr)
-            graphs.append(g)
-            n_rows += R
-            qkv_fl, qkv_by = 2.0 * R * 3 * d * d, 2.0 * (3 * d * d + 4 * R * d)
-            att_fl, att_by = 4.0 * d * R * N, 2.0 * (2 * d * N + 2 * R * d)
-            floor_us += max(qkv_by / hbm * 1e-3, qkv_fl / tc * 1e-6) + max(att_by / hbm * 1e-3, att_fl / tc * 1e-6)
-        for _ in range(2):
-            for g in graphs:
-                g.replay()
+    if want("flash_verify"):
+        # Flash-Verify stress: draft forward, eps unmasking, verify acceptance, top-k
+        wl = synth.flash_verify()
+        e, s, g = wl.extra, wl.shape, wl.geom
+        rows = e["rows"]
+        B, ms, V = wl.batch, e["max_search"], e["vocab"]
+        ctx = fdl.fdl_create(s.d_model, s.n_heads, s.head_dim, s.rope_theta, B, wl.max_seq, wl.max_views,
+                             g.page_size, g.n_pages, rows.n_rows, V, "bf16", stream=stream)
+        Ws = [bf(e["w"]), bf(e["w"])]
+        res = layer_kernels("flash_verify", wl, rows, bf(e["x"]), Ws, bf(e["k_cache"]), bf(e["v_cache"]), ctx)
+        del Ws
+        logits = bf(e["logits"])
+        Rw = logits.shape[0]
+        wseq, wpos = i32(e["window_row_seq"]), i32(e["window_row_pos"])
+        conf = torch.empty(Rw, dtype=torch.float32, device="cuda")
+        arg = torch.empty(Rw, dtype=torch.int32, device="cuda")
+        com = torch.empty(Rw, dtype=torch.uint8, device="cuda")
+        srows = torch.empty((B, ms), dtype=torch.int32, device="cuda")
+        nsr = torch.empty((B,), dtype=torch.int32, device="cuda")
+        um = lambda: ctx.unmask_verify(B, ms, logits=logits, row_seq=wseq, row_pos=wpos, eps=e["eps"],
+                                       force_progress=False, conf=conf, argmax=arg, commit=com, search_rows=srows,
+                                       n_search=nsr)
+        res["unmask (eps rule)"] = entry(timed([um], 50), None, 2.0 * Rw * V)
+        um()
         torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        passes = 5
-        a.record(stream)
-        for _ in range(passes):
-            for g in graphs:
-                g.replay()
-        b.record(stream)
-        torch.cuda.synchronize()
+        ns_host = nsr.cpu().numpy()
+        mask_logits = torch.empty((B * ms, V), dtype=torch.bfloat16, device="cuda")
+        mask_logits.copy_(logits[: B * ms])
+        draft = arg[: B * ms].clone()
+        acc = torch.empty(B * ms, dtype=torch.uint8, device="cuda")
+        nacc = torch.empty(B, dtype=torch.int32, device="cuda")
+        mconf = torch.empty(B * ms, dtype=torch.float32, device="cuda")
+        marg = torch.empty(B * ms, dtype=torch.int32, device="cuda")
+        vf = lambda: ctx.unmask_verify(B, ms, mask_logits=mask_logits, draft_tok=draft, gamma=e["gamma"], n_search=nsr,
+                                       accept=acc, n_accept=nacc, mask_conf=mconf, mask_argmax=marg)
+        res["verify (acceptance)"] = entry(timed([vf], 50), None, 2.0 * float(ns_host.sum()) * V)
+        res["verify (acceptance)"]["valid_rows"] = int(ns_host.sum())
+        track = torch.rand((B, wl.max_seq), device="cuda")
+        elig, sl = torch.as_tensor(e["eligible"]).cuda(), i32(wl.seq_len)
+        idx = torch.empty((B, 32), dtype=torch.int32, device="cuda")
+        cnt = torch.empty((B,), dtype=torch.int32, device="cuda")
+        res["track_topk"] = entry(timed([lambda: ctx.track_topk(track, elig, sl, 32, idx, cnt)], 200))
         ctx.sync_status()
-        us = a.elapsed_time(b) / passes * 1e3
-        results.append({"config": f"refresh_{name}_llada_b1_p512_g256_blk32", "steps": len(steps),
-                        "rows": n_rows, "us_per_decode_layer": round(us, 1),
-                        "us_per_step": round(us / len(steps), 2),
-                        "rows_per_s": round(n_rows / us * 1e6, 1),
-                        "roofline_floor_us": round(floor_us, 1), "frac_roofline": round(floor_us / us, 3)})
-        del graphs, keep
-    ctx.close()
-    del Ws
+        results.append({"config": "flash_verify_b32", **res})
+        ctx.close()
 
-    # Whole denoising steps of a LLaDA-8B-shaped model with random weights
-    # (32 layers, d_model 4096, 32 heads, SwiGLU 12288, vocab 126464; 16 GB
-    # of bf16 weights): batch 1, prompt 512 + gen 256, window 32, 32 tracked,
-    # up to 16 search tokens. The first step is the full forward over all 768
-    # positions; the steady steps run a draft forward over 64 rows, the LM
-    # head, a verify forward and the acceptance. Wall time per call (the step
-    # reads its decisions back three times). The floor counts the weights
-    # read by both forwards and both LM-head passes, and each forward's cache
-    # read, at the measured HBM rate.
-    L, d, F, V, Hh, hd = 32, 4096, 12288, 126464, 32, 128
-    P, G, Wn, BTk, MSk = 512, 256, 32, 32, 16
-    N = P + G
-    ctx = fdl.fdl_create(d, Hh, hd, 5e5, 1, N, 2 * MSk, N + 2 * MSk, 1, N, V, "bf16", stream=stream)
-    gen = torch.Generator(device="cuda").manual_seed(1017)
+    if want("lm_head"):
+        # fused LM head + eps unmasking (the step after the layers): the LLaDA
+        # vocabulary and width against the 32 window rows; the weight (1.04 GB,
+        # two seeded copies) is the algorithmic traffic
+        d, V, Rw = 4096, 126464, 32
+        ctx = fdl.fdl_create(d, 32, 128, 5e5, 1, 64, 0, 64, 1, 64, V, "bf16", stream=stream)
+        gen = torch.Generator(device="cuda").manual_seed(1009)
+        W_lm = [(torch.randn((V, d), device="cuda", generator=gen) * 0.02).bfloat16() for _ in range(2)]
+        hid = torch.randn((Rw, d), device="cuda", generator=gen).bfloat16()
+        rs, rp = i32(np.zeros(Rw)), i32(512 + np.arange(Rw))
+        conf = torch.empty(Rw, dtype=torch.float32, device="cuda")
+        arg = torch.empty(Rw, dtype=torch.int32, device="cuda")
+        com = torch.empty(Rw, dtype=torch.uint8, device="cuda")
+        srows = torch.empty((1, 16), dtype=torch.int32, device="cuda")
+        nsr = torch.empty((1,), dtype=torch.int32, device="cuda")
+        lm = [lambda W=W: ctx.lm_head_unmask(hid, W, 1, 16, row_seq=rs, row_pos=rp, eps=0.9, force_progress=True,
+                                             conf=conf, argmax=arg, commit=com, search_rows=srows, n_search=nsr)
+              for W in W_lm]
+        res = {"lm_head_unmask": entry(timed(lm, 50), 2.0 * Rw * V * d, 2.0 * (V * d + Rw * d))}
+        ctx.sync_status()
+        results.append({"config": "lm_head_llada_vocab_w32", "rows": Rw, **res})
+        ctx.close()
+        del W_lm
 
-    def rnd(*shape, std=0.02):
-        return (torch.randn(shape, device="cuda", generator=gen, dtype=torch.bfloat16) * std)
+    if want("refresh"):
+        # KV-cache refresh policies over one scripted decode of one layer: LLaDA
+        # layer shape, batch 1, prompt 512 + gen 256, block (window) 32, two
+        # positions unmasked per step (128 steps). Each step is the projection
+        # and the attention of the rows the policy chooses, one graph per step,
+        # replayed in order; the two weight copies alternate between steps
+        # (200 MB > L2).
+        d, Hh, hd, P, G, blk = 4096, 32, 128, 512, 256, 32
+        N = P + G
+        ctx = fdl.fdl_create(d, Hh, hd, 5e5, 1, N, 0, N, 1, N, 16, "bf16", stream=stream)
+        gen = torch.Generator(device="cuda").manual_seed(1011)
+        Ws = [(torch.randn((3 * d, d), device="cuda", generator=gen) * 0.02).bfloat16() for _ in range(2)]
+        X = torch.randn((N, d), device="cuda", generator=gen).bfloat16()
+        kc = torch.zeros((N, d), dtype=torch.bfloat16, device="cuda")
+        vc = torch.zeros_like(kc)
+        q = torch.empty((N, Hh, hd), dtype=torch.bfloat16, device="cuda")
+        o = torch.empty_like(q)
+        lse = torch.empty((N, Hh), dtype=torch.float32, device="cuda")
+        track = torch.zeros((1, N), dtype=torch.float32, device="cuda")
+        bt, kvl = i32([[0]]), i32([N])
+        names = {fdl.FDL_REFRESH_FULL: "full_recompute", fdl.FDL_REFRESH_PREFIX: "fastdllm_prefix_cache",
+                 fdl.FDL_REFRESH_DUAL: "fastdllm_dual_cache", fdl.FDL_REFRESH_FREECACHE: "freecache",
+                 fdl.FDL_REFRESH_FLASH_DRAFT: "flash_dllm_draft_forward_only"}
+        for policy, name in names.items():
+            rng = np.random.default_rng([1011, policy])
+            masked = np.zeros((1, N), np.uint8)
+            masked[0, P:] = 1
+            state = np.full(1, -1, np.int32)
+            steps = []
+            while masked.any():
+                tracked = n_tracked = None
+                if policy == fdl.FDL_REFRESH_FLASH_DRAFT:
+                    tracked = rng.permutation(np.nonzero(masked[0] == 0)[0])[:32].astype(np.int32)[None]
+                    n_tracked = np.array([tracked.shape[1]], np.int32)
+                rows = fdl.fdl_refresh_rows(policy, [P], [N], masked, blk, state, tracked, n_tracked)
+                steps.append(rows)
+                masked[0, synth.trace_unmask(rng, rows.row_rope_pos[rows.row_kind == 1], 2, 2)] = 0
+            graphs, keep, n_rows, floor_us = [], [], 0, 0.0
+            for t, rows in enumerate(steps):
+                R = rows.n_rows
+                args_t = (i32(rows.row_seq), i32(rows.row_rope_pos), i32(rows.row_kind), i32(rows.cu_seqlens))
+                keep.append(args_t)
+                rs, rp, rk, cu = args_t
+                tr = track if policy == fdl.FDL_REFRESH_FLASH_DRAFT else None
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    ctx.qkv_rope_cache_write(X[:R], Ws[t % 2], rs, rp, rp, bt, kc, vc, q[:R])
+                    ctx.sched_attn(q[:R], kc, vc, bt, cu, kvl, rk, o[:R], lse_out=lse[:R], track_scores=tr)
+                graphs.append(g)
+                n_rows += R
+                qkv_fl, qkv_by = 2.0 * R * 3 * d * d, 2.0 * (3 * d * d + 4 * R * d)
+                att_fl, att_by = 4.0 * d * R * N, 2.0 * (2 * d * N + 2 * R * d)
+                floor_us += max(qkv_by / hbm * 1e-3, qkv_fl / tc * 1e-6) + max(att_by / hbm * 1e-3, att_fl / tc * 1e-6)
+            for _ in range(2):
+                for g in graphs:
+                    g.replay()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            passes = 5
+            a.record(stream)
+            for _ in range(passes):
+                for g in graphs:
+                    g.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ctx.sync_status()
+            us = a.elapsed_time(b) / passes * 1e3
+            results.append({"config": f"refresh_{name}_llada_b1_p512_g256_blk32", "steps": len(steps),
+                            "rows": n_rows, "us_per_decode_layer": round(us, 1),
+                            "us_per_step": round(us / len(steps), 2),
+                            "rows_per_s": round(n_rows / us * 1e6, 1),
+                            "roofline_floor_us": round(floor_us, 1), "frac_roofline": round(floor_us / us, 3)})
+            del graphs, keep
+        ctx.close()
+        del Ws
 
-    ones = torch.ones(d, dtype=torch.bfloat16, device="cuda")
-    model = dict(ffn=F, eps=1e-5, embed=rnd(V, d, std=1.0), g_final=ones,
-                 layers=[dict(g_attn=ones, w_qkv=rnd(3 * d, d), w_o=rnd(d, d), g_mlp=ones, w_gu=rnd(2 * F, d),
-                              w_down=rnd(d, F)) for _ in range(L)])
-    w_lm = rnd(V, d)
-    kcs = [torch.zeros((N + 2 * MSk, d), dtype=torch.bfloat16, device="cuda") for _ in range(L)]
-    vcs = [torch.zeros_like(kcs[0]) for _ in range(L)]
-    params = dict(window=Wn, track_budget=BTk, max_search=MSk, eps=0.9, gamma=0.8, force_progress=True,
-                  mask_id=V - 1, max_views=2 * MSk)
-    rng = np.random.default_rng(1017)
-    toks = np.full((1, N), V - 1, np.int32)
-    toks[0, :P] = rng.integers(0, V - 1, P)
-    msk = np.zeros((1, N), np.uint8)
-    msk[0, P:] = 1
-    seqs = dict(prompt_len=np.array([P], np.int32), seq_len=np.array([N], np.int32), tokens=toks, masked=msk,
-                tracked=np.full((1, BTk), -1, np.int32), n_tracked=np.zeros(1, np.int32),
-                state=np.full(1, -1, np.int32))
-    ws = torch.empty(ctx.flash_workspace_bytes(F, params, 1, N), dtype=torch.uint8, device="cuda")
-    bt = i32([[0]])
-    times, decoded, rows = [], [], []
-    for t in range(10):
-        before = int(seqs["masked"].sum())
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        rec = ctx.flash_step(model, w_lm, kcs, vcs, bt, params, seqs, ws, trace=False)
-        torch.cuda.synchronize()
-        times.append((time.perf_counter() - t0) * 1e3)
-        decoded.append(before - int(seqs["masked"].sum()))
-    ctx.sync_status()
-    layer_w = 2.0 * (3 * d * d + d * d + 2 * F * d + F * d)
-    fwd_bytes = L * layer_w + L * 2.0 * 2 * d * N            # weights + one K and V read of the cache
-    floor_ms = (2 * fwd_bytes + 2 * 2.0 * V * d) / (hbm * 1e9) * 1e3
-    steady = times[2:]
-    results.append({"config": "flash_step_llada8b_shape_32_layers_b1_p512_g256", "first_step_ms": round(times[0], 2),
-                    "steady_step_ms": round(statistics.median(steady), 2),
-                    "steady_steps_timed": len(steady), "tokens_decoded_per_step": decoded,
-                    "weights_gb": round((L * layer_w + 2 * 2.0 * V * d) / 1e9, 2),
-                    "steady_floor_ms": round(floor_ms, 2),
-                    "frac_hbm_floor": round(floor_ms / statistics.median(steady), 3),
-                    "note": "random weights: confidences sit near 1/vocab, so each step commits its one forced "
-                            "token and the verify forward runs on 16 search tokens"})
-    ctx.close()
-    del model, w_lm, kcs, vcs
+    if want("flash_step"):
+        # Whole denoising steps of a LLaDA-8B-shaped model with random weights
+        # (32 layers, d_model 4096, 32 heads, SwiGLU 12288, vocab 126464; 16 GB
+        # of bf16 weights): batch 1, prompt 512 + gen 256, window 32, 32 tracked,
+        # up to 16 search tokens. The first step is the full forward over all 768
+        # positions; the steady steps run a draft forward over 64 rows, the LM
+        # head, a verify forward and the acceptance. Wall time per call (the step
+        # reads its decisions back three times). The floor counts the weights
+        # read by both forwards and both LM-head passes, and each forward's cache
+        # read, at the measured HBM rate.
+        L, d, F, V, Hh, hd = 32, 4096, 12288, 126464, 32, 128
+        P, G, Wn, BTk, MSk = 512, 256, 32, 32, 16
+        N = P + G
+        ctx = fdl.fdl_create(d, Hh, hd, 5e5, 1, N, 2 * MSk, N + 2 * MSk, 1, N, V, "bf16", stream=stream)
+        gen = torch.Generator(device="cuda").manual_seed(1017)
+
+        def rnd(*shape, std=0.02):
+            return (torch.randn(shape, device="cuda", generator=gen, dtype=torch.bfloat16) * std)
+
+        ones = torch.ones(d, dtype=torch.bfloat16, device="cuda")
+        model = dict(ffn=F, eps=1e-5, embed=rnd(V, d, std=1.0), g_final=ones,
+                     layers=[dict(g_attn=ones, w_qkv=rnd(3 * d, d), w_o=rnd(d, d), g_mlp=ones, w_gu=rnd(2 * F, d),
+                                  w_down=rnd(d, F)) for _ in range(L)])
+        w_lm = rnd(V, d)
+        kcs = [torch.zeros((N + 2 * MSk, d), dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+        vcs = [torch.zeros_like(kcs[0]) for _ in range(L)]
+        params = dict(window=Wn, track_budget=BTk, max_search=MSk, eps=0.9, gamma=0.8, force_progress=True,
+                      mask_id=V - 1, max_views=2 * MSk)
+        rng = np.random.default_rng(1017)
+        toks = np.full((1, N), V - 1, np.int32)
+        toks[0, :P] = rng.integers(0, V - 1, P)
+        msk = np.zeros((1, N), np.uint8)
+        msk[0, P:] = 1
+        seqs = dict(prompt_len=np.array([P], np.int32), seq_len=np.array([N], np.int32), tokens=toks, masked=msk,
+                    tracked=np.full((1, BTk), -1, np.int32), n_tracked=np.zeros(1, np.int32),
+                    state=np.full(1, -1, np.int32))
+        ws = torch.empty(ctx.flash_workspace_bytes(F, params, 1, N), dtype=torch.uint8, device="cuda")
+        bt = i32([[0]])
+        times, decoded, rows = [], [], []
+        for t in range(10):
+            before = int(seqs["masked"].sum())
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            rec = ctx.flash_step(model, w_lm, kcs, vcs, bt, params, seqs, ws, trace=False)
+            torch.cuda.synchronize()
+            times.append((time.perf_counter() - t0) * 1e3)
+            decoded.append(before - int(seqs["masked"].sum()))
+        ctx.sync_status()
+        layer_w = 2.0 * (3 * d * d + d * d + 2 * F * d + F * d)
+        fwd_bytes = L * layer_w + L * 2.0 * 2 * d * N            # weights + one K and V read of the cache
+        floor_ms = (2 * fwd_bytes + 2 * 2.0 * V * d) / (hbm * 1e9) * 1e3
+        steady = times[2:]
+        results.append({"config": "flash_step_llada8b_shape_32_layers_b1_p512_g256", "first_step_ms": round(times[0], 2),
+                        "steady_step_ms": round(statistics.median(steady), 2),
+                        "steady_steps_timed": len(steady), "tokens_decoded_per_step": decoded,
+                        "weights_gb": round((L * layer_w + 2 * 2.0 * V * d) / 1e9, 2),
+                        "steady_floor_ms": round(floor_ms, 2),
+                        "frac_hbm_floor": round(floor_ms / statistics.median(steady), 3),
+                        "note": "random weights: confidences sit near 1/vocab, so each step commits its one forced "
+                                "token and the verify forward runs on 16 search tokens",
+                        "timing": "wall clock of each fdl_flash_step call (direct launches; the step reads its "
+                                  "decisions back three times), median of the steady steps"})
+        ctx.close()
+        del model, w_lm, kcs, vcs
     for r in results:
-        r.update({"peaks": {"hbm_gbs": hbm, "bf16_tflops": tc, "source": src},
-                  "timing": "CUDA-graph replays of one call on the dedicated stream; algorithmic work"})
+        r.setdefault("timing", "CUDA-graph replays of one call on the dedicated stream; algorithmic work")
+        r["peaks"] = {"hbm_gbs": hbm, "bf16_tflops": tc, "source": src}
         print(json.dumps(r), flush=True)
 
 
@@ -779,12 +795,16 @@ def main():
     ap.add_argument("--impl", default="fdl", choices=["fdl", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--configs", action="store_true",
+    ap.add_argument("--configs", nargs="?", const="all", default=None, metavar="SECTION",
                     help="time each kernel on the ragged-batch, 32-layer-chain and Flash-Verify workloads, "
-                         "the fused LM head, and one layer's decode under each KV-cache refresh policy")
+                         "the fused LM head, one layer's decode under each KV-cache refresh policy and whole "
+                         "denoising steps of a 32-layer model (all, or one of ragged, chain, flash_verify, "
+                         "lm_head, refresh, flash_step)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.configs:
+        if args.configs != "all" and args.configs not in CONFIG_SECTIONS:
+            raise SystemExit(f"unknown configuration {args.configs!r}; one of {', '.join(CONFIG_SECTIONS)}")
         run_configs(args)
         return
     world, rank, local = dist_init()
