@@ -34,9 +34,11 @@ __global__ void __launch_bounds__(kRowThreads) embed_kernel(const int* __restric
   for (int i = threadIdx.x; i < d; i += kRowThreads) dst[i] = ok ? __bfloat162float(src[i]) : 0.f;
 }
 
-// One CTA per row. The sum of squares is reduced in a fixed order (each
-// thread's strided elements in order, a fixed xor tree per warp, the warps'
-// sums in warp order), so the result does not depend on timing.
+// One CTA per row, four consecutive elements per thread and load (d is a
+// multiple of 128), the loads of a thread issued together. The sum of squares
+// is reduced in a fixed order (each thread's elements in order, a fixed xor
+// tree per warp, the warps' sums in warp order), so the result does not
+// depend on timing.
 __global__ void __launch_bounds__(kRowThreads) rmsnorm_kernel(const float* __restrict__ h, int d,
                                                               const __nv_bfloat16* __restrict__ g, float eps,
                                                               __nv_bfloat16* __restrict__ out) {
@@ -45,9 +47,17 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_kernel(const float* __res
   fdl::grid_dep_wait();
   fdl::grid_dep_launch();
   const int r = blockIdx.x;
-  const float* x = h + (size_t)r * d;
+  const float4* x = reinterpret_cast<const float4*>(h + (size_t)r * d);
+  const int n4 = d / 4;
   float ss = 0.f;
-  for (int i = threadIdx.x; i < d; i += kRowThreads) ss = fmaf(x[i], x[i], ss);
+#pragma unroll 4
+  for (int i = threadIdx.x; i < n4; i += kRowThreads) {
+    const float4 v = x[i];
+    ss = fmaf(v.x, v.x, ss);
+    ss = fmaf(v.y, v.y, ss);
+    ss = fmaf(v.z, v.z, ss);
+    ss = fmaf(v.w, v.w, ss);
+  }
   for (int off = 16; off; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
   if ((threadIdx.x & 31) == 0) warp_sum[threadIdx.x >> 5] = ss;
   __syncthreads();
@@ -58,23 +68,46 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_kernel(const float* __res
   }
   __syncthreads();
   const float s = scale;
-  __nv_bfloat16* y = out + (size_t)r * d;
-  for (int i = threadIdx.x; i < d; i += kRowThreads) y[i] = __float2bfloat16_rn(x[i] * s * __bfloat162float(g[i]));
+  const uint2* g4 = reinterpret_cast<const uint2*>(g);
+  uint2* y = reinterpret_cast<uint2*>(out + (size_t)r * d);
+#pragma unroll 4
+  for (int i = threadIdx.x; i < n4; i += kRowThreads) {
+    const float4 v = x[i];
+    const uint2 gw = g4[i];
+    const __nv_bfloat162 g01 = *reinterpret_cast<const __nv_bfloat162*>(&gw.x);
+    const __nv_bfloat162 g23 = *reinterpret_cast<const __nv_bfloat162*>(&gw.y);
+    const __nv_bfloat162 y01 = __floats2bfloat162_rn(v.x * s * __low2float(g01), v.y * s * __high2float(g01));
+    const __nv_bfloat162 y23 = __floats2bfloat162_rn(v.z * s * __low2float(g23), v.w * s * __high2float(g23));
+    uint2 o;
+    o.x = *reinterpret_cast<const unsigned*>(&y01);
+    o.y = *reinterpret_cast<const unsigned*>(&y23);
+    y[i] = o;
+  }
 }
 
+// Grid (rows, chunks of kRowThreads * 8 elements): each thread takes eight
+// consecutive gate and up elements with one 16-byte load each (F is a
+// multiple of 64).
 __global__ void __launch_bounds__(kRowThreads) swiglu_kernel(const __nv_bfloat16* __restrict__ gu, int F,
                                                              __nv_bfloat16* __restrict__ u) {
   fdl::grid_dep_wait();
   fdl::grid_dep_launch();
   const int r = blockIdx.x;
-  const __nv_bfloat16* gate = gu + (size_t)r * 2 * F;
-  const __nv_bfloat16* up = gate + F;
-  __nv_bfloat16* dst = u + (size_t)r * F;
-  for (int i = threadIdx.x; i < F; i += kRowThreads) {
-    const float a = __bfloat162float(gate[i]);
-    const float silu = a / (1.f + expf(-a));
-    dst[i] = __float2bfloat16_rn(silu * __bfloat162float(up[i]));
+  const int i8 = blockIdx.y * kRowThreads + threadIdx.x;  // index of an 8-element group
+  if (i8 * 8 >= F) return;
+  const uint4 gw = reinterpret_cast<const uint4*>(gu + (size_t)r * 2 * F)[i8];
+  const uint4 uw = reinterpret_cast<const uint4*>(gu + (size_t)r * 2 * F + F)[i8];
+  const __nv_bfloat162* ga = reinterpret_cast<const __nv_bfloat162*>(&gw);
+  const __nv_bfloat162* ua = reinterpret_cast<const __nv_bfloat162*>(&uw);
+  uint4 ow;
+  __nv_bfloat162* oa = reinterpret_cast<__nv_bfloat162*>(&ow);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float a0 = __low2float(ga[k]), a1 = __high2float(ga[k]);
+    const float s0 = a0 / (1.f + expf(-a0)), s1 = a1 / (1.f + expf(-a1));
+    oa[k] = __floats2bfloat162_rn(s0 * __low2float(ua[k]), s1 * __high2float(ua[k]));
   }
+  reinterpret_cast<uint4*>(u + (size_t)r * F)[i8] = ow;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -124,13 +157,19 @@ cudaError_t fdl_launch_embed(fdl_ctx* ctx, const int* tokens, int R, const void*
 
 cudaError_t fdl_launch_rmsnorm(fdl_ctx* ctx, const float* h, int R, const void* g, float eps, void* out) {
   if (R <= 0) return cudaSuccess;
+  if (ctx->cfg.d_model % 4 != 0 ||
+      ((reinterpret_cast<uintptr_t>(h) | reinterpret_cast<uintptr_t>(out)) & 15) || (reinterpret_cast<uintptr_t>(g) & 7))
+    return cudaErrorMisalignedAddress;
   return fdl_launch_pdl(rmsnorm_kernel, dim3(R), dim3(kRowThreads), 0, ctx->stream, 1, h, ctx->cfg.d_model,
                         reinterpret_cast<const __nv_bfloat16*>(g), eps, reinterpret_cast<__nv_bfloat16*>(out));
 }
 
 cudaError_t fdl_launch_swiglu(fdl_ctx* ctx, const void* gu, int R, int F, void* u) {
   if (R <= 0) return cudaSuccess;
-  return fdl_launch_pdl(swiglu_kernel, dim3(R), dim3(kRowThreads), 0, ctx->stream, 1,
+  if (F % 8 != 0 || ((reinterpret_cast<uintptr_t>(gu) | reinterpret_cast<uintptr_t>(u)) & 15))
+    return cudaErrorMisalignedAddress;
+  const int chunks = (F / 8 + kRowThreads - 1) / kRowThreads;
+  return fdl_launch_pdl(swiglu_kernel, dim3(R, chunks), dim3(kRowThreads), 0, ctx->stream, 1,
                         reinterpret_cast<const __nv_bfloat16*>(gu), F, reinterpret_cast<__nv_bfloat16*>(u));
 }
 
