@@ -261,19 +261,11 @@ cudaError_t launch(fdl_ctx* ctx, DenseParams p, const void* X, const void* W, in
     return cudaErrorInvalidValue;
   const int tiles_r = (p.R + BN - 1) / BN, tiles_f = p.N / kBM;
   const int tiles = tiles_r * tiles_f;
-  // Split K until the launch holds about two waves of resident CTAs: one
-  // CTA streams its weight tile at a rate set by the bytes its ring keeps in
-  // flight, so a launch of fewer CTAs than two per SM leaves HBM idle (192
-  // tiles of the SwiGLU gate/up product at 64 rows ran at a third of the
-  // copy rate unsplit). Capped by the split-K workspace.
   const int per_sm = BN == 64 ? 2 : 1;
-  const int slots = ctx->num_sms * per_sm;
   int ks = 1;
-  if (tiles < 2 * slots) ks = (2 * slots + tiles - 1) / tiles;
+  if (tiles < ctx->num_sms * per_sm) ks = (ctx->num_sms * per_sm) / tiles;
   ks = max(1, min(ks, min(p.nkb, 8)));
-  const size_t fit = ctx->qkv_partial_floats / ((size_t)tiles * BN * kBM);
-  if ((size_t)ks > fit) ks = fit >= 1 ? (int)fit : 1;
-  if (tiles > ctx->qkv_tickets) ks = 1;
+  if ((size_t)tiles * ks * BN * kBM > ctx->qkv_partial_floats || tiles > ctx->qkv_tickets) ks = 1;
   p.ksplit = ks;
   p.partials = ctx->qkv_partials;
   p.tickets = ctx->qkv_ticket_buf;
