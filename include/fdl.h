@@ -503,7 +503,10 @@ fdl_status fdl_verify_rows(int B, const int* seq_len, const int* tracked, int tr
  * B*max_search <= 64 (the fused LM head), 2*max_search <= config.max_views,
  * the first step's rows (every position of every sequence) <= max_rows.
  * A step on sequences with nothing left masked returns FDL_OK and does
- * nothing.
+ * nothing. An error before the decisions are applied (a bad argument, a
+ * rejected row set, a device error reported at a read-back) leaves the
+ * sequences as they were; an error while choosing the next tracked set leaves
+ * the decoded tokens in place and the tracked set unchanged.
  * ---------------------------------------------------------------------- */
 typedef struct {
   int window;         /* beta_m: masked-window rows per sequence          */

@@ -96,6 +96,18 @@ Scratch carve(char* base, const fdl_ctx* ctx, int ffn, const fdl_flash_params* p
   return s;
 }
 
+// Puts the sequences' refresh state back on every return before the step
+// has decoded anything, so a failed call leaves the host state as it was.
+struct StateGuard {
+  int* state;
+  std::vector<int> saved;
+  bool done = false;
+  StateGuard(int* st, int n) : state(st), saved(st, st + n) {}
+  ~StateGuard() {
+    if (!done) std::copy(saved.begin(), saved.end(), state);
+  }
+};
+
 struct Rows {
   std::vector<int> seq, rope, cache, kind, tok, cu;
   int n = 0;
@@ -163,7 +175,7 @@ extern "C" fdl_status fdl_flash_step(fdl_ctx* ctx, const fdl_model* m, const voi
   ra.max_rows = R_max;
   ra.row_seq = rw.seq.data(), ra.row_rope_pos = rw.rope.data(), ra.row_cache_pos = rw.cache.data();
   ra.row_kind = rw.kind.data(), ra.cu_seqlens = rw.cu.data(), ra.n_rows = &rw.n;
-  std::vector<int> state_before(s->state, s->state + B);
+  StateGuard guard(s->state, B);
   rc = fdl_refresh_rows(&ra);
   if (rc != FDL_OK) return loop_fail(ctx, rc, "fdl_flash_step: draft rows rejected (max_rows %d)", R_max);
   if (trace && trace->n_rows) trace->n_rows[0] = rw.n, trace->n_rows[1] = 0;
@@ -178,10 +190,7 @@ extern "C" fdl_status fdl_flash_step(fdl_ctx* ctx, const fdl_model* m, const voi
     }
   }
   const int RW = (int)win_idx.size();
-  if (RW < 1 || RW > B * W) {
-    std::copy(state_before.begin(), state_before.end(), s->state);
-    return loop_fail(ctx, FDL_ERR_INVALID_ARG, "fdl_flash_step: %d window rows", RW);
-  }
+  if (RW < 1 || RW > B * W) return loop_fail(ctx, FDL_ERR_INVALID_ARG, "fdl_flash_step: %d window rows", RW);
   FDL_CU(h2d(d.seq, rw.seq.data(), rw.n * 4));
   FDL_CU(h2d(d.rope, rw.rope.data(), rw.n * 4));
   FDL_CU(h2d(d.kind, rw.kind.data(), rw.n * 4));
@@ -246,9 +255,9 @@ extern "C" fdl_status fdl_flash_step(fdl_ctx* ctx, const fdl_model* m, const voi
     }
     Rows vr;
     vr.resize(R_max, B);
-    FDL_TRY(fdl_verify_rows(B, s->seq_len, s->tracked, BT, s->n_tracked, spos.data(), MS, ns_host.data(),
-                            BT + W, R_max, vr.seq.data(), vr.rope.data(), vr.cache.data(), vr.kind.data(),
-                            vr.cu.data(), &vr.n));
+    rc = fdl_verify_rows(B, s->seq_len, s->tracked, BT, s->n_tracked, spos.data(), MS, ns_host.data(), BT + W,
+                         R_max, vr.seq.data(), vr.rope.data(), vr.cache.data(), vr.kind.data(), vr.cu.data(), &vr.n);
+    if (rc != FDL_OK) return loop_fail(ctx, rc, "fdl_flash_step: verify rows rejected (max_rows %d)", R_max);
     std::vector<int> gidx((size_t)B * MS, -1);
     for (int r = 0; r < vr.n; ++r) {
       const int b = vr.seq[r], k = vr.kind[r];
@@ -295,6 +304,7 @@ extern "C" fdl_status fdl_flash_step(fdl_ctx* ctx, const fdl_model* m, const voi
   }
 
   // ---- decode, then the next tracked set from the draft forward's tracker
+  guard.done = true;  // from here on the step updates the sequences
   std::vector<std::vector<int>> fresh(B);
   for (int b = 0; b < B; ++b) {
     std::vector<std::pair<int, int>> c, a;
