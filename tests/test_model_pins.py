@@ -3,7 +3,9 @@
 RMSNorm and SiLU against hand values and a library routine; a full-refresh
 forward through the cache machinery (paged, permuted pages) against a plain
 dense transformer computed without any cache; the exactness of a selective
-refresh whose tokens did not change; and a network whose blocks add nothing.
+refresh whose tokens did not change; a network whose blocks add nothing; and,
+for one layer, the verify forward's extreme views against plain forwards
+with the search positions all drafted or all masked.
 """
 import math
 
@@ -108,3 +110,48 @@ def test_model_case_recipe():
     assert abs(m["layers"][0]["w_qkv"].std() - 0.02) < 1e-3
     g = m["layers"][1]["g_mlp"]
     assert g.min() >= 0.79 and g.max() <= 1.21
+
+
+def test_verify_views_equal_plain_forwards_for_one_layer():
+    # With one layer, a key depends only on its own token, so the verify
+    # forward's views reduce to plain bidirectional forwards: the last draft
+    # view sees every search position's draft (and no mask view), the first
+    # mask view sees every search position masked.
+    from oracle import refresh as rf
+    m = synth.model_values(synth.model_case(seed=9, d=64, n_heads=2, n_layers=1, ffn=64, vocab=40,
+                                            out_std=0.5, lm_std=0.2))
+    mask_id = 39
+    n, prompt = 30, 12
+    rng = np.random.default_rng(10)
+    tokens = np.full(n, mask_id)
+    tokens[:prompt] = rng.integers(0, mask_id, prompt)
+    tokens[[14, 20]] = [5, 7]                                # two decoded generated positions
+    search = [17, 13, 25]                                    # in acceptance order
+    drafts = [3, 11, 29]
+    views = 2 * len(search)
+    geom = synth.flat_geometry(1, n + views)
+    z = [np.zeros((n + views, 64))]
+    # the draft forward over every position fills the cache
+    full, kc, vc, _ = _forward(m, tokens, _full_rows(n), geom, z, [z[0].copy()], dtype="f32")
+    # verify forward: two tracked rows, then the views
+    vrows = rf.verify_rows([14, 3], search, n, query_budget=8)
+    v_seq = np.zeros(len(vrows), np.int32)
+    v_rope = np.array([r[0] for r in vrows], np.int32)
+    v_cache = np.array([r[1] for r in vrows], np.int32)
+    v_kind = np.array([r[2] for r in vrows], np.int32)
+    v_tok = np.array([tokens[p] if k < 2 else (drafts[(k - 2) // 2] if k % 2 == 0 else mask_id)
+                      for p, _, k in vrows])
+    out, _, _, _ = om.model_forward(m, v_tok, v_seq, v_rope, v_cache, v_kind, np.array([0, len(vrows)], np.int32),
+                                    np.array([n]), geom.block_table, geom.page_size, kc, vc, "f32",
+                                    search_pos=np.array([search]), n_search=np.array([len(search)]))
+    filled = tokens.copy()
+    filled[search] = drafts
+    last_draft = [i for i, (_, _, k) in enumerate(vrows) if k == 2 + 2 * (len(search) - 1)][0]
+    first_mask = [i for i, (_, _, k) in enumerate(vrows) if k == 3][0]
+    np.testing.assert_allclose(out[last_draft], om.dense_forward(m, filled)[search[-1]], atol=2e-5, rtol=0)
+    np.testing.assert_allclose(out[first_mask], om.dense_forward(m, tokens)[search[0]], atol=2e-5, rtol=0)
+    # the tracked rows are the plain forward's too (they see base keys only)
+    np.testing.assert_allclose(out[0], om.dense_forward(m, tokens)[14], atol=2e-5, rtol=0)
+    # and a middle draft view differs from both extremes (it sees a mix)
+    mid = [i for i, (_, _, k) in enumerate(vrows) if k == 4][0]
+    assert np.abs(out[mid] - om.dense_forward(m, tokens)[search[1]]).max() > 1e-3
