@@ -32,7 +32,11 @@
  *                             draft forward
  *   fdl_verify_rows           (host) the query rows of a Flash-Verify forward
  *
- * Conventions shared by every entry point (but the two host row builders)
+ * Conventions shared by every entry point (exceptions: the two host row
+ * builders take and return host arrays and touch no device; fdl_flash_step
+ * keeps its sequences' state in host arrays and synchronises the stream;
+ * the per-layer pointer arrays of fdl_model_forward and fdl_flash_step are
+ * host arrays of device pointers)
  *   - All tensor arguments are DEVICE pointers owned by the caller (for
  *     example PyTorch allocations); the library never frees them.
  *   - Every call is asynchronous on the context's CUDA stream.
@@ -47,7 +51,9 @@
  *     FDL_ERR_DEVICE_INDEX or FDL_ERR_TIMEOUT.
  *   - Floating-point tensors use the context dtype (FDL_F32 or FDL_BF16);
  *     accumulation is fp32. Index tensors are int32, masks are uint8.
- *   - A context is not thread-safe; use one per host thread.
+ *   - A context is not thread-safe, and calls on one context must not overlap
+ *     on the GPU (they share its workspace): use one context per host thread
+ *     and one per stream when calls run concurrently.
  */
 #ifndef FDL_H_
 #define FDL_H_
