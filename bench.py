@@ -87,8 +87,11 @@ class Clocks:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
+        self.lines = []
+        self.reader = None
 
     def __enter__(self):
+        import threading
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
@@ -96,17 +99,30 @@ class Clocks:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+        if self.proc:
+            def read():
+                for line in self.proc.stdout:
+                    self.lines.append(line)
+            self.reader = threading.Thread(target=read, daemon=True)
+            self.reader.start()
         return self
 
+    def wait_live(self, timeout_s: float):
+        """Waits (up to timeout_s) until the sampler has printed a sample."""
+        end = time.perf_counter() + timeout_s
+        while self.proc and not self.lines and time.perf_counter() < end and self.proc.poll() is None:
+            time.sleep(0.01)
+
     def __exit__(self, *exc):
-        self.out = ""
         if self.proc:
             self.proc.terminate()
             try:
-                self.out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                self.out = ""
+            if self.reader:
+                self.reader.join(timeout=5)
+        self.out = "".join(self.lines)
 
     def summary(self):
         sm, mx, reasons = [], [], set()
@@ -126,6 +142,63 @@ class Clocks:
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+class Nvml:
+    """SM clock and throttle reasons read straight from the driver's NVML
+    library (libnvidia-ml, part of the driver) through ctypes: one read takes
+    microseconds, so it can bracket a timed region closely. Only queries;
+    nothing is set."""
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+               0x4: "sw_power_cap"}
+
+    def __init__(self, index: int):
+        import ctypes
+        self.ok = False
+        try:
+            self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.lib.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            if self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h)) != 0:
+                return
+            self.ok = True
+        except OSError:
+            pass
+
+    def read(self):
+        import ctypes
+        if not self.ok:
+            return None
+        mhz, mx, why = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(mhz)) != 0:   # NVML_CLOCK_SM
+            return None
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))
+        reasons = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(self.lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        reasons(self.h, ctypes.byref(why))
+        return {"sm_mhz": int(mhz.value), "sm_max_mhz": int(mx.value),
+                "reasons": sorted(n for bit, n in self.REASONS.items() if why.value & bit)}
+
+
+def clock_record(clk, before, after):
+    """The line's clocks: the sampler's median SM clock and reasons over the
+    loaded window, plus the NVML reads that bracket the timed steps."""
+    rec = clk.summary()
+    rec["nvml_before_timed"] = before
+    rec["nvml_after_timed"] = after
+    reasons = set(rec["reasons"])
+    for r in (before, after):
+        if r:
+            reasons.update(r["reasons"])
+    rec["reasons"] = sorted(reasons)
+    if rec["sm_mhz"] is None and before and after:
+        rec["sm_mhz"] = (before["sm_mhz"] + after["sm_mhz"]) / 2
+        rec["sm_max_mhz"] = max(before["sm_max_mhz"], after["sm_max_mhz"])
+    rec["how"] = ("nvidia-smi every 50 ms from an untimed 0.3 s pre-roll under load through the warm-ups, the "
+                  "timed steps and the roofline replays (sm_mhz = median of those samples); NVML SM clock and "
+                  "reasons read immediately before and after the timed steps")
+    return rec
 
 
 def dist_init():
@@ -206,6 +279,52 @@ def cpu_leg(wl, budget_s: float):
     return done / dt, steps, dt
 
 
+def flash_verify_oracle_sample(fv, budget_s: float):
+    """Times the oracle on a bounded sample of the Flash-Verify stress
+    layer-step: the draft forward's layer for its first sequence (32 window +
+    32 tracked rows against that sequence's 1536 cached keys), that
+    sequence's top-32 and the eps unmasking of its 32 window rows over the
+    126464-entry vocabulary, repeated for about budget_s."""
+    import oracle
+    e, s, g = fv.extra, fv.shape, fv.geom
+    rows = e["rows"]
+    n = int(rows.cu_seqlens[1])
+    slots = g.page_size
+    w = e.setdefault("w_vals", e["w"].values())
+    kc = e["k_cache"].values()[:slots]
+    vc = e["v_cache"].values()[:slots]
+    x = e["x"].values()[:n]
+    logits = e["logits"].values()[:32]
+    bt = np.zeros((1, 1), np.int32)
+    done, steps, t0 = 0, 0, time.perf_counter()
+    while True:
+        q, kc2, vc2 = oracle.qkv_rope_cache_write(
+            x, w, s.n_heads, s.head_dim, s.rope_theta, rows.row_rope_pos[:n], np.zeros(n, np.int32),
+            rows.row_cache_pos[:n], bt, slots, kc, vc, s.dtype)
+        _, _, tr = oracle.sched_attn(q, kc2, vc2, bt, slots, np.array([0, n], np.int32), fv.seq_len[:1],
+                                     rows.row_kind[:n], max_seq=fv.max_seq, dtype=s.dtype)
+        oracle.track_topk(tr.astype(np.float32), e["eligible"][:1], fv.seq_len[:1], e["topk"])
+        oracle.unmask(logits, np.zeros(32, np.int32), e["window_pos"], 1, e["eps"], False, e["max_search"])
+        done += n
+        steps += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    return done / (time.perf_counter() - t0), steps, time.perf_counter() - t0
+
+
+def cpu_leg_subprocess(budget_s: float, threads: int):
+    """cpu_leg in a fresh interpreter whose BLAS and OpenMP pools are held to
+    `threads` threads (set before numpy loads)."""
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[k] = str(threads)
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-leg", "--cpu-seconds", str(budget_s)],
+                       env=env, capture_output=True, text=True, timeout=600)
+    if r.returncode != 0:
+        return None
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
 def run_reference(args, world, rank):
     """The oracle as the reference arm: W untimed steps, then exactly K timed
     steps, each a bounded sample of the layer-step (its first r of the 64
@@ -223,7 +342,8 @@ def run_reference(args, world, rank):
     R = e["rows"].n_rows
     t0 = time.perf_counter()
     oracle_step(wl, R)                                  # calibration, untimed
-    per_row = (time.perf_counter() - t0) / R
+    full_step_s = time.perf_counter() - t0
+    per_row = full_step_s / R
     K = args.steps
     r = int(max(1, min(R, 60.0 / (K * per_row))))
     for _ in range(args.warmup):
@@ -237,10 +357,15 @@ def run_reference(args, world, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "query-rows/s", "n_gpus": args.gpus,
         "steps": K, "warmup": args.warmup, "ms_per_step": 1e3 * dt / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "global_batch": 1, "seq_len": 768, "rows_per_step": 64},
+        "config": {"workload": WORKLOAD, "global_batch": 1, "seq_len": 768, "rows_per_step": 64,
+                   "rows_per_timed_sample": r,
+                   "ms_per_step_is": f"the time of one {r}-row sample of the 64-row layer-step",
+                   "full_64_row_step_ms": 1e3 * full_step_s},
         "cpu_baseline": {"value": value, "unit": "query-rows/s", "cores": cores, "kind": "oracle",
+                         "rows_per_sample": r,
                          "sample": f"{K} layer-steps of the float64 numpy oracle, each over the first {r} of "
-                                   f"the 64 query rows (the whole K-step run {dt:.1f} s)"},
+                                   f"the 64 query rows (the whole K-step run {dt:.1f} s); one untimed full "
+                                   f"64-row step took {1e3 * full_step_s:.0f} ms"},
         "e2e": {"value": value, "unit": "query-rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -364,35 +489,50 @@ def run_gpu(args, world, rank, local):
     with torch.cuda.graph(qkv_graph, stream=stream):
         for c in range(n_copies):
             qkv_part(c)
-    for i in range(args.warmup):
-        step_graphs[i % n_copies].replay()
-    qkv_graph.replay()
-    ctx.sync_status()
-    ctx_side.sync_status()
     K = args.steps
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
+    nvml = Nvml(local)
+    n_qkv = max(20, K // n_copies)
+    q0e, q1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # The nvidia-smi sampler runs from before a short untimed pre-roll (so
+    # that it is live and the clocks have settled under load) through the
+    # warm-ups, the timed steps and the roofline replays; NVML reads taken
+    # right before and right after the timed steps bracket them closely even
+    # when they last only a millisecond.
     with Clocks(local) as clk:
+        clk.wait_live(5.0)
+        pre_end, i = time.perf_counter() + 0.3, 0
+        while time.perf_counter() < pre_end:
+            for _ in range(50):
+                step_graphs[i % n_copies].replay()
+                i += 1
+            torch.cuda.synchronize()
+        for i in range(args.warmup):
+            step_graphs[i % n_copies].replay()
+        qkv_graph.replay()
+        ctx.sync_status()
+        ctx_side.sync_status()
+        barrier(world)
+        torch.cuda.synchronize()
+        nv_before = nvml.read()
         t0.record(stream)
         for i in range(K):
             step_graphs[i % n_copies].replay()
         t1.record(stream)
         torch.cuda.synchronize()
-    barrier(world)
-    ctx.sync_status()
-    ctx_side.sync_status()
+        nv_after = nvml.read()
+        barrier(world)
+        ctx.sync_status()
+        ctx_side.sync_status()
+        q0e.record(stream)
+        for i in range(n_qkv):
+            qkv_graph.replay()
+        q1e.record(stream)
+        torch.cuda.synchronize()
     ms_total = t0.elapsed_time(t1)
     ms_total = max_over_ranks(ms_total, world)
     ms_step = ms_total / K
     value = whole_job_rate(R, K, ms_total, world)
-    n_qkv = max(1, K // n_copies)
-    q0e, q1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    q0e.record(stream)
-    for i in range(n_qkv):
-        qkv_graph.replay()
-    q1e.record(stream)
-    torch.cuda.synchronize()
     qkv_ms = [q0e.elapsed_time(q1e) / (n_qkv * n_copies)]
     qkv_timing = (f"CUDA events over {n_qkv * n_copies} back-to-back graph launches of the projection "
                   f"(rotating copies), right after the timed steps")
@@ -450,14 +590,36 @@ def run_gpu(args, world, rank, local):
                      "unit": "GB/s", "frac": achieved / hbm, "traffic": qkv_traffic(), "peak_source": src,
                      "algorithmic_bytes": qkv_bytes, "avg_launch_us": qkv_avg * 1e3,
                      "timing": qkv_timing},
-        "clocks": clk.summary(),
+        "clocks": clock_record(clk, nv_before, nv_after),
     }
+    if not args.no_configs:
+        # kernel fractions on the other configurations (ragged batch, one
+        # layer of the 32-layer chain, Flash-Verify stress), a few seconds of
+        # GPU time, so that they are recorded with the headline
+        fv = synth.flash_verify()
+        cfgs = config_results(("ragged", "chain", "flash_verify"), reps_scale=0.5, workloads={"flash_verify": fv})
+        line["configs"] = {r.pop("config"): {k: v for k, v in r.items() if k != "peaks"} for r in cfgs}
+    else:
+        fv = None
     if not args.no_cpu_baseline:
         cpu_value, cpu_steps, cpu_dt = cpu_leg(wl, args.cpu_seconds)
         line["cpu_baseline"] = {"value": cpu_value, "unit": "query-rows/s", "cores": os.cpu_count(),
-                                "kind": "oracle",
+                                "threads": "numpy default (all cores for BLAS)", "kind": "oracle",
                                 "sample": f"{cpu_steps} full layer-steps (64 rows) of the float64 numpy oracle "
                                           f"in {cpu_dt:.1f} s"}
+        one = cpu_leg_subprocess(args.cpu_seconds, 1)
+        if one:
+            line["cpu_baseline"]["one_thread"] = {
+                "value": one["value"], "unit": "query-rows/s", "threads": 1,
+                "sample": f"{one['steps']} full layer-steps (64 rows) in {one['dt']:.1f} s, BLAS and OpenMP "
+                          f"pools held to one thread"}
+        if fv is not None:
+            v, n, dt = flash_verify_oracle_sample(fv, args.cpu_seconds / 2)
+            line["cpu_baseline"]["flash_verify_sample"] = {
+                "value": v, "unit": "query-rows/s", "cores": os.cpu_count(),
+                "sample": f"{n} repetitions in {dt:.1f} s of one sequence of the Flash-Verify stress layer-step "
+                          f"(64 draft rows: projection, attention over 1536 keys with the tracker, top-32, eps "
+                          f"unmasking of 32 rows over 126464 logits); a sample, not the 32-sequence step"}
     print(json.dumps(line), flush=True)
 
 
@@ -468,6 +630,13 @@ CONFIG_SECTIONS = ("ragged", "chain", "flash_verify", "lm_head", "refresh", "fla
 
 
 def run_configs(args):
+    """Prints one JSON line per configuration of config_results."""
+    sections = CONFIG_SECTIONS if args.configs == "all" else (args.configs,)
+    for r in config_results(sections):
+        print(json.dumps(r), flush=True)
+
+
+def config_results(sections, reps_scale: float = 1.0, workloads=None):
     """Times each kernel of the path on the ragged batch, one layer of the
     32-layer chain and the Flash-Verify stress workload, and the fused LM
     head + unmasking over the LLaDA vocabulary: CUDA-graph replays of one
@@ -475,7 +644,7 @@ def run_configs(args):
     peaks. Then one layer's projection + attention over a whole scripted
     decode under each KV-cache refresh policy, against the sum of the
     per-kernel roofline floors, and whole denoising steps of a 32-layer
-    LLaDA-8B-shaped model. Prints one JSON line per configuration."""
+    LLaDA-8B-shaped model. Returns one dict per configuration."""
     import torch
 
     import kv_cache_attention_gb300 as fdl
@@ -495,6 +664,7 @@ def run_configs(args):
 
     def timed(fns, reps):
         """Average µs of one call; fns rotate over input copies, one per graph."""
+        reps = max(len(fns), int(reps * reps_scale))
         graphs = []
         for fn in fns:
             g = torch.cuda.CUDAGraph()
@@ -551,10 +721,9 @@ def run_configs(args):
         return out
 
     results = []
-    only = args.configs if args.configs != "all" else None
 
     def want(name):
-        return only is None or only == name
+        return name in sections
 
     if want("ragged"):
         # ragged batch of 16 (paged cache, half full refresh)
@@ -592,7 +761,7 @@ def run_configs(args):
 
     if want("flash_verify"):
         # Flash-Verify stress: draft forward, eps unmasking, verify acceptance, top-k
-        wl = synth.flash_verify()
+        wl = (workloads or {}).get("flash_verify") or synth.flash_verify()
         e, s, g = wl.extra, wl.shape, wl.geom
         rows = e["rows"]
         B, ms, V = wl.batch, e["max_search"], e["vocab"]
@@ -803,7 +972,8 @@ def run_configs(args):
     for r in results:
         r.setdefault("timing", "CUDA-graph replays of one call on the dedicated stream; algorithmic work")
         r["peaks"] = {"hbm_gbs": hbm, "bf16_tflops": tc, "source": src}
-        print(json.dumps(r), flush=True)
+    torch.cuda.synchronize()
+    return results
 
 
 def main():
@@ -814,6 +984,9 @@ def main():
     ap.add_argument("--impl", default="fdl", choices=["fdl", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="leave the other configurations' kernel fractions out of the headline line")
+    ap.add_argument("--cpu-leg", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--configs", nargs="?", const="all", default=None, metavar="SECTION",
                     help="time each kernel on the ragged-batch, 32-layer-chain and Flash-Verify workloads, "
                          "the fused LM head, one layer's decode under each KV-cache refresh policy and whole "
@@ -821,6 +994,13 @@ def main():
                          "lm_head, refresh, flash_step)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.cpu_leg:
+        # the oracle on the headline workload only (run in a subprocess with
+        # limited threads by cpu_leg_subprocess)
+        import synth
+        v, n, dt = cpu_leg(synth.llada_layer(), args.cpu_seconds)
+        print(json.dumps({"value": v, "steps": n, "dt": dt}), flush=True)
+        return
     if args.configs:
         if args.configs != "all" and args.configs not in CONFIG_SECTIONS:
             raise SystemExit(f"unknown configuration {args.configs!r}; one of {', '.join(CONFIG_SECTIONS)}")

@@ -123,6 +123,16 @@ int fdl_tile_m(const fdl_ctx* ctx);
 /* Number of int32 a worklist_out buffer needs for R rows over B sequences:
  * 1 (item count) + 4 per possible item. */
 int fdl_worklist_capacity(const fdl_ctx* ctx, int R, int B);
+/* Failure-path testing: sets the budget, in SM clock cycles, of every wait
+ * in the main loop of this context's tensor-core projection (the TMA ring's
+ * full/empty mbarriers). 0 restores the default of about 2 s, far above any
+ * legitimate wait. A budget shorter than a DRAM load makes the wait give up:
+ * the kernel then lets its loads in flight land, waits for its issued
+ * products, frees its TMEM, writes no output, keeps its split-K counters
+ * consistent and sets the device error word, so fdl_sync_status returns
+ * FDL_ERR_TIMEOUT and the context stays usable. The drain waits keep the
+ * default budget. Returns FDL_ERR_INVALID_ARG for a negative budget. */
+fdl_status fdl_set_wait_budget(fdl_ctx* ctx, long long cycles);
 
 /* ------------------------------------------------------------------------
  * Flash-Cache fused projection (paper digest, "Core method": QKV projection,
@@ -301,8 +311,9 @@ fdl_status fdl_lm_head_verify(fdl_ctx* ctx, const void* mask_hidden, const void*
  * 70 KB that every GPU loading the library holds until the process exits.
  *
  * Arguments and results are those of fdl_sched_attn (same kernels), with the
- * limits taken from *cfg (max_batch and max_rows are ignored; the call's B
- * and R apply) and the work list not exported. Limits of the static scratch:
+ * limits taken from *cfg and the work list not exported. *cfg is checked as
+ * fdl_create checks it, except max_batch, max_rows and vocab, which are
+ * ignored (the call's B and R apply). Limits of the static scratch:
  * B <= 1024 and ceil(R / fdl_tile_m) + B <= 4096 work items, where the tile
  * is 128 rows for bf16 contexts with head_dim 128 and 16 rows otherwise;
  * larger calls return FDL_ERR_INVALID_ARG (reason on stderr). Device-side
@@ -311,8 +322,9 @@ fdl_status fdl_lm_head_verify(fdl_ctx* ctx, const void* mask_hidden, const void*
  * word: 1 index, 2 timeout, 4 shape.
  *
  * The first call on a device looks up the scratch array's device address
- * (cudaGetSymbolAddress) and caches it; make that first call before any
- * stream capture. Every call on a device shares the array and rewrites all
+ * (cudaGetSymbolAddress) and caches it for the life of the process; make
+ * that first call before any stream capture, and do not use the library on
+ * a device after a cudaDeviceReset of it (the reset unloads the array). Every call on a device shares the array and rewrites all
  * of it that it reads; calls that overlap on the GPU (several streams or host
  * threads) race on it and must be serialised by the caller.
  * ---------------------------------------------------------------------- */

@@ -40,7 +40,7 @@ def FDL_KIND_MASK_VIEW(j: int) -> int:
 
 # Every symbol include/fdl.h declares.
 EXPORTS = (
-    "fdl_create", "fdl_destroy", "fdl_set_stream", "fdl_last_error", "fdl_sync_status",
+    "fdl_create", "fdl_destroy", "fdl_set_stream", "fdl_set_wait_budget", "fdl_last_error", "fdl_sync_status",
     "fdl_tile_m", "fdl_worklist_capacity", "fdl_qkv_rope_cache_write", "fdl_sched_attn",
     "fdl_track_topk", "fdl_unmask_verify", "fdl_sched_attn_noalloc", "fdl_lm_head_unmask",
     "fdl_refresh_rows", "fdl_verify_rows", "fdl_lm_head_verify", "fdl_model_workspace_bytes",
@@ -143,6 +143,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.fdl_destroy.restype = None
     L.fdl_set_stream.argtypes = [p, p]
     L.fdl_set_stream.restype = i
+    L.fdl_set_wait_budget.argtypes = [p, ctypes.c_longlong]
+    L.fdl_set_wait_budget.restype = i
     L.fdl_last_error.argtypes = [p]
     L.fdl_last_error.restype = ctypes.c_char_p
     L.fdl_sync_status.argtypes = [p]
@@ -230,6 +232,9 @@ class Context:
 
     def sync_status(self) -> None:
         self._check(load_library().fdl_sync_status(self.handle), "fdl_sync_status")
+
+    def set_wait_budget(self, cycles: int) -> None:
+        self._check(load_library().fdl_set_wait_budget(self.handle, int(cycles)), "fdl_set_wait_budget")
 
     def qkv_rope_cache_write(self, X, Wqkv, row_seq, row_rope_pos, row_cache_pos, block_table,
                              k_cache, v_cache, q_out) -> None:

@@ -1048,12 +1048,8 @@ cudaError_t fdl_launch_attn_tc(fdl_ctx* ctx, const void* q, const void* k_cache,
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) |
        reinterpret_cast<uintptr_t>(v_cache) | reinterpret_cast<uintptr_t>(o_out)) & 15)
     return cudaErrorMisalignedAddress;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static fdl_smem_limit smem_limit;
+  if (cudaError_t e = smem_limit.ensure((const void*)attn_tc_kernel, ctx->device, SMEM_BYTES)) return e;
   const int n_slots = c.n_pages * c.page_size;
   CUtensorMap mq, mk, mv;
   if (!map2d(&mq, q, R, c.d_model, kBM) || !map2d(&mk, k_cache, n_slots, c.d_model, kBN) ||

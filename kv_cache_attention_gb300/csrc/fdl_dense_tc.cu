@@ -249,13 +249,8 @@ template <int BN>
 cudaError_t launch(fdl_ctx* ctx, DenseParams p, const void* X, const void* W, int K) {
   using Cf = Cfg<BN>;
   static_assert(Cf::SMEM_BYTES <= 227 * 1024, "shared memory budget");
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(dense_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static fdl_smem_limit smem_limit;
+  if (cudaError_t e = smem_limit.ensure((const void*)dense_tc_kernel<BN>, ctx->device, Cf::SMEM_BYTES)) return e;
   CUtensorMap mw, mx;
   if (!dense_map(&mw, W, (uint64_t)p.N, (uint64_t)K, kBM) || !dense_map(&mx, X, (uint64_t)p.R, (uint64_t)K, BN))
     return cudaErrorInvalidValue;

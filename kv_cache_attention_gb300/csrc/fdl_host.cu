@@ -33,7 +33,9 @@ fdl_status launched(fdl_ctx* ctx, cudaError_t e, const char* what) {
   return FDL_OK;
 }
 
-bool config_ok(const fdl_config* c, char* why, size_t n) {
+}  // namespace
+
+bool fdl_config_ok(const fdl_config* c, char* why, size_t n) {
 #define FDL_REQ(cond, msg)          \
   if (!(cond)) {                    \
     snprintf(why, n, "%s", msg);    \
@@ -55,8 +57,6 @@ bool config_ok(const fdl_config* c, char* why, size_t n) {
   return true;
 }
 
-}  // namespace
-
 bool fdl_pdl_enabled() {
   static const bool on = [] {
     const char* v = getenv("FDL_DISABLE_PDL");
@@ -71,7 +71,7 @@ fdl_status fdl_create(const fdl_config* cfg, void* cuda_stream, fdl_ctx** out) {
   if (!cfg || !out) return FDL_ERR_INVALID_ARG;
   *out = nullptr;
   char why[256];
-  if (!config_ok(cfg, why, sizeof(why))) {
+  if (!fdl_config_ok(cfg, why, sizeof(why))) {
     fprintf(stderr, "fdl_create: %s\n", why);
     return FDL_ERR_INVALID_ARG;
   }
@@ -146,6 +146,13 @@ void fdl_destroy(fdl_ctx* ctx) {
 fdl_status fdl_set_stream(fdl_ctx* ctx, void* cuda_stream) {
   if (!ctx) return FDL_ERR_INVALID_ARG;
   ctx->stream = (cudaStream_t)cuda_stream;
+  return FDL_OK;
+}
+
+fdl_status fdl_set_wait_budget(fdl_ctx* ctx, long long cycles) {
+  if (!ctx) return FDL_ERR_INVALID_ARG;
+  if (cycles < 0) return fail(ctx, FDL_ERR_INVALID_ARG, "wait budget must be >= 0");
+  ctx->wait_budget = cycles;
   return FDL_OK;
 }
 

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/fdl.h"
 
 // Device error-word bits (fdl_sync_status maps them to fdl_status).
@@ -37,6 +39,7 @@ struct fdl_ctx {
   unsigned* qkv_ticket_buf;  // per-tile arrival counters (zero between calls)
   int qkv_tickets;
   float* lm_part;       // per-vocabulary-tile statistics of the fused LM head (bf16 contexts)
+  long long wait_budget;  // projection main-loop wait budget in cycles (0 = the default ~2 s)
   char last_error[512];
 };
 
@@ -135,6 +138,25 @@ cudaError_t fdl_launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size
   cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
+
+// Raises one kernel's dynamic shared-memory limit on the current device.
+// The attribute belongs to a device, so it is set once per device (one bit
+// per device ordinal below 64; higher ordinals set it on every launch).
+// cudaFuncSetAttribute is thread-safe and idempotent, so two host threads
+// that race here at most set it twice.
+struct fdl_smem_limit {
+  std::atomic<unsigned long long> done{0};
+  cudaError_t ensure(const void* kernel, int device, int bytes) {
+    const unsigned long long bit = device >= 0 && device < 64 ? 1ull << device : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+    return e;
+  }
+};
+
+// Checks a configuration as fdl_create does; false with the reason in `why`.
+bool fdl_config_ok(const fdl_config* c, char* why, size_t n);
 
 // Launchers implemented by the kernel translation units. Each returns a
 // cudaError_t from the launch.

@@ -37,7 +37,10 @@ std::mutex g_scratch_mu;
 
 // Device address of the scratch array on the current device. The name
 // g_attn_scratch in host code is only a host-side stand-in, so the address
-// is looked up once per device and cached.
+// is looked up once per device (on that device's first call) and cached for
+// the life of the process. A cudaDeviceReset unloads the module that holds
+// the array, so the library must not be used on a device after resetting it
+// (the same holds for every context created before the reset).
 cudaError_t scratch_address(int device, int** out) {
   if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
@@ -68,11 +71,17 @@ extern "C" fdl_status fdl_sched_attn_noalloc(const fdl_config* cfg, void* cuda_s
                                              float* track_scores, int track_ld, unsigned* device_error) {
   if (!cfg) return reject("NULL config");
   const fdl_config& c = *cfg;
-  if (c.n_heads <= 0 || c.d_model != c.n_heads * c.head_dim || (c.head_dim != 64 && c.head_dim != 128) ||
-      (c.dtype != FDL_F32 && c.dtype != FDL_BF16) || c.page_size <= 0 || c.n_pages <= 0 || c.max_seq <= 0 ||
-      c.max_views < 0 || c.max_views % 2 != 0 || c.max_views > 512)
-    return reject("inconsistent config (d_model, heads, head_dim, dtype, pages or views)");
   if (B < 0 || R < 0) return reject("negative B or R");
+  {
+    // the checks fdl_create makes, except the limits that size a context's
+    // workspace (max_batch, max_rows, vocab): this call has none
+    fdl_config cc = c;
+    cc.max_batch = 1;
+    cc.max_rows = 1;
+    cc.vocab = 1;
+    char why[256];
+    if (!fdl_config_ok(&cc, why, sizeof(why))) return reject(why);
+  }
   if (B == 0 || R == 0) return FDL_OK;
   if (B > kMaxSeqs) return reject("B exceeds the 1024 sequences the static scratch holds");
   const int tile = fdl_attn_tc_supported(c) ? FDL_TILE_M_TC : FDL_TILE_M_SIMT;

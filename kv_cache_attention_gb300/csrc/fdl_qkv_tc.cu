@@ -67,6 +67,7 @@ struct TcParams {
   float* partials;     // [tiles * ksplit][BN][128] fp32 split-K partial tiles
   unsigned* tickets;   // [tiles] arrival counters, zero between launches
   unsigned* err;
+  long long wait_budget;  // cycles of the main loop's mbarrier waits
 };
 
 template <int BN>
@@ -140,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, BN == 64 ? 2 : 1)
       for (int kb = kb0 + pre; kb < kb1; ++kb, ++it) {
         const int s = it % C::STAGES;
         const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
-        if (!tc::mbar_wait(&empty[s], ph ^ 1u, abort_flag)) break;
+        if (!tc::mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.wait_budget)) break;
         uint8_t* a = pipe + s * C::STAGE_BYTES;
         tc::mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
         tc::tma_load_2d(a, &tmap_w, kb * kBK, f0, &full[s]);
@@ -164,7 +165,7 @@ __global__ void __launch_bounds__(kThreads, BN == 64 ? 2 : 1)
       for (int kb = kb0; kb < kb1; ++kb, ++it) {
         const int s = it % C::STAGES;
         const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
-        if (!tc::mbar_wait(&full[s], ph, abort_flag)) break;
+        if (!tc::mbar_wait(&full[s], ph, abort_flag, p.wait_budget)) break;
         tc::fence_after_sync();
         const uint32_t a = tc::smem_addr(pipe + s * C::STAGE_BYTES);
         const uint64_t ad = tc::desc_kmajor_sw128(a);
@@ -175,6 +176,11 @@ __global__ void __launch_bounds__(kThreads, BN == 64 ? 2 : 1)
         tc::mma_commit(&empty[s]);
       }
       tc::mma_commit(tmem_full);
+      // every product issued has finished before the CTA barrier below, also
+      // when the loop above gave up (the TMEM is freed after that barrier)
+      long long t0 = clock64();
+      while (!tc::mbar_try_wait(tmem_full, 0) && clock64() - t0 < tc::kWaitBudgetCycles) {
+      }
     }
     __syncwarp();
   } else {
@@ -203,17 +209,20 @@ __global__ void __launch_bounds__(kThreads, BN == 64 ? 2 : 1)
       col_pos[c] = pos;
       col_dst[c] = pos >= 0 ? dst : -1;
     }
-    tc::named_bar(1, kEpiThreads);
-    tc::mbar_wait(tmem_full, 0, abort_flag);
-    tc::fence_after_sync();
   }
+  // After this barrier every load has landed (or been drained), every
+  // product has finished and no thread waits on a barrier again, so the
+  // abort flag is final and every thread reads the same value.
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const bool ok = !*abort_flag;
 
   const int q = warp & 3;          // TMEM lane quadrant of this warp
   const int t = q * 32 + lane;     // tile row = output feature f0 + t
   const uint32_t t_lane = tmem + ((uint32_t)(q * 32) << 16);
-  const bool epi = warp >= 2 && !*abort_flag;
 
-  if (epi) {
+  if (warp >= 2) {
     const int half = p.hd / 2;
     const int i = (f0 + t) % p.hd;
     const int jj = i % half;
@@ -263,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, BN == 64 ? 2 : 1)
     };
 
     if (ks == 1) {
-      for (int c0 = 0; c0 < BN; c0 += CH) {
+      for (int c0 = 0; ok && c0 < BN; c0 += CH) {
         float v[CH];
         load_rotated(c0, v);
 #pragma unroll
@@ -272,9 +281,11 @@ __global__ void __launch_bounds__(kThreads, BN == 64 ? 2 : 1)
         store_rows(c0, CH);
       }
     } else {
-      // publish this split's rotated partial tile, then take a ticket
+      // publish this split's rotated partial tile, then take a ticket (a
+      // split that gave up publishes nothing but still takes its ticket, so
+      // the counter is back at zero for the next launch)
       float* mine = p.partials + ((size_t)tile_lin * ks + rank) * BN * kBM;
-      for (int c0 = 0; c0 < BN; c0 += CH) {
+      for (int c0 = 0; ok && c0 < BN; c0 += CH) {
         float v[CH];
         load_rotated(c0, v);
 #pragma unroll
@@ -291,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, BN == 64 ? 2 : 1)
         }
       }
       tc::named_bar(1, kEpiThreads);
-      if (*is_last) {
+      if (*is_last && ok) {
         // sum the ks rotated partials in split order (all loads of a chunk
         // in flight together), round to bf16 and store
         const float* parts = p.partials + (size_t)tile_lin * ks * BN * kBM;
@@ -357,12 +368,8 @@ template <int BN>
 cudaError_t launch(fdl_ctx* ctx, const TcParams& p0, const void* X, const void* W) {
   static_assert(Cfg<BN>::SMEM_BYTES <= 227 * 1024, "shared memory budget");
   using Cf = Cfg<BN>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(qkv_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static fdl_smem_limit smem_limit;
+  if (cudaError_t e = smem_limit.ensure((const void*)qkv_tc_kernel<BN>, ctx->device, Cf::SMEM_BYTES)) return e;
   const fdl_config& c = ctx->cfg;
   CUtensorMap mw, mx;
   if (!make_map(&mw, W, (uint64_t)3 * c.d_model, c.d_model, kBM) || !make_map(&mx, X, p0.R, c.d_model, BN))
@@ -421,6 +428,7 @@ cudaError_t fdl_launch_qkv_tc(fdl_ctx* ctx, const void* X, const void* W, int R,
   p.rope_sin = ctx->rope_sin;
   p.rope_positions = ctx->rope_positions;
   p.err = ctx->err_word;
+  p.wait_budget = ctx->wait_budget > 0 ? ctx->wait_budget : tc::kWaitBudgetCycles;
   if (R <= 64) return launch<64>(ctx, p, X, W);
   if (R <= 128) return launch<128>(ctx, p, X, W);
   return launch<256>(ctx, p, X, W);

@@ -868,12 +868,8 @@ cudaError_t fdl_launch_lm_head(fdl_ctx* ctx, const void* hidden, const void* w_l
   if (c.dtype != FDL_BF16 || R < 1 || R > kLmBN || c.d_model % kLmBK != 0 || !ctx->lm_part)
     return cudaErrorNotSupported;
   if ((reinterpret_cast<uintptr_t>(hidden) | reinterpret_cast<uintptr_t>(w_lm)) & 15) return cudaErrorMisalignedAddress;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(lm_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kLmSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static fdl_smem_limit smem_limit;
+  if (cudaError_t e = smem_limit.ensure((const void*)lm_head_kernel, ctx->device, kLmSmem)) return e;
   CUtensorMap mw, mh;
   if (!lm_map(&mw, w_lm, (uint64_t)c.vocab, c.d_model, kLmBM) || !lm_map(&mh, hidden, R, c.d_model, kLmBN))
     return cudaErrorInvalidValue;

@@ -47,13 +47,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for the phase of `parity` to complete; false if the budget ran out
-// or `abort` (shared flag) was raised by another thread.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+// Non-blocking test of the phase of `parity`.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase of `parity` to complete; false if the budget (in
+// cycles) ran out or `abort` (shared flag) was raised by another thread.
+// A budget other than the default polls with the non-blocking test, so that
+// a budget shorter than try_wait's own suspend time is still honoured.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          long long budget = kWaitBudgetCycles) {
   long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
+  const bool poll = budget != kWaitBudgetCycles;
+  while (!(poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity))) {
     if (*abort) return false;
-    if (clock64() - t0 > kWaitBudgetCycles) {
+    if (clock64() - t0 > budget) {
       *abort = 1;
       return false;
     }

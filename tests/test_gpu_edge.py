@@ -190,3 +190,47 @@ def test_unmask_ties_and_forced_progress_per_sequence():
         assert H.host(sr).tolist() == u["search_rows"].tolist()
         assert H.host(ns).tolist() == u["n_search"].tolist()
     ctx.close()
+
+
+def _projection(ctx, wl):
+    e, s, g = wl.extra, wl.shape, wl.geom
+    rows = e["rows"]
+    kc, vc = H.dev(e["k_cache"]), H.dev(e["v_cache"])
+    q = H.empty((rows.n_rows, s.n_heads, s.head_dim), s.dtype)
+    ctx.qkv_rope_cache_write(H.dev(e["x"]), H.dev(e["w"]), H.ints(rows.row_seq), H.ints(rows.row_rope_pos),
+                             H.ints(rows.row_cache_pos), H.ints(g.block_table), kc, vc, q)
+    return q, kc, vc
+
+
+def test_bounded_wait_runs_out_and_the_context_stays_usable():
+    """A main-loop wait budget of 300 cycles is far shorter than a DRAM load,
+    so the tensor-core projection's first wait gives up: the kernel drains
+    its loads, writes nothing and reports FDL_ERR_TIMEOUT through the error
+    word. With the default budget restored, the next call on the same
+    context (same split-K counters) matches the oracle."""
+    import kv_cache_attention_gb300 as fdl
+    wl = synth.projection_case(seed=7301, d_model=512, n_heads=4, n_rows=64)
+    e, s, g = wl.extra, wl.shape, wl.geom
+    rows = e["rows"]
+    ctx = fdl.fdl_create(s.d_model, s.n_heads, s.head_dim, s.rope_theta, wl.batch, wl.max_seq, 0,
+                         g.page_size, g.n_pages, rows.n_rows, 16, s.dtype)
+    with pytest.raises(fdl.FdlError) as ei:
+        ctx.set_wait_budget(-1)
+    assert ei.value.status == fdl.FDL_ERR_INVALID_ARG
+    ctx.set_wait_budget(300)
+    _projection(ctx, wl)
+    with pytest.raises(fdl.FdlError) as ei:
+        ctx.sync_status()
+    assert ei.value.status == fdl.FDL_ERR_TIMEOUT
+    ctx.set_wait_budget(0)
+    for _ in range(2):
+        q, kc, vc = _projection(ctx, wl)
+        ctx.sync_status()
+        q_o, kc_o, vc_o = oracle.qkv_rope_cache_write(
+            e["x"].values(), e["w"].values(), s.n_heads, s.head_dim, s.rope_theta, rows.row_rope_pos,
+            rows.row_seq, rows.row_cache_pos, g.block_table, g.page_size, e["k_cache"].values(),
+            e["v_cache"].values(), s.dtype)
+        H.assert_close(H.host(q), q_o, s.dtype, "q_out after a timed-out call")
+        H.assert_close(H.host(kc), kc_o, s.dtype, "k_cache after a timed-out call")
+        H.assert_close(H.host(vc), vc_o, s.dtype, "v_cache after a timed-out call")
+    ctx.close()
