@@ -8,12 +8,12 @@ GPU consumes exactly the oracle's inputs (its stored caches and Q, its
 float32 scores) so each kernel is held to the stage tolerances, and the
 tracked sets feeding the next step are identical on both sides.
 
-test_chain_full_size: the full 32 layers x 16 steps on the GPU alone, checked
-by properties that hold at any size: every sequence's scores sum to the
-number of layers, top-32 equals a full sort of the scores the kernel got,
-sampled projection rows match the oracle, and a teacher-forced re-run gives
-the same scores to within fp32 reassociation and the same tracked sets
-wherever their cut is not a near-tie."""
+test_chain_full_size: the full 32 layers x 16 steps (after the init
+forward), teacher-forced stage by stage: layers 0, 15 and 31 of every step
+compared in full, a seeded 5% of the rows of every other layer, the total
+tracker mass and the top-32 of every step; then a re-run fed the first run's
+tracked sets gives the same scores to within fp32 reassociation and the same
+tracked sets wherever their cut is not a near-tie."""
 import numpy as np
 import pytest
 
@@ -105,6 +105,19 @@ def test_chain_teacher_forced():
 
 @pytest.mark.slow
 def test_chain_full_size():
+    """All 32 layers x (init + 16 steps), teacher-forced layer by layer: the
+    oracle of each checked stage gets the GPU's own inputs to it (the caches
+    before the projection, then Q and the caches after it), and the chain
+    follows the GPU's tracked sets.
+
+    Layers 0, 15 and 31 of every step are compared in full: every Q row, every
+    written K/V slot, every O row, the LSE and the layer's tracker increment.
+    Every other layer compares a seeded 5% of its rows, drawn from two seeded
+    sequences: their Q, their K/V slots, their O and LSE (the tracker
+    increment needs all of a sequence's window rows, so it is compared at the
+    full layers, and its layer sum through the total mass). After each step:
+    every sequence's scores sum to the number of layers, and the top-32 equals
+    a full sort of the scores the kernel produced."""
     import torch
     L, S = 32, 16
     wl, ctx = _setup(L, S)
@@ -114,10 +127,14 @@ def test_chain_full_size():
     bt = H.ints(g.block_table)
     kv_len = H.ints(wl.seq_len)
     n_slots = g.n_pages * g.page_size
-    W = [H.dev(synth.chain_weight(seed, l, d)) for l in range(L)]
+    P = g.page_size
+    Wt = [synth.chain_weight(seed, l, d) for l in range(L)]
+    W = [H.dev(t) for t in Wt]
+    W32 = [t.values().astype(np.float32) for t in Wt]      # exact: bf16 values
+    del Wt
     elig = H.u8(e["eligible"])
     k = e["topk"]
-    sample_layers = (0, 15, 31)
+    full_layers = (0, 15, 31)
 
     def run(check, forced=None):
         caches = [(torch.zeros((n_slots, d), dtype=torch.bfloat16, device="cuda"),
@@ -131,23 +148,71 @@ def test_chain_full_size():
                                   H.ints(rows.row_kind), H.ints(rows.cu_seqlens))
             q = H.empty((R, Hh, hd), dt)
             o = H.empty((R, Hh, hd), dt)
+            lse = torch.empty((R, Hh), dtype=torch.float32, device="cuda")
             for layer in range(L):
                 x = synth.chain_hidden(seed, step, layer, R, d)
                 kc, vc = caches[layer]
+                full = check and layer in full_layers
+                if full:
+                    kc_before, vc_before = H.host(kc), H.host(vc)
                 ctx.qkv_rope_cache_write(H.dev(x), W[layer], rs, rp, rc, bt, kc, vc, q)
-                if check and layer in sample_layers and step in (0, S):
-                    ctx.sync_status()
-                    pick = np.random.default_rng(step * 100 + layer).choice(R, size=16, replace=False)
-                    w = synth.chain_weight(seed, layer, d)
-                    q_o, _, _ = oracle.qkv_rope_cache_write(
-                        x.values()[pick], w.values(), Hh, hd, s.rope_theta, rows.row_rope_pos[pick],
-                        rows.row_seq[pick], np.full(16, -1), g.block_table, g.page_size,
-                        np.zeros((1, d)), np.zeros((1, d)), dt)
-                    H.assert_close(H.host(q)[pick], q_o, dt, f"sampled q step {step} layer {layer}")
-                ctx.sched_attn(q, kc, vc, bt, cu, kv_len, rk, o, track_scores=score)
+                before = score.clone() if full else None
+                ctx.sched_attn(q, kc, vc, bt, cu, kv_len, rk, o, lse_out=lse, track_scores=score)
+                if not check:
+                    continue
+                ctx.sync_status()
+                tag = f"step {step} layer {layer}"
+                if full:
+                    q_o, kc_o, vc_o = oracle.qkv_rope_cache_write(
+                        x.values(), W32[layer], Hh, hd, s.rope_theta, rows.row_rope_pos, rows.row_seq,
+                        rows.row_cache_pos, g.block_table, P, kc_before, vc_before, dt)
+                    del kc_before, vc_before
+                    H.assert_close(H.host(q), q_o, dt, f"q {tag}")
+                    written = oracle.slot_map(rows.row_seq, rows.row_cache_pos, g.block_table, P)
+                    kc_g, vc_g = H.host(kc), H.host(vc)
+                    H.assert_close(kc_g[written], kc_o[written], dt, f"k {tag}")
+                    H.assert_close(vc_g[written], vc_o[written], dt, f"v {tag}")
+                    del kc_o, vc_o
+                    o_o, lse_o, tr_o = oracle.sched_attn(H.host(q), kc_g, vc_g, g.block_table, P, rows.cu_seqlens,
+                                                         wl.seq_len, rows.row_kind, max_seq=N, dtype=dt)
+                    H.assert_close(H.host(o), o_o, dt, f"O {tag}")
+                    H.assert_close(H.host(lse), lse_o, "f32", f"LSE {tag}")
+                    H.assert_close(H.host(score) - H.host(before), tr_o, "f32", f"tracker increment {tag}")
+                    continue
+                # a seeded 5% of the rows, from two seeded sequences
+                rng = np.random.default_rng([seed, 9, step, layer])
+                seqs = np.sort(rng.choice(B, size=2, replace=False))
+                n_pick = max(2, int(round(0.05 * R)))
+                pick = []
+                for j, b in enumerate(seqs):
+                    lo, hi = int(rows.cu_seqlens[b]), int(rows.cu_seqlens[b + 1])
+                    m = n_pick // 2 + (n_pick % 2 if j == 0 else 0)
+                    pick.append(np.sort(rng.choice(np.arange(lo, hi), size=min(m, hi - lo), replace=False)))
+                pick = np.concatenate(pick)
+                pick_t = torch.as_tensor(pick, device="cuda")
+                # projection of the picked rows into a compact cache (slot j = picked row j)
+                q_o, kc_o, vc_o = oracle.qkv_rope_cache_write(
+                    x.values()[pick], W32[layer], Hh, hd, s.rope_theta, rows.row_rope_pos[pick],
+                    np.zeros(len(pick), np.int32), np.arange(len(pick)), np.zeros((1, 1), np.int32), len(pick),
+                    np.zeros((len(pick), d)), np.zeros((len(pick), d)), dt)
+                H.assert_close(H.host(q[pick_t]), q_o, dt, f"sampled q {tag}")
+                slots = torch.as_tensor(oracle.slot_map(rows.row_seq[pick], rows.row_cache_pos[pick], g.block_table, P),
+                                        device="cuda")
+                H.assert_close(H.host(kc[slots]), kc_o, dt, f"sampled k {tag}")
+                H.assert_close(H.host(vc[slots]), vc_o, dt, f"sampled v {tag}")
+                # attention of the picked rows over their sequences' GPU caches
+                # (a compact two-page copy of the two sequences' slots)
+                sl = torch.cat([torch.arange(int(b) * P, int(b) * P + P, device="cuda") for b in seqs])
+                kc2, vc2 = H.host(kc[sl]), H.host(vc[sl])
+                cnt = [int(np.sum(rows.row_seq[pick] == b)) for b in seqs]
+                cu2 = np.array([0, cnt[0], cnt[0] + cnt[1]], np.int32)
+                o_o, lse_o, _ = oracle.sched_attn(H.host(q[pick_t]), kc2, vc2, np.array([[0], [1]], np.int32), P,
+                                                  cu2, wl.seq_len[seqs], rows.row_kind[pick], max_seq=N, dtype=dt)
+                H.assert_close(H.host(o[pick_t]), o_o, dt, f"sampled O {tag}")
+                H.assert_close(H.host(lse[pick_t]), lse_o, "f32", f"sampled LSE {tag}")
             idx = torch.empty((B, k), dtype=torch.int32, device="cuda")
-            cnt = torch.empty((B,), dtype=torch.int32, device="cuda")
-            ctx.track_topk(score, elig, kv_len, k, idx, cnt)
+            cnt_t = torch.empty((B,), dtype=torch.int32, device="cuda")
+            ctx.track_topk(score, elig, kv_len, k, idx, cnt_t)
             ctx.sync_status()
             sc, ih = H.host(score), H.host(idx)
             if check:

@@ -5,11 +5,22 @@ set) against the float64 step oracle, by teacher forcing.
 
 Each step starts the oracle from the GPU's own state (tokens, masks, tracked
 set and the caches, downloaded before the step) and forces it to follow the
-GPU's decisions. Compared: the row sets (exact), the window rows' and mask
-views' confidences and predictions (tolerance, and exact argmax where the
-top two logits are apart), the tracker scores, the caches after the step;
-the GPU's decisions must be exactly the decision rules applied to its own
-confidences, and its next state exactly what those decisions give."""
+GPU's decisions. Compared:
+  * the row sets, exactly;
+  * the final rows of both forwards, element by element (two bf16 ulps where
+    an ulp exceeds the bf16 tolerance, as for the whole-model forward);
+  * each stage boundary on identical inputs: the fused LM head run on the
+    oracle's own final window rows must give the oracle's confidences (fp32
+    tolerance) and exactly its argmax, commit mask and search lists; the
+    verify-side LM head run on the oracle's own mask-view rows must give its
+    mask confidences and exactly its predictions and acceptance (a step whose
+    oracle values hold a near-tie, where fp32 and float64 may decide
+    differently, is checked by the rule instead, and most steps must be
+    clear of one);
+  * the tracker scores and the caches after the step;
+  * the GPU's own decisions, which must be the decision rules applied to its
+    own confidences, and its next state, which must be exactly what those
+    decisions give."""
 import numpy as np
 import pytest
 
@@ -57,6 +68,7 @@ def test_flash_steps_teacher_forced():
     bt = H.ints(geom.block_table)
     ws = torch.empty(ctx.flash_workspace_bytes(mc["ffn"], params, B, N), dtype=torch.uint8, device="cuda")
     saw = dict(commit=0, search=0, accept=0, verify_steps=0)
+    checked_steps = exact_steps = exact_verify = 0
     for step in range(40):
         if not seqs["masked"].any():
             break
@@ -76,14 +88,12 @@ def test_flash_steps_teacher_forced():
         assert int(rec["n_rows"][0]) == len(tr["draft_pos"]), step
         assert rec["window_pos"][:RW].tolist() == tr["window_pos"].tolist()
         assert rec["window_seq"][:RW].tolist() == tr["window_seq"].tolist()
-        # the draft forward's final rows, then the window rows' confidences and
-        # predictions (the logits have a standard deviation near 4.5 here, so a
-        # relative difference r in a hidden row moves a logit by about 4.5 r)
+        # the draft forward's final rows
         _rows_close(rec["draft_final"], tr["draft_final"], f"draft rows, step {step}")
         dec = tr["unmask"]
-        np.testing.assert_allclose(rec["conf"][:RW], dec["conf"], atol=1e-2, rtol=5e-2)
-        clear = _top2_gap(tr["window_logits"]) > 0.2
-        assert np.array_equal(rec["argmax"][:RW][clear], dec["argmax"][clear])
+        # stage boundary: the LM head and the eps decisions on the oracle's rows
+        exact_steps += _lm_unmask_stage(ctx, wl, tr, dec, B, params, f"step {step}")
+        checked_steps += 1
         # the GPU's decisions are the rule applied to its own confidences
         want = _decide(rec["conf"][:RW], tr["window_seq"], tr["window_pos"], B, params["eps"], True, MS)
         assert rec["commit"][:RW].tolist() == want["commit"].tolist()
@@ -97,10 +107,7 @@ def test_flash_steps_teacher_forced():
             assert int(rec["n_rows"][1]) == len(tr["verify"]["final"])
             ver = tr["verify"]
             _rows_close(rec["verify_final"], ver["final"], f"verify rows, step {step}")
-            valid = np.array([b * MS + j for b in range(B) for j in range(int(rec["n_search"][b]))])
-            np.testing.assert_allclose(rec["mask_conf"][valid], ver["mask_conf"][valid], atol=1e-2, rtol=5e-2)
-            mgap = _top2_gap(ver["mask_logits"])[valid]
-            assert np.array_equal(rec["mask_argmax"][valid][mgap > 0.2], ver["mask_argmax"][valid][mgap > 0.2])
+            exact_verify += _lm_verify_stage(ctx, wl, ver, rec["n_search"], B, params, f"step {step}")
             acc, n_acc = _verify_rule(rec["mask_conf"], rec["mask_argmax"], ver["draft_tok"], rec["n_search"],
                                       params["gamma"], B, MS)
             assert rec["n_accept"].tolist() == n_acc.tolist()
@@ -125,7 +132,90 @@ def test_flash_steps_teacher_forced():
         pytest.fail("decode did not finish")
     assert not seqs["masked"].any()
     assert saw["commit"] > 0 and saw["search"] > 0 and saw["accept"] > 0 and saw["verify_steps"] > 0
+    # the identical-input stage checks were exact on most steps
+    assert exact_steps >= 0.8 * checked_steps, (exact_steps, checked_steps)
+    assert exact_verify >= 0.8 * saw["verify_steps"], (exact_verify, saw["verify_steps"])
     ctx.close()
+
+
+def _near_ties(conf, logits, row_seq, threshold):
+    """True where float64 and fp32 may decide differently: the top two logits
+    within 1e-3, a confidence within 1e-5 of the (float32) threshold, or two
+    confidences of one sequence within 1e-6 relative of each other."""
+    conf = np.asarray(conf, np.float64)
+    if len(conf) == 0:
+        return False
+    if (_top2_gap(logits) < 1e-3).any():
+        return True
+    if (np.abs(conf - np.float64(np.float32(threshold))) < 1e-5).any():
+        return True
+    for b in np.unique(row_seq):
+        c = np.sort(conf[np.asarray(row_seq) == b])
+        if len(c) > 1 and (np.diff(c) < 1e-6 * c[1:]).any():
+            return True
+    return False
+
+
+def _lm_unmask_stage(ctx, wl, tr, dec, B, params, what):
+    """The fused LM head + eps decisions on the oracle's own final window rows
+    against the oracle's decisions from the same rows. Returns 1 when the
+    decisions were compared exactly (0 when a near-tie left them to the rule)."""
+    torch = H.torch_mod()
+    MS = params["max_search"]
+    hid = H.dev(synth.make_tensor(tr["draft_final"][tr["window_rows"]], "bf16"))
+    RW = hid.shape[0]
+    conf = torch.empty(RW, dtype=torch.float32, device="cuda")
+    arg = torch.empty(RW, dtype=torch.int32, device="cuda")
+    com = torch.empty(RW, dtype=torch.uint8, device="cuda")
+    srows = torch.full((B, MS), -7, dtype=torch.int32, device="cuda")
+    nsr = torch.empty((B,), dtype=torch.int32, device="cuda")
+    ctx.lm_head_unmask(hid, wl, B, MS, row_seq=H.ints(tr["window_seq"]), row_pos=H.ints(tr["window_pos"]),
+                       eps=params["eps"], force_progress=True, conf=conf, argmax=arg, commit=com,
+                       search_rows=srows, n_search=nsr)
+    ctx.sync_status()
+    conf, arg, com, srows, nsr = H.host(conf), H.host(arg), H.host(com), H.host(srows), H.host(nsr)
+    H.assert_close(conf, dec["conf"], "f32", f"LM-head confidences on the oracle's rows, {what}")
+    if _near_ties(dec["conf"], tr["window_logits"], tr["window_seq"], params["eps"]):
+        want = _decide(conf, tr["window_seq"], tr["window_pos"], B, params["eps"], True, MS)
+        assert com.tolist() == want["commit"].tolist(), what
+        assert srows.tolist() == want["search_rows"].tolist(), what
+        return 0
+    assert arg.tolist() == dec["argmax"].tolist(), what
+    assert com.tolist() == dec["commit"].tolist(), what
+    assert nsr.tolist() == dec["n_search"].tolist(), what
+    assert srows.tolist() == dec["search_rows"].tolist(), what
+    return 1
+
+
+def _lm_verify_stage(ctx, wl, ver, n_search, B, params, what):
+    """The verify-side LM head on the oracle's own mask-view rows (the
+    verify forward's layout) against the oracle's acceptance from them."""
+    torch = H.torch_mod()
+    MS = params["max_search"]
+    mr = ver["mask_rows"]
+    hv = np.zeros((B * MS, ver["final"].shape[1]))
+    hv[mr >= 0] = ver["final"][mr[mr >= 0]]
+    dtok = np.where(ver["draft_tok"] >= 0, ver["draft_tok"], 0)
+    acc = torch.empty(B * MS, dtype=torch.uint8, device="cuda")
+    nacc = torch.empty(B, dtype=torch.int32, device="cuda")
+    mconf = torch.empty(B * MS, dtype=torch.float32, device="cuda")
+    marg = torch.empty(B * MS, dtype=torch.int32, device="cuda")
+    ctx.lm_head_verify(H.dev(synth.make_tensor(hv, "bf16")), wl, B, MS, n_search=H.ints(n_search),
+                       draft_tok=H.ints(dtok), gamma=params["gamma"], accept=acc, n_accept=nacc, mask_conf=mconf,
+                       mask_argmax=marg)
+    ctx.sync_status()
+    mconf, marg, acc, nacc = H.host(mconf), H.host(marg), H.host(acc), H.host(nacc)
+    valid = np.array([b * MS + j for b in range(B) for j in range(int(n_search[b]))])
+    H.assert_close(mconf[valid], ver["mask_conf"][valid], "f32", f"mask-view confidences on the oracle's rows, {what}")
+    gap = _top2_gap(ver["mask_logits"][valid])
+    if (gap < 1e-3).any() or (np.abs(ver["mask_conf"][valid] - np.float64(np.float32(params["gamma"]))) < 1e-5).any():
+        a, n = _verify_rule(mconf, marg, ver["draft_tok"], n_search, params["gamma"], B, MS)
+        assert nacc.tolist() == n.tolist(), what
+        return 0
+    assert marg[valid].tolist() == ver["mask_argmax"][valid].tolist(), what
+    assert nacc.tolist() == ver["n_accept"].tolist(), what
+    assert acc[valid].tolist() == ver["accept"][valid].tolist(), what
+    return 1
 
 
 def _top2_gap(logits):
@@ -135,12 +225,16 @@ def _top2_gap(logits):
 
 
 def _rows_close(gpu, ref, what):
-    """Each final row (unit RMS times the gains) within 1e-2 relative RMS of
-    the oracle's: bf16 roundings of the intermediates on both sides, carried
-    through two layers whose W_o and W_down are large. A row taken from the
-    wrong position or sequence would be off by about sqrt(2)."""
+    """The final rows element by element, with the whole-model forward's
+    rule: bf16 of unit-RMS values that passed through every layer, so where
+    an fp32 and a float64 rounding upstream put a value across a rounding
+    boundary two bf16 ulps are allowed where an ulp exceeds the bf16
+    tolerance."""
     gpu = np.asarray(gpu, np.float64)
     assert gpu.shape == ref.shape, (what, gpu.shape, ref.shape)
-    rel = np.sqrt(((gpu - ref) ** 2).mean(1) / (ref ** 2).mean(1))
-    assert (rel < 1e-2).all(), f"{what}: worst row relative RMS difference {rel.max():.3e}"
+    err = np.abs(gpu - ref)
+    allowed = np.maximum(H.BF16_TOL, 2.0 * H.bf16_ulp(ref))
+    bad = err > allowed
+    assert not bad.any(), (f"{what}: {int(bad.sum())} of {err.size} elements out of tolerance, worst error "
+                           f"{err.max():.3e} ({(err / np.maximum(H.bf16_ulp(ref), 1e-30)).max():.1f} ulps)")
 
