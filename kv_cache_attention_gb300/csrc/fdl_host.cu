@@ -106,8 +106,6 @@ fdl_status fdl_create(const fdl_config* cfg, void* cuda_stream, fdl_ctx** out) {
   e = e ? e : cudaMalloc(&ctx->worklist, (1 + 4 * (size_t)ctx->worklist_items) * sizeof(int));
   e = e ? e : cudaMalloc(&ctx->n_masked, cfg->max_batch * sizeof(int));
   e = e ? e : cudaMalloc(&ctx->tickets, 8 * sizeof(unsigned));
-  ctx->row_slots = 8192;
-  e = e ? e : cudaMalloc(&ctx->row_part, (size_t)ctx->row_slots * 3 * sizeof(float));
   if (cfg->dtype == FDL_BF16) {
     ctx->qkv_partial_floats = fdl_qkv_partial_floats(ctx->num_sms);
     ctx->qkv_tickets = 4 * ctx->num_sms;
@@ -136,7 +134,6 @@ void fdl_destroy(fdl_ctx* ctx) {
   cudaFree(ctx->worklist);
   cudaFree(ctx->n_masked);
   cudaFree(ctx->tickets);
-  cudaFree(ctx->row_part);
   cudaFree(ctx->qkv_partials);
   cudaFree(ctx->qkv_ticket_buf);
   cudaFree(ctx->lm_part);

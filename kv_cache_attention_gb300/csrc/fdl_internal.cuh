@@ -32,8 +32,6 @@ struct fdl_ctx {
   int worklist_items;
   int* n_masked;        // [max_batch] WINDOW rows per sequence
   unsigned* tickets;    // [8] last-block tickets (left at zero between calls)
-  float* row_part;      // split partials of the vocab reductions
-  int row_slots;        // rows x splits the partial buffer above holds
   float* qkv_partials;  // split-K partial tiles of the tensor-core projection
   size_t qkv_partial_floats;
   unsigned* qkv_ticket_buf;  // per-tile arrival counters (zero between calls)

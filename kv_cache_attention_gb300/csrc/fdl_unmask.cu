@@ -9,15 +9,16 @@
 // parallel decoding": commit the most confident token when none passes.
 //
 // Both phases are HBM-bound reductions over vocab-wide logits rows. A row is
-// split across independent CTAs; every CTA streams its slice with 128-bit
-// loads, keeps (max, sum exp, argmax) per thread over register blocks (tree
-// max, then the sum of exponentials with four accumulators), and merges with
-// warp shuffles. Each CTA publishes its slice partial to a workspace slot (a
-// row in one slice writes its confidence directly) and takes one ticket for
-// the whole grid; the last CTA to arrive merges every row's partials by a
-// fixed xor tree, so the result does not depend on timing, and takes the
-// per-sequence decisions: one launch per phase, and nothing ever waits on
-// another CTA.
+// split across the CTAs of one thread-block cluster (up to 8); every CTA
+// streams its slice with 128-bit loads, keeps (max, sum exp, argmax) per
+// thread over register blocks (tree max, then the sum of exponentials with
+// four accumulators), and merges with warp shuffles. The slices' statistics
+// meet in the row leader's (cluster rank 0) shared memory through
+// distributed shared memory and are merged there in rank order, so the
+// result does not depend on timing; the leader writes the row's confidence
+// and argmax and takes one ticket per row. The leader that arrives last
+// takes the per-sequence decisions: one launch per phase, and the only wait
+// on another CTA is the cluster barrier of co-scheduled CTAs.
 #include <cudaTypedefs.h>
 
 #include "fdl_internal.cuh"
@@ -26,7 +27,7 @@
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kMaxSplit = 16;
+constexpr int kMaxSplit = 8;  // CTAs per row: one (portable) thread-block cluster
 
 struct Stat {
   float m;  // running max
@@ -112,7 +113,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 template <typename T>
 __device__ Stat slice_stat(const T* row, int lo, int hi, bool vec_ok) {
   constexpr int N = 16 / sizeof(T);
-  constexpr int kVB = 4;
+  constexpr int kVB = 8;
   Stat st{-INFINITY, 0.f, 0x7fffffff};
   const int tid = threadIdx.x;
   int i = lo;
@@ -178,7 +179,7 @@ struct RowParams {
   const void* logits;
   int vocab;
   int n_rows;        // rows with a ticket (all of them, valid or not)
-  int split;         // CTAs per row (cluster size)
+  int split;         // CTAs per row (the row's cluster)
   int chunk;         // elements per CTA slice (multiple of 8)
   bool vec_ok;
   // verify phase: row r = b*max_search + j is valid only when j < n_search[b]
@@ -186,8 +187,8 @@ struct RowParams {
   int max_search;
   float* out_conf;
   int* out_arg;
-  float* part;                 // [n_rows * split][3] split partials (max, sum, argmax bits)
-  unsigned* ticket;            // arrival counter of the whole grid, zero between calls
+  float* part;                 // fused LM head: per-CTA statistics [CTA][row][3] (max, sum, argmax bits)
+  unsigned* ticket;            // arrival counter of the rows, zero between calls
   unsigned* err;
   // unmask decisions
   int phase;         // 0 = unmask, 1 = verify
@@ -382,6 +383,7 @@ constexpr int kPreRows = kThreads;
 template <typename T>
 __global__ void __launch_bounds__(kThreads) row_reduce_kernel(RowParams p) {
   __shared__ Stat warp_stat[kThreads / 32];
+  __shared__ float4 cl_stat[kMaxSplit];  // row leader: every slice's (max, sum, argmax bits)
   __shared__ unsigned go;
   __shared__ int pre_seq[kPreRows], pre_pos[kPreRows];
   __shared__ float pre_conf[kPreRows];
@@ -420,89 +422,48 @@ __global__ void __launch_bounds__(kThreads) row_reduce_kernel(RowParams p) {
     // fixed xor tree (lane 0 ends with the result)
     Stat acc = lane < kThreads / 32 ? warp_stat[lane] : none;
     for (int off = kThreads / 64; off; off >>= 1) acc = shfl_merge(acc, off);
-    if (lane == 0) {
-      if (valid) {
-        if (p.split > 1) {
-          float* slot = p.part + ((size_t)row * p.split + sp) * 3;
-          __stcg(slot, acc.m);
-          __stcg(slot + 1, acc.s);
-          __stcg(slot + 2, __int_as_float(acc.i));
-        } else {
-          p.out_conf[row] = 1.f / acc.s;  // acc.s = sum exp(x - max) >= 1
-          p.out_arg[row] = acc.i;
-        }
-      }
-      // one ticket for the whole grid: the last CTA finishes every row. The
-      // add releases this CTA's partial and, for the last arrival, acquires
-      // every other CTA's (passed on to the CTA's threads by the barrier)
-      unsigned t;
-      asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(t) : "l"(p.ticket) : "memory");
-      go = t == gridDim.x - 1u ? 1u : 0u;
+    if (lane == 0 && p.split > 1) {
+      // into slot sp of the row leader's (cluster rank 0) shared memory
+      const uint32_t dst = tc::map_cluster(tc::smem_addr(&cl_stat[sp]), 0u);
+      asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "f"(acc.m), "f"(acc.s),
+                   "f"(__int_as_float(acc.i)), "f"(0.f)
+                   : "memory");
     }
+    if (lane == 0) warp_stat[0] = acc;
+  }
+  if (p.split > 1) {
+    // The CTAs of a row form a cluster: after the barrier (release /
+    // acquire at cluster scope) the leader holds every slice's statistic.
+    tc::cluster_sync();
+    if (sp != 0) return;
+  } else {
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    if (valid) {
+      Stat acc = warp_stat[0];
+      if (p.split > 1) {
+        // the slices in rank order
+        auto slot = [&](int k) { return Stat{cl_stat[k].x, cl_stat[k].y, __float_as_int(cl_stat[k].z)}; };
+        acc = slot(0);
+        for (int k = 1; k < p.split; ++k) acc = merge(acc, slot(k));
+      }
+      p.out_conf[row] = 1.f / acc.s;  // acc.s = sum exp(x - max) >= 1
+      p.out_arg[row] = acc.i;
+    }
+    // one ticket per row for the whole grid: the row leader that arrives
+    // last takes the decisions. The add releases this row's result and,
+    // for the last arrival, acquires every other row's (passed on to the
+    // CTA's threads by the barrier)
+    unsigned t;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(t) : "l"(p.ticket) : "memory");
+    go = t == (unsigned)(gridDim.x / p.split) - 1u ? 1u : 0u;
   }
   __syncthreads();
   if (!go) return;
-  if (p.split > 1) {
-    const int n_rows = p.n_rows, split = p.split;
-    const float* part = p.part;
-    float* out_conf = p.out_conf;
-    int* out_arg = p.out_arg;
-    if (split <= 4) {
-      // many rows, few slices: one thread per row, its slices' loads in
-      // flight together, merged in slice order
-      for (int r = threadIdx.x; r < n_rows; r += kThreads) {
-        if (!row_valid(r)) continue;
-        Stat a[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          a[k] = none;
-          if (k < split) {
-            const float* o = part + ((size_t)r * split + k) * 3;
-            a[k] = Stat{__ldcg(o), __ldcg(o + 1), __float_as_int(__ldcg(o + 2))};
-          }
-        }
-        const Stat m = merge(merge(a[0], a[1]), merge(a[2], a[3]));
-        out_conf[r] = 1.f / m.s;
-        out_arg[r] = m.i;
-        if (pre) pre_conf[r] = 1.f / m.s;
-      }
-    } else {
-      // few rows, many slices: a warp takes 4 rows per round with all their
-      // loads in flight, lane k holding slice k; a fixed xor tree merges them
-      constexpr int kRowsPerWarp = 4;
-      for (int r0 = warp * kRowsPerWarp; r0 < n_rows; r0 += (kThreads / 32) * kRowsPerWarp) {
-        Stat a[kRowsPerWarp];
-        bool v[kRowsPerWarp];
-#pragma unroll
-        for (int u = 0; u < kRowsPerWarp; ++u) {
-          v[u] = row_valid(r0 + u);
-          a[u] = none;
-          if (v[u] && lane < split) {
-            const float* o = part + ((size_t)(r0 + u) * split + lane) * 3;
-            a[u] = Stat{__ldcg(o), __ldcg(o + 1), __float_as_int(__ldcg(o + 2))};
-          }
-        }
-        // level by level over the rows, so the rows' shuffles overlap (the
-        // level loop stays rolled: this code runs once per launch)
-#pragma unroll 1
-        for (int off = kMaxSplit / 2; off; off >>= 1)
-#pragma unroll
-          for (int u = 0; u < kRowsPerWarp; ++u) a[u] = shfl_merge(a[u], off);
-#pragma unroll
-        for (int u = 0; u < kRowsPerWarp; ++u) {
-          if (v[u] && lane == 0) {
-            out_conf[r0 + u] = 1.f / a[u].s;
-            out_arg[r0 + u] = a[u].i;
-            if (pre) pre_conf[r0 + u] = 1.f / a[u].s;
-          }
-        }
-      }
-    }
-    __syncthreads();  // this CTA's confidences are written before the decisions read them
-  }
   if (p.phase == 0) {
-    if (pre && p.split == 1) {
-      // one slice per row: every CTA wrote its row's confidence to global memory
+    if (pre) {
+      // every row leader wrote its row's confidence to global memory
       for (int r = threadIdx.x; r < n_rows_all; r += kThreads) pre_conf[r] = __ldcg(p.out_conf + r);
     }
     __syncthreads();
@@ -521,16 +482,14 @@ cudaError_t launch_phase(fdl_ctx* ctx, RowParams p) {
   int split = (4 * ctx->num_sms + p.n_rows - 1) / p.n_rows;
   split = max(1, min(split, kMaxSplit));
   split = min(split, max(1, V / 2048));
-  if ((size_t)p.n_rows * split > (size_t)ctx->row_slots) split = 1;
   int chunk = (V + split - 1) / split;
   chunk = (chunk + 7) / 8 * 8;
   split = (V + chunk - 1) / chunk;
   p.split = split;
   p.chunk = chunk;
-  p.part = ctx->row_part;
   p.vec_ok = ((reinterpret_cast<uintptr_t>(p.logits) & 15) == 0) && ((size_t)V * sizeof(T)) % 16 == 0;
-  return fdl_launch_pdl(row_reduce_kernel<T>, dim3((unsigned)(p.n_rows * split)), dim3(kThreads), 0, ctx->stream, 1,
-                        p);
+  return fdl_launch_pdl(row_reduce_kernel<T>, dim3((unsigned)(p.n_rows * split)), dim3(kThreads), 0, ctx->stream,
+                        split, p);
 }
 
 

@@ -90,6 +90,14 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// 16-byte global -> shared copy that completes asynchronously (no register
+// staging); cp_async_wait_all waits for every such copy of this thread.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_dst)), "l"(gmem_src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // ------------------------------------------------------------------ tcgen05
 // Shared-memory matrix descriptor, K-major operand in the 128-byte swizzle
 // layout that a TMA tile load with CU_TENSOR_MAP_SWIZZLE_128B produces:
