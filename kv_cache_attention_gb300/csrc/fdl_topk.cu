@@ -208,11 +208,10 @@ topk_kernel(const float* __restrict__ scores, const unsigned char* __restrict__ 
   constexpr int kWarps = kThreads / 32;
   __shared__ unsigned skey[kStage];
   __shared__ __align__(16) unsigned hist[3][256];
-  __shared__ unsigned w_cnt[kWarps], w_or[kWarps], w_and[kWarps], w_tie[kWarps];
+  __shared__ unsigned w_cnt[kWarps], w_or[kWarps], w_and[kWarps], w_tie[kWarps], w_cand[kWarps];
   // candidate (key, position) packed as key << 32 | ~position: a larger
   // value ranks first, so ties on the key go to the lower position
   __shared__ __align__(16) unsigned long long cand[kMaxK];
-  __shared__ unsigned n_cand;
 
   const int b = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -251,7 +250,6 @@ topk_kernel(const float* __restrict__ scores, const unsigned char* __restrict__ 
     w_and[warp] = kand;
   }
   if (tid < 256) hist[0][tid] = 0u;
-  if (tid == 0) n_cand = 0u;
   __syncthreads();
   // every lane of every warp forms the block totals (lanes past the warp
   // count contribute the identity; the xor tree spans all 32 lanes, so every
@@ -368,24 +366,42 @@ topk_kernel(const float* __restrict__ scores, const unsigned char* __restrict__ 
     for (int w = 0; w < warp; ++w) off += w_tie[w];
     tie_rank = off + incl - ties;
   }
+  // each thread's candidates in position order, placed by a block prefix
+  // count (no atomics, so the candidate order is fixed)
+  bool tk[kPer];
+  unsigned mine = 0u;
 #pragma unroll
   for (int j = 0; j < kPer; ++j) {
-    if (j >= per) continue;
     const unsigned key = r[j];
-    if (key == 0u) continue;
-    bool take;
-    if (cut_ties) take = key > T || (key == T && tie_rank++ < need);
-    else take = key >= low;
-    if (take) {
-      const unsigned slot = atomicAdd(&n_cand, 1u);
-      if (slot < (unsigned)kMaxK) {
-        cand[slot] = ((unsigned long long)key << 32) | (unsigned)~(unsigned)(lo + j);
-      }
+    bool take = false;
+    if (j < per && key != 0u) {
+      if (cut_ties) take = key > T || (key == T && tie_rank++ < need);
+      else take = key >= low;
+    }
+    tk[j] = take;
+    mine += take ? 1u : 0u;
+  }
+  const unsigned cincl = warp_incl_scan(mine, lane);
+  if (lane == 31) w_cand[warp] = cincl;
+  __syncthreads();
+  unsigned coff = 0u, ctot = 0u;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const unsigned v = w_cand[w];
+    coff += w < warp ? v : 0u;
+    ctot += v;
+  }
+  unsigned slot = coff + cincl - mine;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    if (tk[j]) {
+      if (slot < (unsigned)kMaxK) cand[slot] = ((unsigned long long)r[j] << 32) | (unsigned)~(unsigned)(lo + j);
+      ++slot;
     }
   }
   __syncthreads();
-  const int m = (int)min(n_cand, (unsigned)kMaxK);
-  if (tid == 0 && (n_cand > (unsigned)kMaxK || n_cand < kk)) fdl::raise_error(err, FDL_DEVERR_SHAPE);
+  const int m = (int)min(ctot, (unsigned)kMaxK);
+  if (tid == 0 && (ctot > (unsigned)kMaxK || ctot < kk)) fdl::raise_error(err, FDL_DEVERR_SHAPE);
   // rank every candidate by (key desc, position asc) among the candidates
   // (which hold every key that can rank above it) and scatter the first kk
   for (int c = tid; c < m; c += kThreads) {
