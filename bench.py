@@ -827,6 +827,36 @@ def config_results(sections, reps_scale: float = 1.0, workloads=None):
         ctx.sync_status()
         results.append({"config": "lm_head_llada_vocab_w32", "rows": Rw, **res})
         ctx.close()
+        # the Flash-Verify stress scale: 32 sequences x 32 window rows, and the
+        # verify side's 32 x 16 mask views (tensor-bound: about R FLOP per byte)
+        B5, W5, M5 = 32, 32, 16
+        ctx = fdl.fdl_create(d, 32, 128, 5e5, B5, 64, 0, 64, 1, B5 * W5, V, "bf16", stream=stream)
+        R5 = B5 * W5
+        hid5 = torch.randn((R5, d), device="cuda", generator=gen).bfloat16()
+        rs5, rp5 = i32(np.repeat(np.arange(B5), W5)), i32(np.tile(512 + np.arange(W5), B5))
+        conf5 = torch.empty(R5, dtype=torch.float32, device="cuda")
+        arg5 = torch.empty(R5, dtype=torch.int32, device="cuda")
+        com5 = torch.empty(R5, dtype=torch.uint8, device="cuda")
+        sr5 = torch.empty((B5, M5), dtype=torch.int32, device="cuda")
+        ns5 = torch.empty((B5,), dtype=torch.int32, device="cuda")
+        lm5 = [lambda W=W: ctx.lm_head_unmask(hid5, W, B5, M5, row_seq=rs5, row_pos=rp5, eps=0.9,
+                                              force_progress=True, conf=conf5, argmax=arg5, commit=com5,
+                                              search_rows=sr5, n_search=ns5) for W in W_lm]
+        res5 = {"lm_head_unmask": entry(timed(lm5, 10), 2.0 * R5 * V * d, 2.0 * (V * d + R5 * d))}
+        Rv = B5 * M5
+        nsv = i32(np.full(B5, M5))
+        drv = torch.zeros(Rv, dtype=torch.int32, device="cuda")
+        accv = torch.empty(Rv, dtype=torch.uint8, device="cuda")
+        nav = torch.empty(B5, dtype=torch.int32, device="cuda")
+        mcv = torch.empty(Rv, dtype=torch.float32, device="cuda")
+        mav = torch.empty(Rv, dtype=torch.int32, device="cuda")
+        lmv = [lambda W=W: ctx.lm_head_verify(hid5[:Rv], W, B5, M5, n_search=nsv, draft_tok=drv, gamma=0.8,
+                                              accept=accv, n_accept=nav, mask_conf=mcv, mask_argmax=mav)
+               for W in W_lm]
+        res5["lm_head_verify (512 mask views)"] = entry(timed(lmv, 10), 2.0 * Rv * V * d, 2.0 * (V * d + Rv * d))
+        ctx.sync_status()
+        results.append({"config": "lm_head_llada_vocab_b32_w32", "rows": R5, **res5})
+        ctx.close()
         del W_lm
 
     if want("refresh"):

@@ -273,9 +273,12 @@ fdl_status fdl_unmask_verify(fdl_ctx* ctx, const fdl_unmask_args* args);
  *
  * hidden: [R_w, d_model] bf16, the window rows' final hidden states (16-byte
  * aligned); w_lm: [vocab, d_model] bf16 row-major (16-byte aligned). bf16
- * contexts only, 1 <= R_w <= 64 (one tile of window rows): otherwise
- * FDL_ERR_UNSUPPORTED / FDL_ERR_INVALID_ARG. The reductions over the
- * vocabulary run in a fixed order, so results do not depend on timing.
+ * contexts only, d_model a multiple of 64, 1 <= R_w <= max_rows: otherwise
+ * FDL_ERR_UNSUPPORTED / FDL_ERR_INVALID_ARG. Up to 64 rows form one column
+ * tile against 128-entry vocabulary tiles; more rows take 128-row tiles
+ * against 256-entry vocabulary tiles (the batched Flash-Verify scale, e.g.
+ * 32 sequences x 32 window rows). The reductions over the vocabulary run in
+ * a fixed order, so results do not depend on timing.
  * ---------------------------------------------------------------------- */
 fdl_status fdl_lm_head_unmask(fdl_ctx* ctx, const void* hidden, const void* w_lm, const fdl_unmask_args* args);
 
@@ -293,7 +296,8 @@ fdl_status fdl_lm_head_unmask(fdl_ctx* ctx, const void* hidden, const void* w_lm
  * mask_hidden: [B*max_search, d_model] bf16, the mask-view rows' final hidden
  * states in the verify forward's layout (rows j >= n_search[b] are read but
  * ignored); w_lm as for fdl_lm_head_unmask. bf16 contexts only,
- * 1 <= B*max_search <= 64: otherwise FDL_ERR_UNSUPPORTED / FDL_ERR_INVALID_ARG.
+ * 1 <= B*max_search <= max_rows: otherwise FDL_ERR_UNSUPPORTED /
+ * FDL_ERR_INVALID_ARG.
  * ---------------------------------------------------------------------- */
 fdl_status fdl_lm_head_verify(fdl_ctx* ctx, const void* mask_hidden, const void* w_lm,
                               const fdl_unmask_args* args);
@@ -518,7 +522,7 @@ fdl_status fdl_verify_rows(int B, const int* seq_len, const int* tracked, int tr
  * (the view keys). The call synchronises the context's stream (it reads the
  * decisions back three times). workspace: device memory of at least
  * fdl_flash_workspace_bytes bytes, 256-byte aligned. Limits: B*window and
- * B*max_search <= 64 (the fused LM head), 2*max_search <= config.max_views,
+ * B*max_search <= config.max_rows, 2*max_search <= config.max_views,
  * the first step's rows (every position of every sequence) <= max_rows.
  * A step on sequences with nothing left masked returns FDL_OK and does
  * nothing. An error before the decisions are applied (a bad argument, a

@@ -112,7 +112,11 @@ fdl_status fdl_create(const fdl_config* cfg, void* cuda_stream, fdl_ctx** out) {
     e = e ? e : cudaMalloc(&ctx->qkv_partials, ctx->qkv_partial_floats * sizeof(float));
     e = e ? e : cudaMalloc(&ctx->qkv_ticket_buf, ctx->qkv_tickets * sizeof(unsigned));
     e = e ? e : cudaMemset(ctx->qkv_ticket_buf, 0, ctx->qkv_tickets * sizeof(unsigned));
-    e = e ? e : cudaMalloc(&ctx->lm_part, fdl_lm_partial_floats(ctx->num_sms) * sizeof(float));
+    ctx->lm_part_floats = fdl_lm_partial_floats(ctx->num_sms, cfg->max_rows);
+    e = e ? e : cudaMalloc(&ctx->lm_part, ctx->lm_part_floats * sizeof(float));
+    ctx->lm_rt_ticket_count = fdl_lm_row_tiles(cfg->max_rows);
+    e = e ? e : cudaMalloc(&ctx->lm_rt_tickets, ctx->lm_rt_ticket_count * sizeof(unsigned));
+    e = e ? e : cudaMemset(ctx->lm_rt_tickets, 0, ctx->lm_rt_ticket_count * sizeof(unsigned));
   }
   e = e ? e : cudaMemcpy(ctx->rope_cos, hc.data(), n_tab * sizeof(float), cudaMemcpyHostToDevice);
   e = e ? e : cudaMemcpy(ctx->rope_sin, hs.data(), n_tab * sizeof(float), cudaMemcpyHostToDevice);
@@ -137,6 +141,7 @@ void fdl_destroy(fdl_ctx* ctx) {
   cudaFree(ctx->qkv_partials);
   cudaFree(ctx->qkv_ticket_buf);
   cudaFree(ctx->lm_part);
+  cudaFree(ctx->lm_rt_tickets);
   free(ctx);
 }
 
@@ -273,8 +278,8 @@ fdl_status fdl_lm_head_unmask(fdl_ctx* ctx, const void* hidden, const void* w_lm
     return fail(ctx, FDL_ERR_UNSUPPORTED, "fdl_lm_head_unmask: bf16 contexts only");
   if (a->B < 1 || a->B > ctx->cfg.max_batch)
     return fail(ctx, FDL_ERR_INVALID_ARG, "B=%d outside [1, max_batch=%d]", a->B, ctx->cfg.max_batch);
-  if (a->R_w < 1 || a->R_w > fdl_lm_head_max_rows())
-    return fail(ctx, FDL_ERR_UNSUPPORTED, "R_w=%d outside [1, %d]", a->R_w, fdl_lm_head_max_rows());
+  if (a->R_w < 1 || a->R_w > ctx->cfg.max_rows)
+    return fail(ctx, FDL_ERR_INVALID_ARG, "R_w=%d outside [1, max_rows=%d]", a->R_w, ctx->cfg.max_rows);
   if (a->max_search < 0 || a->max_search > 1024)
     return fail(ctx, FDL_ERR_INVALID_ARG, "max_search=%d outside [0, 1024]", a->max_search);
   if (!a->row_seq || !a->row_pos || !a->conf || !a->argmax || !a->commit || !a->n_search ||
@@ -297,9 +302,9 @@ fdl_status fdl_lm_head_verify(fdl_ctx* ctx, const void* mask_hidden, const void*
     return fail(ctx, FDL_ERR_INVALID_ARG, "B=%d outside [1, max_batch=%d]", a->B, ctx->cfg.max_batch);
   if (a->max_search < 1 || a->max_search > 1024)
     return fail(ctx, FDL_ERR_INVALID_ARG, "max_search=%d outside [1, 1024]", a->max_search);
-  if ((long long)a->B * a->max_search > fdl_lm_head_max_rows())
-    return fail(ctx, FDL_ERR_UNSUPPORTED, "B*max_search=%lld above %d mask-view rows",
-                (long long)a->B * a->max_search, fdl_lm_head_max_rows());
+  if ((long long)a->B * a->max_search > ctx->cfg.max_rows)
+    return fail(ctx, FDL_ERR_INVALID_ARG, "B*max_search=%lld above max_rows=%d mask-view rows",
+                (long long)a->B * a->max_search, ctx->cfg.max_rows);
   if (!a->n_search || !a->draft_tok || !a->accept || !a->n_accept || !a->mask_conf || !a->mask_argmax)
     return fail(ctx, FDL_ERR_INVALID_ARG, "fdl_lm_head_verify: NULL output or input argument");
   if (!(a->gamma >= 0.f && a->gamma <= 1.f)) return fail(ctx, FDL_ERR_INVALID_ARG, "gamma outside [0,1]");

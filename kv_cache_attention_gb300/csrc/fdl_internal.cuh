@@ -36,7 +36,10 @@ struct fdl_ctx {
   size_t qkv_partial_floats;
   unsigned* qkv_ticket_buf;  // per-tile arrival counters (zero between calls)
   int qkv_tickets;
-  float* lm_part;       // per-vocabulary-tile statistics of the fused LM head (bf16 contexts)
+  float* lm_part;       // per-CTA row statistics of the fused LM head (bf16 contexts)
+  size_t lm_part_floats;
+  unsigned* lm_rt_tickets;  // per-row-tile arrival counters of the many-row LM head (zero between calls)
+  int lm_rt_ticket_count;
   long long wait_budget;  // projection main-loop wait budget in cycles (0 = the default ~2 s)
   char last_error[512];
 };
@@ -181,7 +184,8 @@ cudaError_t fdl_launch_lm_head(fdl_ctx* ctx, const void* hidden, const void* w_l
 // Rows the fused LM head takes in one call, and its workspace floats
 // (one set of per-row statistics per CTA of its persistent grid).
 int fdl_lm_head_max_rows();
-size_t fdl_lm_partial_floats(int num_sms);
+size_t fdl_lm_partial_floats(int num_sms, int max_rows);
+int fdl_lm_row_tiles(int max_rows);
 
 // Workspace floats the tensor-core projection needs for split-K partials.
 size_t fdl_qkv_partial_floats(int num_sms);

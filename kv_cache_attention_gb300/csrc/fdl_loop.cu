@@ -139,8 +139,8 @@ extern "C" fdl_status fdl_flash_step(fdl_ctx* ctx, const fdl_model* m, const voi
   const int B = s->B, W = p->window, MS = p->max_search, BT = p->track_budget, N = s->max_seq;
   if (B < 1 || B > c.max_batch || N < 1 || W < 1 || MS < 0 || BT < 0 || BT > 1024)
     return loop_fail(ctx, FDL_ERR_INVALID_ARG, "fdl_flash_step: bad sizes (B=%d window=%d max_search=%d)", B, W, MS);
-  if (B * W > fdl_lm_head_max_rows() || B * MS > fdl_lm_head_max_rows())
-    return loop_fail(ctx, FDL_ERR_UNSUPPORTED, "B*window and B*max_search must be <= %d", fdl_lm_head_max_rows());
+  if (B * W > ctx->cfg.max_rows || B * MS > ctx->cfg.max_rows)
+    return loop_fail(ctx, FDL_ERR_UNSUPPORTED, "B*window and B*max_search must be <= max_rows=%d", ctx->cfg.max_rows);
   if (2 * MS > c.max_views) return loop_fail(ctx, FDL_ERR_INVALID_ARG, "2*max_search > max_views");
   if (p->mask_token < 0 || p->mask_token >= c.vocab) return loop_fail(ctx, FDL_ERR_INVALID_ARG, "bad mask_token");
   Scratch d = carve(reinterpret_cast<char*>(workspace), ctx, m->ffn, p, B, N);

@@ -735,6 +735,245 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   if (threadIdx.x == 0) *p.rp.ticket = 0u;  // ready for the next call
 }
 
+// ---------------------------------------------------------------------------
+// Fused LM head for more than 64 rows. With that many rows the window rows
+// fill the M = 128 datapath themselves, so a tile takes the plain
+// orientation: 128 window rows (TMEM lanes) x 256 vocabulary entries (TMEM
+// columns), D = H_tile . W_tile^T, bf16 in, fp32 accumulate (tcgen05.mma).
+// Every epilogue thread then reduces its own window row along the
+// vocabulary, with no cross-thread reduction. The grid is n_rt row tiles x g
+// CTAs; CTA (rt, i) takes the contiguous vocabulary tiles [i n_vt / g,
+// (i + 1) n_vt / g) of row tile rt, so the n_rt CTAs of one vocabulary range
+// stream the same weight tiles at about the same time and the weight is read
+// from DRAM about once. A 4-stage TMA ring feeds the MMA; two TMEM
+// accumulators (2 x 256 columns) let the epilogue of one tile overlap the
+// products of the next. Each row's (max, sum, argmax) runs over the CTA's
+// tiles in order in registers; the CTA publishes them, the last CTA of the
+// row tile (one ticket per row tile) merges the g CTAs' statistics in CTA
+// order and writes the rows' confidences and argmaxes, and the row tile that
+// finishes last (a second ticket) takes the unmask or verify decisions.
+// Every merge is in a fixed order.
+// ---------------------------------------------------------------------------
+constexpr int kRM = 128;  // window rows per row tile
+constexpr int kRN = 256;  // vocabulary entries per tile
+constexpr int kRK = 64;
+constexpr int kRStages = 4;
+constexpr int kRA = kRM * kRK * 2;
+constexpr int kRB = kRN * kRK * 2;
+constexpr int kRStage = kRA + kRB;
+constexpr int kRPipe = kRStages * kRStage;
+constexpr int kRSmem = 1024 + kRPipe + 256;
+static_assert(kRSmem + 8 * 2048 + 8 * 1024 + 64 <= 227 * 1024, "shared memory budget (with the decision staging)");
+
+struct LmRowsParams {
+  RowParams rp;           // decisions; rp.part holds the CTAs' per-row statistics [CTA][128][3]
+  int vocab, nkb, n_vt, g, n_rt;
+  unsigned* rt_tickets;   // [n_rt] arrival counters of the row tiles, zero between calls
+};
+
+__global__ void __launch_bounds__(kLmThreads, 1)
+    lm_rows_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_h,
+                   const LmRowsParams p) {
+  extern __shared__ uint8_t lr_smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(lr_smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* pipe = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRPipe);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kRStages;
+  uint64_t* tmem_full = bars + 2 * kRStages;  // [2]
+  uint64_t* tmem_empty = tmem_full + 2;       // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tmem_empty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  __shared__ unsigned go;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int R = p.rp.n_rows;
+  const int rt = (int)blockIdx.x / p.g, gi = (int)blockIdx.x % p.g;
+  const int vt0 = (int)((long long)gi * p.n_vt / p.g), vt1 = (int)((long long)(gi + 1) * p.n_vt / p.g);
+  const int n_mine = vt1 - vt0;
+  const int n_it = n_mine * p.nkb;
+  const int pre = min(n_it, kRStages);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kRStages; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(&tmem_full[s], 1);
+      tc::mbar_init(&tmem_empty[s], 4);  // the four epilogue warps
+    }
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+    tc::prefetch_tensormap(&tm_w);
+    tc::prefetch_tensormap(&tm_h);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_slot, 2 * kRN);
+    tc::tmem_relinquish();
+  }
+  fdl::grid_dep_wait();
+  fdl::grid_dep_launch();
+  auto issue = [&](int it, int s) {
+    const int j = it / p.nkb, kb = it % p.nkb;
+    uint8_t* a = pipe + s * kRStage;
+    tc::mbar_arrive_expect_tx(&full[s], kRStage);
+    tc::tma_load_2d(a, &tm_h, kb * kRK, rt * kRM, &full[s]);
+    tc::tma_load_2d(a + kRA, &tm_w, kb * kRK, (vt0 + j) * kRN, &full[s]);
+  };
+  if (threadIdx.x == 0)
+    for (int it = 0; it < pre; ++it) issue(it, it);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      for (int it = pre; it < n_it; ++it) {
+        const int s = it % kRStages;
+        if (!tc::mbar_wait(&empty[s], ((uint32_t)(it / kRStages) & 1u) ^ 1u, abort_flag)) break;
+        issue(it, s);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(kRM, kRN);
+      int it = 0;
+      bool ok = true;
+      for (int j = 0; ok && j < n_mine; ++j) {
+        const int buf = j & 1;
+        // the epilogue has read this accumulator's previous tile (j - 2)
+        if (j >= 2 && !tc::mbar_wait(&tmem_empty[buf], (uint32_t)((j - 2) >> 1) & 1u, abort_flag)) break;
+        tc::fence_after_sync();
+        for (int kb = 0; kb < p.nkb; ++kb, ++it) {
+          const int s = it % kRStages;
+          if (!tc::mbar_wait(&full[s], (uint32_t)(it / kRStages) & 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t a = tc::smem_addr(pipe + s * kRStage);
+          const uint64_t ad = tc::desc_kmajor_sw128(a);
+          const uint64_t bd = tc::desc_kmajor_sw128(a + kRA);
+#pragma unroll
+          for (int k = 0; k < kRK / 16; ++k)
+            tc::mma_bf16_ss(tmem + buf * kRN, ad + 2 * k, bd + 2 * k, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+          tc::mma_commit(&empty[s]);
+        }
+        if (ok) tc::mma_commit(&tmem_full[buf]);
+      }
+      // every product issued has finished before the TMEM is freed
+      const int last = ok ? n_mine - 1 : -1;
+      if (last >= 0) {
+        long long t0 = clock64();
+        while (!tc::mbar_try_wait(&tmem_full[last & 1], (uint32_t)(last >> 1) & 1u) &&
+               clock64() - t0 < tc::kWaitBudgetCycles) {
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    // thread = window row rt * 128 + row (its TMEM lane); the row's running
+    // statistics over this CTA's vocabulary tiles, in tile order
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const uint32_t t_lane = tmem + ((uint32_t)(q * 32) << 16);
+    Stat run{-INFINITY, 0.f, 0x7fffffff};
+    for (int j = 0; j < n_mine; ++j) {
+      const int buf = j & 1;
+      const bool got = __all_sync(0xffffffffu, tc::mbar_wait(&tmem_full[buf], (uint32_t)(j >> 1) & 1u, abort_flag));
+      tc::fence_after_sync();
+      const int v0 = (vt0 + j) * kRN;
+#pragma unroll 1
+      for (int c0 = 0; c0 < kRN; c0 += 64) {
+        float v[64];
+        if (!got) break;
+        tc::tmem_ld_32x32b_x64(t_lane + buf * kRN + c0, v);
+        const int nvalid = min(64, p.vocab - (v0 + c0));
+        // the chunk's maximum (first index on ties) before any exponential
+        float m = -INFINITY;
+        int mi = 0;
+#pragma unroll
+        for (int e = 0; e < 64; ++e)
+          if (e < nvalid && v[e] > m) {
+            m = v[e];
+            mi = e;
+          }
+        if (m == -INFINITY) continue;
+        const float mb = m * kLog2e;
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+        for (int e = 0; e < 64; e += 4) {
+          a0 += e < nvalid ? ex2(fmaf(v[e], kLog2e, -mb)) : 0.f;
+          a1 += e + 1 < nvalid ? ex2(fmaf(v[e + 1], kLog2e, -mb)) : 0.f;
+          a2 += e + 2 < nvalid ? ex2(fmaf(v[e + 2], kLog2e, -mb)) : 0.f;
+          a3 += e + 3 < nvalid ? ex2(fmaf(v[e + 3], kLog2e, -mb)) : 0.f;
+        }
+        run = merge(run, Stat{m, (a0 + a1) + (a2 + a3), v0 + c0 + mi});
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&tmem_empty[buf]);  // the accumulator may take tile j + 2
+    }
+    if (rt * kRM + row < R) {
+      float* slot = p.rp.part + ((size_t)blockIdx.x * kRM + row) * 3;
+      __stcg(slot, run.m);
+      __stcg(slot + 1, run.s);
+      __stcg(slot + 2, __int_as_float(run.i));
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) tc::tmem_dealloc(tmem, 2 * kRN);
+  if (threadIdx.x == 0) {
+    if (*abort_flag) fdl::raise_error(p.rp.err, FDL_DEVERR_TIMEOUT);
+    // this CTA's statistics are released by its add; the row tile's last
+    // arrival acquires the others' (passed on by the barrier below)
+    unsigned tk;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(tk) : "l"(p.rt_tickets + rt) : "memory");
+    go = tk == (unsigned)p.g - 1u ? 1u : 0u;
+  }
+  __syncthreads();
+  if (!go) return;
+  // ---- last CTA of the row tile: each row's statistics over the g CTAs in
+  // CTA order (= vocabulary order), then the row's confidence and argmax
+  if (threadIdx.x < kRM) {
+    const int r = rt * kRM + (int)threadIdx.x;
+    if (r < R) {
+      Stat acc{-INFINITY, 0.f, 0x7fffffff};
+      for (int i = 0; i < p.g; ++i) {
+        const float* o = p.rp.part + ((size_t)(rt * p.g + i) * kRM + threadIdx.x) * 3;
+        acc = merge(acc, Stat{__ldcg(o), __ldcg(o + 1), __float_as_int(__ldcg(o + 2))});
+      }
+      // verify: row b*max_search + j holds a mask view only for j < n_search[b]
+      const bool real = p.rp.phase == 0 || r % p.rp.max_search < __ldg(p.rp.n_search + r / p.rp.max_search);
+      if (real) {
+        p.rp.out_conf[r] = acc.s > 0.f ? 1.f / acc.s : 0.f;
+        p.rp.out_arg[r] = acc.i;
+      }
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    p.rt_tickets[rt] = 0u;  // every CTA of the row tile has arrived: ready for the next call
+    unsigned tk;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(tk) : "l"(p.rp.ticket) : "memory");
+    go = tk == (unsigned)p.n_rt - 1u ? 1u : 0u;
+  }
+  __syncthreads();
+  if (!go) return;
+  // ---- the row tile that finished last: the decisions over every row
+  if (p.rp.phase == 0)
+    decide_unmask<2048, 1024>(p.rp, nullptr, nullptr, nullptr);
+  else
+    decide_verify(p.rp);
+  if (threadIdx.x == 0) *p.rp.ticket = 0u;  // ready for the next call
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 lm_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
@@ -759,6 +998,61 @@ bool lm_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Decision parameters shared by both LM-head kernels.
+void lm_decision_params(RowParams& rp, fdl_ctx* ctx, const fdl_unmask_args* a, bool verify, int R) {
+  rp.n_rows = R;
+  rp.part = ctx->lm_part;
+  rp.ticket = ctx->tickets + 2;
+  rp.err = ctx->err_word;
+  rp.B = a->B;
+  rp.max_search = a->max_search;
+  if (!verify) {
+    rp.phase = 0;
+    rp.out_conf = a->conf;
+    rp.out_arg = a->argmax;
+    rp.row_seq = a->row_seq;
+    rp.row_pos = a->row_pos;
+    rp.eps = a->eps;
+    rp.force_progress = a->force_progress;
+    rp.commit = a->commit;
+    rp.search_rows = a->search_rows;
+    rp.n_search_out = a->n_search;
+  } else {
+    rp.phase = 1;
+    rp.out_conf = a->mask_conf;
+    rp.out_arg = a->mask_argmax;
+    rp.n_search = a->n_search;
+    rp.draft_tok = a->draft_tok;
+    rp.gamma = a->gamma;
+    rp.accept = a->accept;
+    rp.n_accept = a->n_accept;
+  }
+}
+
+cudaError_t launch_lm_rows(fdl_ctx* ctx, const void* hidden, const void* w_lm, const fdl_unmask_args* a, bool verify,
+                           int R) {
+  const fdl_config& c = ctx->cfg;
+  static fdl_smem_limit smem_limit;
+  if (cudaError_t e = smem_limit.ensure((const void*)lm_rows_kernel, ctx->device, kRSmem)) return e;
+  CUtensorMap mw, mh;
+  if (!lm_map(&mw, w_lm, (uint64_t)c.vocab, c.d_model, kRN) || !lm_map(&mh, hidden, R, c.d_model, kRM))
+    return cudaErrorInvalidValue;
+  LmRowsParams p = {};
+  lm_decision_params(p.rp, ctx, a, verify, R);
+  p.vocab = c.vocab;
+  p.nkb = c.d_model / kRK;
+  p.n_vt = (c.vocab + kRN - 1) / kRN;
+  p.n_rt = (R + kRM - 1) / kRM;
+  // CTAs per row tile: the row tiles together fill the SMs, each CTA with at
+  // least one vocabulary tile
+  p.g = max(1, min(ctx->num_sms / p.n_rt, p.n_vt));
+  p.rt_tickets = ctx->lm_rt_tickets;
+  if (p.n_rt > ctx->lm_rt_ticket_count || (size_t)p.n_rt * p.g * kRM * 3 > ctx->lm_part_floats)
+    return cudaErrorInvalidValue;
+  return fdl_launch_pdl(lm_rows_kernel, dim3((unsigned)(p.n_rt * p.g)), dim3(kLmThreads), kRSmem, ctx->stream, 1, mw,
+                        mh, p);
 }
 
 }  // namespace
@@ -818,48 +1112,32 @@ cudaError_t fdl_launch_unmask_verify(fdl_ctx* ctx, const fdl_unmask_args* a) {
 
 int fdl_lm_head_max_rows() { return kLmBN; }
 
-size_t fdl_lm_partial_floats(int num_sms) { return (size_t)num_sms * kLmBN * 3; }
+size_t fdl_lm_partial_floats(int num_sms, int max_rows) {
+  // the small kernel: one set of <= 64 rows' statistics per CTA; the many-row
+  // kernel: 128 rows per CTA over n_rt x g <= max(SMs, row tiles) CTAs
+  const size_t n_rt = (size_t)(max_rows + kRM - 1) / kRM;
+  const size_t small = (size_t)num_sms * kLmBN * 3;
+  const size_t rows = (n_rt > (size_t)num_sms ? n_rt : (size_t)num_sms) * kRM * 3;
+  return small > rows ? small : rows;
+}
+
+int fdl_lm_row_tiles(int max_rows) { return (max_rows + kRM - 1) / kRM; }
 
 cudaError_t fdl_launch_lm_head(fdl_ctx* ctx, const void* hidden, const void* w_lm, const fdl_unmask_args* a,
                                bool verify) {
   const fdl_config& c = ctx->cfg;
   const int R = verify ? a->B * a->max_search : a->R_w;
-  if (c.dtype != FDL_BF16 || R < 1 || R > kLmBN || c.d_model % kLmBK != 0 || !ctx->lm_part)
+  if (c.dtype != FDL_BF16 || R < 1 || R > c.max_rows || c.d_model % kLmBK != 0 || !ctx->lm_part)
     return cudaErrorNotSupported;
   if ((reinterpret_cast<uintptr_t>(hidden) | reinterpret_cast<uintptr_t>(w_lm)) & 15) return cudaErrorMisalignedAddress;
+  if (R > kLmBN) return launch_lm_rows(ctx, hidden, w_lm, a, verify, R);
   static fdl_smem_limit smem_limit;
   if (cudaError_t e = smem_limit.ensure((const void*)lm_head_kernel, ctx->device, kLmSmem)) return e;
   CUtensorMap mw, mh;
   if (!lm_map(&mw, w_lm, (uint64_t)c.vocab, c.d_model, kLmBM) || !lm_map(&mh, hidden, R, c.d_model, kLmBN))
     return cudaErrorInvalidValue;
   LmParams p = {};
-  p.rp.n_rows = R;
-  p.rp.part = ctx->lm_part;
-  p.rp.ticket = ctx->tickets + 2;
-  p.rp.err = ctx->err_word;
-  p.rp.B = a->B;
-  p.rp.max_search = a->max_search;
-  if (!verify) {
-    p.rp.phase = 0;
-    p.rp.out_conf = a->conf;
-    p.rp.out_arg = a->argmax;
-    p.rp.row_seq = a->row_seq;
-    p.rp.row_pos = a->row_pos;
-    p.rp.eps = a->eps;
-    p.rp.force_progress = a->force_progress;
-    p.rp.commit = a->commit;
-    p.rp.search_rows = a->search_rows;
-    p.rp.n_search_out = a->n_search;
-  } else {
-    p.rp.phase = 1;
-    p.rp.out_conf = a->mask_conf;
-    p.rp.out_arg = a->mask_argmax;
-    p.rp.n_search = a->n_search;
-    p.rp.draft_tok = a->draft_tok;
-    p.rp.gamma = a->gamma;
-    p.rp.accept = a->accept;
-    p.rp.n_accept = a->n_accept;
-  }
+  lm_decision_params(p.rp, ctx, a, verify, R);
   p.vocab = c.vocab;
   p.nkb = c.d_model / kLmBK;
   p.n_tiles = (c.vocab + kLmBM - 1) / kLmBM;

@@ -120,7 +120,7 @@ def test_lm_head_unmask_limits():
     d, V = 256, 1000
     ctx = fdl.fdl_create(d, 2, 128, 5e5, 2, 64, 0, 64, 1, 128, V, "bf16")
     w = torch.zeros((V, d), dtype=torch.bfloat16, device="cuda")
-    for R in (65, 0):
+    for R in (129, 0):            # max_rows is 128
         h = torch.zeros((max(R, 1), d), dtype=torch.bfloat16, device="cuda")
         hh = h if R else h[:0]
         with pytest.raises(fdl.FdlError):
@@ -130,6 +130,12 @@ def test_lm_head_unmask_limits():
     got = _run(ctx, h, w, np.zeros(64, np.int32), np.arange(64, dtype=np.int32), 1, 0.9, False, 8)
     np.testing.assert_allclose(got[0], 1.0 / V, rtol=1e-5)
     assert got[1].tolist() == [0] * 64
+    assert got[4].tolist() == [8] and got[3][0].tolist() == list(range(8))
+    # 100 rows take the many-row kernel (128-row tiles): the same closed form
+    h = torch.zeros((100, d), dtype=torch.bfloat16, device="cuda")
+    got = _run(ctx, h, w, np.zeros(100, np.int32), np.arange(100, dtype=np.int32), 1, 0.9, False, 8)
+    np.testing.assert_allclose(got[0], 1.0 / V, rtol=1e-5)
+    assert got[1].tolist() == [0] * 100
     assert got[4].tolist() == [8] and got[3][0].tolist() == list(range(8))
     ctx.close()
 
@@ -203,7 +209,7 @@ def test_lm_head_verify_limits():
     z = torch.zeros(80, dtype=torch.int32, device="cuda")
     f = torch.zeros(80, dtype=torch.float32, device="cuda")
     u = torch.zeros(80, dtype=torch.uint8, device="cuda")
-    for B, ms, status in ((13, 5, fdl.FDL_ERR_UNSUPPORTED), (1, 0, fdl.FDL_ERR_INVALID_ARG)):
+    for B, ms, status in ((13, 5, fdl.FDL_ERR_INVALID_ARG), (1, 0, fdl.FDL_ERR_INVALID_ARG)):
         with pytest.raises(fdl.FdlError) as ei:
             ctx.lm_head_verify(h, w, B, ms, n_search=z, draft_tok=z, gamma=0.8, accept=u, n_accept=z,
                                mask_conf=f, mask_argmax=z)
@@ -216,4 +222,102 @@ def test_lm_head_verify_limits():
     ctx.sync_status()
     assert (H.host(nacc) == 0).all() and (H.host(u[:64]) == 0).all()
     np.testing.assert_allclose(H.host(f[:64]), 1.0 / V, rtol=1e-6)
+    ctx.close()
+
+
+def _clear_sequences(conf, logits, row_seq, B, threshold):
+    """Sequences whose float64 values hold no near-tie that fp32 could decide
+    the other way: a top-2 logit gap below 1e-3, a confidence within 1e-5 of
+    the (float32) threshold, or two confidences of the sequence within 1e-6
+    relative of each other."""
+    conf = np.asarray(conf, np.float64)
+    top2 = np.sort(logits, axis=1)[:, -2:]
+    gap_ok = (top2[:, 1] - top2[:, 0]) >= 1e-3
+    thr_ok = np.abs(conf - np.float64(np.float32(threshold))) >= 1e-5
+    out = []
+    for b in range(B):
+        rows = np.nonzero(np.asarray(row_seq) == b)[0]
+        c = np.sort(conf[rows])
+        ties = len(c) > 1 and (np.diff(c) < 1e-6 * c[1:]).any()
+        out.append(bool(gap_ok[rows].all() and thr_ok[rows].all() and not ties))
+    return np.array(out)
+
+
+@pytest.mark.slow
+def test_lm_head_unmask_flash_verify_scale():
+    """The Flash-Verify stress scale: 32 sequences x 32 window rows (1024
+    rows, the many-row kernel) over the LLaDA vocabulary and width, every
+    row's confidence against the float64 oracle, the decisions exactly the
+    oracle's for every sequence clear of a near-tie (and the rule on the
+    kernel's confidences for the others)."""
+    d, V, B, W, ms, eps = 4096, 126464, 32, 32, 16, 0.9
+    R = B * W
+    hidden, w, ids = synth.lm_head_case(seed=1031, vocab=V, d=d, rows=R, planted=0.6)
+    row_seq = np.repeat(np.arange(B), W).astype(np.int32)
+    row_pos = np.tile(512 + np.arange(W), B).astype(np.int32)
+    ctx = _ctx(d, V, B, R)
+    got = _run(ctx, H.dev(hidden), H.dev(w), row_seq, row_pos, B, eps, True, ms)
+    logits = oracle.lm_head_logits(hidden.values(), synth.bf16_bits_to_f32(w.data))
+    ref = oracle.unmask(logits, row_seq, row_pos, B, eps, True, ms)
+    conf, arg, com, srows, nsr = got
+    H.assert_close(conf, ref["conf"], "f32", "confidences at 1024 rows")
+    top2 = np.sort(logits, axis=1)[:, -2:]
+    clear_rows = (top2[:, 1] - top2[:, 0]) > 1e-3
+    assert np.array_equal(arg[clear_rows], ref["argmax"][clear_rows])
+    want = _decide(conf, row_seq, row_pos, B, eps, True, ms)
+    assert com.tolist() == want["commit"].tolist() and srows.tolist() == want["search_rows"].tolist()
+    clear = _clear_sequences(ref["conf"], logits, row_seq, B, eps)
+    assert clear.sum() >= B // 2, clear.sum()
+    for b in np.nonzero(clear)[0]:
+        rows = np.nonzero(row_seq == b)[0]
+        assert com[rows].tolist() == ref["commit"][rows].tolist(), b
+        assert srows[b].tolist() == ref["search_rows"][b].tolist(), b
+        assert nsr[b] == ref["n_search"][b], b
+    assert np.array_equal(arg[ids >= 0], ids[ids >= 0])
+    # the fixed-order reductions repeat bit for bit
+    again = _run(ctx, H.dev(hidden), H.dev(w), row_seq, row_pos, B, eps, True, ms)
+    for x, y in zip(got, again):
+        assert np.array_equal(x, y)
+    ctx.close()
+
+
+@pytest.mark.slow
+def test_lm_head_verify_flash_verify_scale():
+    """32 sequences x 16 mask views (512 rows) over the LLaDA vocabulary:
+    the verify-side fused LM head against the float64 oracle's acceptance."""
+    torch = H.torch_mod()
+    d, V, B, ms, gamma = 4096, 126464, 32, 16, 0.8
+    R = B * ms
+    hidden, w, _ = synth.lm_head_case(seed=1032, vocab=V, d=d, rows=R, planted=1.0)
+    logits = oracle.lm_head_logits(hidden.values(), synth.bf16_bits_to_f32(w.data))
+    rng = np.random.default_rng(1033)
+    n_search = rng.integers(0, ms + 1, B).astype(np.int32)
+    _, a_o = oracle.row_confidence(logits)
+    draft = a_o.astype(np.int32).copy()
+    flip = rng.random(R) < 0.15                         # some drafts disagree with the mask view
+    draft[flip] = (draft[flip] + 1) % V
+    want = oracle.verify(logits, draft, n_search, gamma, B, ms)
+    ctx = _ctx(d, V, B, R)
+    mc = torch.full((R,), -5.0, dtype=torch.float32, device="cuda")
+    ma = torch.full((R,), -5, dtype=torch.int32, device="cuda")
+    acc = torch.full((R,), 7, dtype=torch.uint8, device="cuda")
+    nacc = torch.full((B,), -1, dtype=torch.int32, device="cuda")
+    ctx.lm_head_verify(H.dev(hidden), H.dev(w), B, ms, n_search=H.ints(n_search), draft_tok=H.ints(draft),
+                       gamma=gamma, accept=acc, n_accept=nacc, mask_conf=mc, mask_argmax=ma)
+    ctx.sync_status()
+    mc, ma, acc, nacc = H.host(mc), H.host(ma), H.host(acc), H.host(nacc)
+    valid = np.array([b * ms + j for b in range(B) for j in range(n_search[b])])
+    rest = np.setdiff1d(np.arange(R), valid)
+    assert (mc[rest] == -5.0).all() and (ma[rest] == -5).all()
+    H.assert_close(mc[valid], want["mask_conf"][valid], "f32", "mask-view confidences at 512 rows")
+    top2 = np.sort(logits[valid], axis=1)[:, -2:]
+    assert ((top2[:, 1] - top2[:, 0]) > 1e-3).all()     # planted rows: clear argmaxes
+    assert np.array_equal(ma[valid], want["mask_argmax"][valid])
+    near = np.abs(want["mask_conf"] - np.float64(np.float32(gamma))) < 1e-5
+    for b in range(B):
+        rows = np.arange(b * ms, b * ms + n_search[b])
+        if not near[rows].any():
+            assert nacc[b] == want["n_accept"][b], b
+            assert acc[b * ms:(b + 1) * ms].tolist() == want["accept"][b * ms:(b + 1) * ms].tolist(), b
+    assert want["n_accept"].sum() > 0 and (want["n_accept"] < n_search).any()
     ctx.close()
