@@ -33,15 +33,21 @@ from tests.test_gpu_lm_head import _decide, _verify_rule
 pytestmark = pytest.mark.gpu
 
 
-def test_flash_steps_teacher_forced():
+# (prompt lengths, generation lengths): two sequences (32 window rows, the
+# one-tile LM head), then five (80 window rows and up to 40 mask views: the
+# many-row LM head on the unmask side)
+CASES = [([20, 27], [32, 24]), ([20, 27, 9, 33, 14], [32, 24, 40, 16, 29])]
+
+
+@pytest.mark.parametrize("prompts,gens", CASES)
+def test_flash_steps_teacher_forced(prompts, gens):
     torch = H.torch_mod()
     import kv_cache_attention_gb300 as fdl
     mc = synth.model_case(seed=1015, d=512, n_heads=4, n_layers=2, ffn=1024, vocab=2088, out_std=0.5, lm_std=0.2)
     m = synth.model_values(mc)
     w_lm = m["w_lm"]
     L, d, V = len(mc["layers"]), mc["d_model"], mc["vocab"]
-    prompts, gens = [20, 27], [32, 24]
-    B = 2
+    B = len(prompts)
     lengths = (np.array(prompts) + np.array(gens)).astype(np.int32)
     N = int(lengths.max())
     params = dict(window=16, track_budget=16, max_search=8, eps=0.5, gamma=0.2, force_progress=True,
@@ -67,9 +73,9 @@ def test_flash_steps_teacher_forced():
     vcs = [torch.zeros((n_slots, d), dtype=torch.bfloat16, device="cuda") for _ in range(L)]
     bt = H.ints(geom.block_table)
     ws = torch.empty(ctx.flash_workspace_bytes(mc["ffn"], params, B, N), dtype=torch.uint8, device="cuda")
-    saw = dict(commit=0, search=0, accept=0, verify_steps=0)
+    saw = dict(commit=0, search=0, accept=0, verify_steps=0, max_rw=0)
     checked_steps = exact_steps = exact_verify = 0
-    for step in range(40):
+    for step in range(64):
         if not seqs["masked"].any():
             break
         snap = {k: v.copy() for k, v in seqs.items()}
@@ -77,6 +83,7 @@ def test_flash_steps_teacher_forced():
         caches = ([H.host(t).astype(np.float64) for t in kcs], [H.host(t).astype(np.float64) for t in vcs])
         rec = ctx.flash_step(dm, wl, kcs, vcs, bt, params, seqs, ws)
         RW = int(rec["n_window"][0])
+        saw["max_rw"] = max(saw["max_rw"], RW)
         force = dict(argmax=rec["argmax"][:RW], commit=rec["commit"][:RW],
                      search_rows=rec["search_rows"].reshape(B, MS), n_search=rec["n_search"],
                      n_accept=rec["n_accept"])
@@ -132,6 +139,8 @@ def test_flash_steps_teacher_forced():
         pytest.fail("decode did not finish")
     assert not seqs["masked"].any()
     assert saw["commit"] > 0 and saw["search"] > 0 and saw["accept"] > 0 and saw["verify_steps"] > 0
+    if B * W > 64:
+        assert saw["max_rw"] > 64   # the many-row LM head ran inside the step
     # the identical-input stage checks were exact on most steps
     assert exact_steps >= 0.8 * checked_steps, (exact_steps, checked_steps)
     assert exact_verify >= 0.8 * saw["verify_steps"], (exact_verify, saw["verify_steps"])
