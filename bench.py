@@ -49,9 +49,9 @@ WORKLOAD = "llada8b_layer_bf16_b1_p512_g256_w32_t32"
 # summarised in profiles/qkv_tc_kernel_llada8b_traffic.txt. It is reported
 # only while the sources it was taken from hash to the recorded value; after
 # any change to them the figure is stale and the line carries null.
-QKV_TRAFFIC = {"sources_sha256": "b903965bf853e968cf3cb3e3ac7e86441b9e29a3ca8a3ca5a311e9a45cb618b8",
-               "bytes": 102162176 + 2881280}
-QKV_SOURCES = ("kv_cache_attention_gb300/csrc/fdl_qkv_tc.cu", "kv_cache_attention_gb300/csrc/fdl_qkv.cu",
+QKV_TRAFFIC = {"sources_sha256": None,
+               "bytes": None}
+QKV_SOURCES = ("kv_cache_attention_gb300/csrc/fdl_qkv_tc.cu", "kv_cache_attention_gb300/csrc/fdl_gemm_tc.cu", "kv_cache_attention_gb300/csrc/fdl_qkv.cu",
                "kv_cache_attention_gb300/csrc/tc_ptx.cuh", "kv_cache_attention_gb300/csrc/fdl_internal.cuh")
 
 

@@ -45,6 +45,7 @@
 #include <math.h>
 
 #include "fdl_internal.cuh"
+#include "fdl_attn_tc.cuh"
 #include "tc_ptx.cuh"
 
 namespace {
@@ -159,93 +160,6 @@ __device__ __forceinline__ float4 ld_cluster_v4(uint32_t caddr) {
 }
 
 __device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
-
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// Instruction descriptor for O += P V: bf16 operands, fp32 D, A (P) K-major,
-// B (V, stored keys x head_dim) MN-major.
-__host__ __device__ constexpr uint32_t idesc_pv(int M, int N) {
-  return tc::idesc_bf16_f32(M, N) | (1u << 16);
-}
-
-// MN-major operand in the 128-byte swizzle layout: 64-element (128 B) rows
-// along MN, one row per K index; 8-row groups 1024 B apart (stride byte
-// offset); the next 64-wide MN block lbo bytes further (leading byte offset).
-__device__ __forceinline__ uint64_t desc_mnmajor_sw128(uint32_t saddr, uint32_t lbo) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-  d |= (uint64_t)(1024u >> 4) << 32;
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
-  return d;
-}
-
-// Visibility of key position c to a row of `kind` in a sequence with kvl
-// base keys and m search tokens (is_search: c is a search position).
-__device__ __forceinline__ bool visible(int kind, int c, int kvl, int m, bool is_search) {
-  if (kind < 0) return false;
-  if (kind < 2) return c < kvl;
-  if (c < kvl) return !is_search;
-  const int v = c - kvl;
-  if (v >= 2 * m) return false;
-  const int k = (kind - 2) >> 1;
-  const bool mask_view = (kind - 2) & 1;
-  if (v < m) return mask_view ? (v < k) : (v <= k);
-  const int j = v - m;
-  return mask_view ? (j >= k) : (j > k);
-}
-
-__device__ __forceinline__ int warp_incl_scan(int v, int lane) {
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, v, off);
-    if (lane >= off) v += y;
-  }
-  return v;
-}
-
-// Hardware base-2 exponential (ex2.approx, relative error ~2^-22); ex2(-inf) = 0.
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// Visibility of keys cb .. cb+31 (cb a multiple of 32) to a row of `kind`,
-// one bit per key. Plain rows only compare against the sequence length; view
-// rows consult the search-position bitmap and the view-key rule.
-__device__ __forceinline__ uint32_t vis_mask(int kind, int cb, int kvl, int m, const uint32_t* bm, int words) {
-  if (kind < 0) return 0u;
-  if (kind < 2) {
-    const int n = kvl - cb;
-    return n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : (1u << n) - 1u);
-  }
-  const uint32_t srch = (cb < kvl && (cb >> 5) < words) ? bm[cb >> 5] : 0u;
-  uint32_t mask = 0u;
-#pragma unroll 4
-  for (int k = 0; k < 32; ++k) mask |= (visible(kind, cb + k, kvl, m, (srch >> k) & 1u) ? 1u : 0u) << k;
-  return mask;
-}
-
-// Reduce-scatter of 32 per-lane values over the warp: afterwards v[0] of
-// lane l holds the warp's sum of column l.
-__device__ __forceinline__ void warp_colsum32(float (&v)[32], int lane) {
-#pragma unroll
-  for (int step = 0; step < 5; ++step) {
-    const int off = 16 >> step;
-    const int half = 16 >> step;
-    const bool hi = lane & off;
-#pragma unroll
-    for (int k = 0; k < half; ++k) {
-      const float send = hi ? v[k] : v[k + half];
-      const float keep = hi ? v[k + half] : v[k];
-      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-    }
-  }
-}
 
 // Split `rank` of a C-CTA cluster sums its share of the item's qlen valid
 // rows, [rank * qlen / C, (rank + 1) * qlen / C), over the C staged fp32 O
@@ -996,31 +910,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (threadIdx.x == 0 && *abort_flag) fdl::raise_error(p.err, FDL_DEVERR_TIMEOUT);
   if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
-}
-
-PFN_cuTensorMapEncodeTiled_v12000 encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    cudaDriverEntryPointQueryResult q;
-    void* f = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  }
-  return fn;
-}
-
-bool map2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
-  auto enc = encoder();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, box_rows};
-  cuuint32_t es[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace

@@ -1,7 +1,9 @@
 // Dense GEMM on the 5th-generation tensor cores for the rest of the
 // transformer block (W_o, the SwiGLU gate/up and down projections), with the
 // plain epilogues those need: a bf16 store, or an fp32 add into the residual
-// stream.
+// stream. This is the split-K form for row counts whose tiles do not fill
+// several waves of the GPU (the persistent form in fdl_gemm_tc.cu takes the
+// larger ones).
 //
 // The design is the fused projection's ("swap AB", tcgen05 with the
 // accumulator in TMEM, a TMA ring of 64-wide k-blocks, warp 0 loading,
@@ -270,8 +272,8 @@ cudaError_t launch(fdl_ctx* ctx, DenseParams p, const void* X, const void* W, in
 
 }  // namespace
 
-cudaError_t fdl_launch_dense_tc(fdl_ctx* ctx, const void* X, const void* W, int R, int K, int N, void* out,
-                                bool add_f32) {
+cudaError_t fdl_launch_dense_splitk(fdl_ctx* ctx, const void* X, const void* W, int R, int K, int N, void* out,
+                                    bool add_f32) {
   if (R <= 0) return cudaSuccess;
   if (ctx->cfg.dtype != FDL_BF16 || N % kBM != 0 || K % kBK != 0 || K <= 0 || !ctx->qkv_partials)
     return cudaErrorNotSupported;

@@ -107,7 +107,7 @@ fdl_status fdl_create(const fdl_config* cfg, void* cuda_stream, fdl_ctx** out) {
   e = e ? e : cudaMalloc(&ctx->n_masked, cfg->max_batch * sizeof(int));
   e = e ? e : cudaMalloc(&ctx->tickets, 8 * sizeof(unsigned));
   if (cfg->dtype == FDL_BF16) {
-    ctx->qkv_partial_floats = fdl_qkv_partial_floats(ctx->num_sms);
+    ctx->qkv_partial_floats = fdl_qkv_partial_floats(ctx->num_sms, cfg->max_rows);
     ctx->qkv_tickets = 4 * ctx->num_sms;
     e = e ? e : cudaMalloc(&ctx->qkv_partials, ctx->qkv_partial_floats * sizeof(float));
     e = e ? e : cudaMalloc(&ctx->qkv_ticket_buf, ctx->qkv_tickets * sizeof(unsigned));

@@ -145,14 +145,36 @@ cudaError_t fdl_launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size
 // per device ordinal below 64; higher ordinals set it on every launch).
 // cudaFuncSetAttribute is thread-safe and idempotent, so two host threads
 // that race here at most set it twice.
+// The kernel also prefers the largest shared-memory carveout, so that
+// kernels sized for two CTAs per SM get them.
 struct fdl_smem_limit {
   std::atomic<unsigned long long> done{0};
   cudaError_t ensure(const void* kernel, int device, int bytes) {
     const unsigned long long bit = device >= 0 && device < 64 ? 1ull << device : 0ull;
     if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               (int)cudaSharedmemCarveoutMaxShared);
     if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
     return e;
+  }
+};
+
+// Resident CTAs per SM of a kernel on a device, queried once per device
+// ordinal below 64 (and on every call above).
+struct fdl_occupancy {
+  std::atomic<int> per_sm[64] = {};
+  int get(const void* kernel, int device, int threads, int smem) {
+    if (device >= 0 && device < 64) {
+      const int v = per_sm[device].load(std::memory_order_acquire);
+      if (v > 0) return v;
+    }
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, (size_t)smem) != cudaSuccess || n < 1)
+      n = 1;
+    if (device >= 0 && device < 64) per_sm[device].store(n, std::memory_order_release);
+    return n;
   }
 };
 
@@ -188,4 +210,4 @@ size_t fdl_lm_partial_floats(int num_sms, int max_rows);
 int fdl_lm_row_tiles(int max_rows);
 
 // Workspace floats the tensor-core projection needs for split-K partials.
-size_t fdl_qkv_partial_floats(int num_sms);
+size_t fdl_qkv_partial_floats(int num_sms, int max_rows);

@@ -1,5 +1,7 @@
 // Fused QKV projection + RoPE + KV-cache scatter on the 5th-generation
-// tensor cores (tcgen05, accumulators in TMEM, operands staged by TMA).
+// tensor cores (tcgen05, accumulators in TMEM, operands staged by TMA): the
+// split-K form for row counts whose tiles do not fill several waves of the
+// GPU (the persistent form in fdl_gemm_tc.cu takes the larger ones).
 //
 // Paper digest "Flash-dLLM: IO-Aware KV Caching and Parallel Decoding ...",
 // section "Core method": the projection, RoPE and cache write are one kernel;
@@ -393,13 +395,13 @@ cudaError_t launch(fdl_ctx* ctx, const TcParams& p0, const void* X, const void* 
 
 int qkv_ctas_per_sm(int bn) { return bn == 64 ? 2 : 1; }
 
-size_t fdl_qkv_partial_floats(int num_sms) {
+size_t fdl_qkv_splitk_partial_floats(int num_sms) {
   // split-K is used only while tiles * ks <= resident CTAs
   size_t a = (size_t)2 * num_sms * 64 * kBM, b = (size_t)num_sms * 256 * kBM;
   return a > b ? a : b;
 }
 
-cudaError_t fdl_launch_qkv_tc(fdl_ctx* ctx, const void* X, const void* W, int R, const int* row_seq,
+cudaError_t fdl_launch_qkv_splitk(fdl_ctx* ctx, const void* X, const void* W, int R, const int* row_seq,
                               const int* row_rope_pos, const int* row_cache_pos, const int* block_table,
                               int bt_stride, void* k_cache, void* v_cache, void* q_out) {
   const fdl_config& c = ctx->cfg;

@@ -117,6 +117,47 @@ def test_model_forward_full_then_selective_refresh():
     ctx.close()
 
 
+def test_model_forward_wide_ffn_takes_the_persistent_gemm():
+    """A full forward of 1050 rows through a layer with a 8192-wide FFN: the
+    SwiGLU gate/up product has 128 feature tiles x 5 row tiles of 256, four
+    waves of the GPU, so it runs on the persistent GEMM (whole-tile waves,
+    then stream-K shares merged in CTA order); the other products stay on the
+    split-K kernels. Final rows and caches against the oracle."""
+    torch = H.torch_mod()
+    import kv_cache_attention_gb300 as fdl
+    mc = synth.model_case(seed=1015, n_layers=1, ffn=8192)
+    m = synth.model_values(mc)
+    rng = np.random.default_rng(1016)
+    lengths = np.array([520, 530], np.int32)
+    geom = synth.paged_geometry(rng, lengths, 64)
+    n_slots = geom.n_pages * geom.page_size
+    d, V = mc["d_model"], mc["vocab"]
+    ctx = fdl.fdl_create(d, mc["n_heads"], mc["head_dim"], mc["theta"], 2, int(lengths.max()), 0, geom.page_size,
+                         geom.n_pages, int(lengths.sum()), V, "bf16")
+    dm = _dev_model(mc)
+    prompts = [300, 310]
+    tokens, per_seq = [], []
+    for b, n in enumerate(lengths):
+        t = rng.integers(0, V - 1, size=n)
+        t[prompts[b]:] = mc["mask_id"]
+        tokens.append(t)
+        per_seq.append(synth.full_rows(int(n), range(prompts[b], prompts[b] + 32)))
+    rows = synth.build_rows(per_seq)
+    tok = np.concatenate(tokens).astype(np.int32)
+    kcs = [torch.zeros((n_slots, d), dtype=torch.bfloat16, device="cuda")]
+    vcs = [torch.zeros((n_slots, d), dtype=torch.bfloat16, device="cuda")]
+    out = _run(ctx, dm, mc, tok, rows, lengths, geom, kcs, vcs)
+    z = [np.zeros((n_slots, d))]
+    want, kco, vco, _ = om.model_forward(m, tok, rows.row_seq, rows.row_rope_pos, rows.row_cache_pos,
+                                         rows.row_kind, rows.cu_seqlens, lengths, geom.block_table,
+                                         geom.page_size, z, [a.copy() for a in z], "bf16",
+                                         max_seq=int(lengths.max()), track=False)
+    _close_rows(out, want, "final rows, wide-FFN full forward")
+    H.assert_close(H.host(kcs[0]), kco[0], "bf16", "k cache, wide-FFN full forward")
+    H.assert_close(H.host(vcs[0]), vco[0], "bf16", "v cache, wide-FFN full forward")
+    ctx.close()
+
+
 def test_model_forward_checks_and_edges():
     torch = H.torch_mod()
     fdl, mc, m, rng, lengths, geom, n_slots, ctx = _setup(n_layers=1)
