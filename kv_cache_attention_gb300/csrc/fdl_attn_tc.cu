@@ -486,6 +486,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (C > 1) tc::cluster_wait();  // matches the setup arrive
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // The readiness checks are non-blocking (mbarrier.test_wait): a blocking
+    // try_wait suspends the thread on the one barrier it tests, however soon
+    // another product's operands land.
     // Issues whichever product is ready: O_g += P V for the next tile whose P
     // and V have landed (first, since it frees a P tile), else the next S =
     // Q K^T whose K tile and S buffer are free. Neither kind waits for the
@@ -500,8 +503,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       long long t_last = clock64();
       while (ok && pi < n_my) {
         bool progressed = false;
-        if (tc::mbar_try_wait(&p_full[pi & 1], (uint32_t)(pi >> 1) & 1u) &&
-            tc::mbar_try_wait(&v_full[pi % kVS], (uint32_t)(pi / kVS) & 1u)) {
+        if (tc::mbar_test_wait(&p_full[pi & 1], (uint32_t)(pi >> 1) & 1u) &&
+            tc::mbar_test_wait(&v_full[pi % kVS], (uint32_t)(pi / kVS) & 1u)) {
           tc::fence_after_sync();
           const int g = pi & 1;
           const uint32_t av = tc::smem_addr(vring + (pi % kVS) * VT_BYTES);
@@ -515,8 +518,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++pi;
           progressed = true;
         }
-        if (si < n_s && tc::mbar_try_wait(&k_full[si % kKS], (uint32_t)(si / kKS) & 1u) &&
-            (si < kSB || tc::mbar_try_wait(&s_free[si % kSB], (uint32_t)((si - kSB) / kSB) & 1u))) {
+        if (si < n_s && tc::mbar_test_wait(&k_full[si % kKS], (uint32_t)(si / kKS) & 1u) &&
+            (si < kSB || tc::mbar_test_wait(&s_free[si % kSB], (uint32_t)((si - kSB) / kSB) & 1u))) {
           tc::fence_after_sync();
           const int sb = si % kSB;
           const uint32_t ak = tc::smem_addr(kring + (si % kKS) * KT_BYTES);
@@ -914,6 +917,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
+bool fdl_attn_pair_applies(int R, int B, int C);
+cudaError_t fdl_launch_attn_pair(fdl_ctx* ctx, const void* q, const void* k_cache, const void* v_cache,
+                                 const int* block_table, int bt_stride, const int* cu_seqlens_q, const int* kv_len,
+                                 int B, int R, const int* row_kind, const int* search_pos, int search_ld,
+                                 const int* n_search, int max_search_tokens, void* o_out, float* lse_out, float* track,
+                                 int track_ld, int* worklist_out);
+
 bool fdl_attn_tc_supported(const fdl_config& c) {
   // head_dim 128, bf16, and every 64-key tile inside one page: pages are a
   // multiple of 64 slots, or one page holds a whole sequence plus its views
@@ -977,6 +987,11 @@ cudaError_t fdl_launch_attn_tc(fdl_ctx* ctx, const void* q, const void* k_cache,
   int C = 1;
   while (C < kMaxC && est_items * c.n_heads * (2 * C) <= ctx->num_sms) C *= 2;
   p.C = C;
+  // sequences of two or more query tiles without a KV split: two tiles per CTA
+  if (decode && fdl_attn_pair_applies(R, B, C))
+    return fdl_launch_attn_pair(ctx, q, k_cache, v_cache, block_table, bt_stride, cu_seqlens_q, kv_len, B, R,
+                                row_kind, search_pos, search_ld, n_search, max_search_tokens, o_out, lse_out, track,
+                                track_ld, worklist_out);
   // grid (split, head, item): items vary slowest, so the CTAs of real items
   // are scheduled before any idle tail. Sequence b contributes
   // ceil(rows_b / 128) items, and summed over the sequences with rows that
