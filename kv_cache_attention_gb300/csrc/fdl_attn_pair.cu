@@ -530,17 +530,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 64; ++e) x[e] = 0.f;
         return 0.f;
       }
+      const float nm = -m;
       float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
       for (int e = 0; e < 64; e += 4) {
-        x[e] = ex2(fmaf(x[e], sc, -m));
-        x[e + 1] = ex2(fmaf(x[e + 1], sc, -m));
-        x[e + 2] = ex2(fmaf(x[e + 2], sc, -m));
-        x[e + 3] = ex2(fmaf(x[e + 3], sc, -m));
-        s0 += x[e];
-        s1 += x[e + 1];
-        s2 += x[e + 2];
-        s3 += x[e + 3];
+        ffma2(x[e], x[e + 1], x[e], x[e + 1], sc, sc, nm, nm);
+        ffma2(x[e + 2], x[e + 3], x[e + 2], x[e + 3], sc, sc, nm, nm);
+        x[e] = ex2(x[e]);
+        x[e + 1] = ex2(x[e + 1]);
+        x[e + 2] = ex2(x[e + 2]);
+        x[e + 3] = ex2(x[e + 3]);
+        fadd2(s0, s1, s0, s1, x[e], x[e + 1]);
+        fadd2(s2, s3, s2, s3, x[e + 2], x[e + 3]);
       }
       return (s0 + s1) + (s2 + s3);
     };
