@@ -51,7 +51,7 @@ WORKLOAD = "llada8b_layer_bf16_b1_p512_g256_w32_t32"
 # any change to them the figure is stale and the line carries null.
 QKV_TRAFFIC = {"sources_sha256": None,
                "bytes": None}
-QKV_SOURCES = ("kv_cache_attention_gb300/csrc/fdl_qkv_tc.cu", "kv_cache_attention_gb300/csrc/fdl_gemm_tc.cu", "kv_cache_attention_gb300/csrc/fdl_qkv.cu",
+QKV_SOURCES = ("kv_cache_attention_gb300/csrc/fdl_qkv_tc.cu", "kv_cache_attention_gb300/csrc/fdl_gemm_tc.cu", "kv_cache_attention_gb300/csrc/fdl_gemm_stream.cu", "kv_cache_attention_gb300/csrc/fdl_qkv.cu",
                "kv_cache_attention_gb300/csrc/tc_ptx.cuh", "kv_cache_attention_gb300/csrc/fdl_internal.cuh")
 
 

@@ -12,8 +12,10 @@
 //   dense             out (+)= X W^T for the rest of the transformer block
 //                     (W_o, the SwiGLU gate/up and down projections): a bf16
 //                     store, or an fp32 add into the residual stream.
-// Smaller row counts take the split-K kernels (fdl_qkv_tc.cu,
-// fdl_dense_tc.cu); fdl_launch_qkv_tc and fdl_launch_dense_tc below choose.
+// Up to 64 rows take the weight-streaming kernels (fdl_gemm_stream.cu), the
+// row counts between those and four waves of tiles the split-K kernels
+// (fdl_qkv_tc.cu, fdl_dense_tc.cu); fdl_launch_qkv_tc and
+// fdl_launch_dense_tc below choose.
 //
 // Orientation ("swap AB"): a tile is 128 output features on the TMEM lanes
 // against 256 rows on the TMEM columns. A projection tile covers whole
@@ -677,6 +679,9 @@ cudaError_t fdl_launch_qkv_tc(fdl_ctx* ctx, const void* X, const void* W, int R,
       (reinterpret_cast<uintptr_t>(v_cache) & 15))
     return cudaErrorNotSupported;
   if (R <= 0) return cudaSuccess;
+  if (fdl_stream_gemm_applies(ctx, R, c.d_model, 3 * c.d_model))
+    return fdl_launch_qkv_stream(ctx, X, W, R, row_seq, row_rope_pos, row_cache_pos, block_table, bt_stride,
+                                 k_cache, v_cache, q_out);
   if (!persistent_pays(ctx, R, 3 * c.d_model))
     return fdl_launch_qkv_splitk(ctx, X, W, R, row_seq, row_rope_pos, row_cache_pos, block_table, bt_stride,
                                  k_cache, v_cache, q_out);
@@ -708,6 +713,7 @@ cudaError_t fdl_launch_dense_tc(fdl_ctx* ctx, const void* X, const void* W, int 
     return cudaErrorNotSupported;
   if ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(W) | reinterpret_cast<uintptr_t>(out)) & 15)
     return cudaErrorMisalignedAddress;
+  if (fdl_stream_gemm_applies(ctx, R, K, N)) return fdl_launch_dense_stream(ctx, X, W, R, K, N, out, add_f32);
   if (!persistent_pays(ctx, R, N)) return fdl_launch_dense_splitk(ctx, X, W, R, K, N, out, add_f32);
   SkParams p = {};
   p.R = R;

@@ -211,3 +211,13 @@ int fdl_lm_row_tiles(int max_rows);
 
 // Workspace floats the tensor-core projection needs for split-K partials.
 size_t fdl_qkv_partial_floats(int num_sms, int max_rows);
+
+// The weight-streaming GEMM for up to 64 rows (fdl_gemm_stream.cu): whether
+// it takes an [R, K] x [N, K]^T product on this context, and its projection
+// and dense forms (same contracts as fdl_launch_qkv_tc / fdl_launch_dense_tc).
+bool fdl_stream_gemm_applies(const fdl_ctx* ctx, int R, int K, int N);
+cudaError_t fdl_launch_qkv_stream(fdl_ctx* ctx, const void* X, const void* W, int R, const int* row_seq,
+                                  const int* row_rope_pos, const int* row_cache_pos, const int* block_table,
+                                  int bt_stride, void* k_cache, void* v_cache, void* q_out);
+cudaError_t fdl_launch_dense_stream(fdl_ctx* ctx, const void* X, const void* W, int R, int K, int N, void* out,
+                                    bool add_f32);
