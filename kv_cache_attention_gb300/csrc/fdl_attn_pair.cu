@@ -89,7 +89,8 @@ constexpr int OFF_FLAGS = OFF_BITMAP + 768 * 4;       // int [8]: WINDOW rows in
 constexpr int OFF_SLOTS = OFF_FLAGS + 64;             // int [kMaxSub]
 constexpr int OFF_ITEM = OFF_SLOTS + 4 * kMaxSub;     // int [16]
 constexpr int OFF_CU = OFF_ITEM + 64;                 // int [kMaxDecodeB + 1]
-constexpr int MISC_BYTES = OFF_CU + 4 * (kMaxDecodeB + 1);
+constexpr int OFF_WBITS = OFF_CU + 4 * (kMaxDecodeB + 1);  // uint32 [kTrkWords]: the sequence's WINDOW tiles, then 2 flags
+constexpr int MISC_BYTES = OFF_WBITS + 4 * (kTrkWords + 2);
 constexpr int SMEM_BYTES = 1024 + OFF_MISC + MISC_BYTES;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 static_assert(8 * (1 + 2 * kKS + 2 * kVS + 10) + 16 <= OFF_KINDS, "barriers fit");
@@ -111,6 +112,9 @@ struct PairParams {
   float* lse;
   float* track;
   int track_ld;
+  float* trk_part;        // deterministic tracker partials (null: atomics into track)
+  unsigned* trk_ticket;
+  int trk_ld;
   int H, d, R;
   float scale_log2;       // log2(e) / sqrt(head_dim)
   int bitmap_words;
@@ -146,6 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* slots = reinterpret_cast<int*>(misc + OFF_SLOTS);              // [n_sub]
   int* s_item = reinterpret_cast<int*>(misc + OFF_ITEM);
   int* s_cu = reinterpret_cast<int*>(misc + OFF_CU);
+  uint32_t* wbits = reinterpret_cast<uint32_t*>(misc + OFF_WBITS);  // [kTrkWords], [kTrkWords]: overflow, +1: last
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x;
@@ -193,6 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the shape error.
   for (int i = threadIdx.x; i <= p.B; i += kThreads) s_cu[i] = p.cu[i];
   if (threadIdx.x == 0) s_item[7] = 0;
+  if (threadIdx.x < kTrkWords + 1) wbits[threadIdx.x] = 0u;
   __syncthreads();
   if (warp == 0) {
     bool bad = s_cu[0] != 0 || s_cu[p.B] != p.R;
@@ -342,8 +348,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int w = t_local; w < p.bitmap_words; w += 256) bitmap[w] = 0u;
     if (p.track) {
+      // and the sequence's 128-row tiles that hold them (the tracker's slots)
       int cnt = 0;
-      for (int r = s_cu[b] + t_local; r < s_cu[b + 1]; r += 256) cnt += p.row_kind[r] == FDL_KIND_WINDOW ? 1 : 0;
+      for (int r = s_cu[b] + t_local; r < s_cu[b + 1]; r += 256) {
+        if (p.row_kind[r] != FDL_KIND_WINDOW) continue;
+        ++cnt;
+        const int tt = (r - s_cu[b]) / kBM;
+        if (tt < 32 * kTrkWords) atomicOr(&wbits[tt >> 5], 1u << (tt & 31));
+        else wbits[kTrkWords] = 1u;
+      }
       for (int off = 16; off; off >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
       if (lane == 0 && cnt) atomicAdd(&s_item[7], cnt);
     }
@@ -357,6 +370,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool any_window = false;
   for (int i = 0; i < 8; ++i) any_window |= win_flags[i] != 0;
   const bool two_pass = do_track && any_window;
+  // deterministic tracker: each tile's slot among the sequence's WINDOW
+  // tiles, and the pairs (CTAs per head) that hold any of them
+  const int tile0 = (q0 - s_cu[b]) / kBM;
+  int trk_n = 0, trk_pairs = 0;
+  const int trk_slot0 = trk_rank(wbits, tile0, trk_n);
+  const int trk_slot1 = trk_slot0 + (int)((wbits[tile0 >> 5] >> (tile0 & 31)) & 1u);
+  for (int w = 0; w < kTrkWords; ++w) trk_pairs += __popc((wbits[w] | (wbits[w] >> 1)) & 0x55555555u);
+  const bool trk_det = p.trk_part != nullptr && wbits[kTrkWords] == 0u && trk_n <= FDL_TRK_SLOTS;
   const int sA = two_pass ? n_tiles : 0;  // S products of pass A per group
   const int n_s = sA + n_tiles;          // S products per group = K tile loads
 
@@ -692,7 +713,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int c = c0 + t_g;
           const float v = ((colw[(g * 4 + 0) * kBN + t_g] + colw[(g * 4 + 1) * kBN + t_g]) +
                            colw[(g * 4 + 2) * kBN + t_g]) + colw[(g * 4 + 3) * kBN + t_g];
-          if (c < kvl && v != 0.f) atomicAdd(p.track + (size_t)b * p.track_ld + c, v * wscale);
+          if (c < kvl) {
+            const int tg = tile0 + g;
+            if (!trk_det) {
+              if (v != 0.f) atomicAdd(p.track + (size_t)b * p.track_ld + c, v * wscale);
+            } else if ((wbits[tg >> 5] >> (tg & 31)) & 1u) {
+              trk_row(p.trk_part, b, g ? trk_slot1 : trk_slot0, h, p.H, p.trk_ld)[c] = v * wscale;
+            }
+          }
         }
         tc::named_bar(4 + g, 128);
       }
@@ -735,10 +763,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  if (trk_det && two_pass && softmax_warp) __threadfence();  // this thread's partials, before the ticket below
   tc::fence_before_sync();
   __syncthreads();
   if (threadIdx.x == 0 && *abort_flag) fdl::raise_error(p.err, FDL_DEVERR_TIMEOUT);
   if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
+  // deterministic tracker: the sequence's last contributing CTA (of its
+  // pairs with WINDOW tiles x heads) adds the partials to the scores
+  if (trk_det && two_pass &&
+      trk_last(p.trk_ticket + b * kTrkTickets, (unsigned)(trk_pairs * p.H),
+               reinterpret_cast<int*>(wbits + kTrkWords + 1)))
+    trk_finalize(p.trk_part, p.track, p.track_ld, b, trk_n, p.H, p.trk_ld, 0, kvl, reinterpret_cast<float*>(kring),
+                 (kKS * KT_BYTES) / 4);
 }
 
 }  // namespace
@@ -781,6 +817,9 @@ cudaError_t fdl_launch_attn_pair(fdl_ctx* ctx, const void* q, const void* k_cach
   p.lse = lse_out;
   p.track = track;
   p.track_ld = track_ld;
+  p.trk_part = ctx->trk_part;
+  p.trk_ticket = ctx->trk_ticket;
+  p.trk_ld = ctx->trk_ld;
   p.H = c.n_heads;
   p.d = c.d_model;
   p.R = R;

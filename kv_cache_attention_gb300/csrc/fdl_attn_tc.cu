@@ -79,15 +79,16 @@ constexpr int OFF_MISC = OFF_ML + ML_BYTES;
 // the search bitmap (<= 768 words), the two groups' (max, sum) per row,
 // flags, key-tile slots
 constexpr int OFF_KINDS = 256;                      // int [128]
-constexpr int OFF_COLACC = OFF_KINDS + 4 * kBM;     // float [2][64]
-constexpr int OFF_BITMAP = OFF_COLACC + 2 * 64 * 4;  // uint32 [768]
+constexpr int OFF_COLACC = OFF_KINDS + 4 * kBM;     // float [2 groups][4 warps][64]
+constexpr int OFF_BITMAP = OFF_COLACC + 2 * 4 * 64 * 4;  // uint32 [768]
 constexpr int OFF_HALFML = OFF_BITMAP + 768 * 4;    // float [2][128][2]
 constexpr int OFF_FLAGS = OFF_HALFML + 2 * kBM * 2 * 4;
 constexpr int OFF_SLOTS = OFF_FLAGS + 256;          // int [kMaxTiles]
 constexpr int OFF_ITEM = OFF_SLOTS + 4 * kMaxTiles;  // int [8]: item count, b, q0, qlen, n_keys, WINDOW rows of b
 constexpr int kMaxDecodeB = 1024;                   // batch whose cu_seqlens_q the kernel stages
 constexpr int OFF_CU = OFF_ITEM + 32;               // int [kMaxDecodeB + 1]
-constexpr int MISC_BYTES = OFF_CU + 4 * (kMaxDecodeB + 1);
+constexpr int OFF_WBITS = OFF_CU + 4 * (kMaxDecodeB + 1);  // uint32 [kTrkWords]: the sequence's WINDOW tiles, then 2 flags
+constexpr int MISC_BYTES = OFF_WBITS + 4 * (kTrkWords + 2);
 static_assert(8 * (1 + 2 * kKS + 2 * kVS + 2 * kSB + 5) + 8 <= OFF_KINDS, "barriers fit");
 static_assert(256 + 64 * kSB <= kTmemCols, "TMEM columns");
 constexpr int SMEM_BYTES = 1024 + OFF_MISC + MISC_BYTES;
@@ -114,6 +115,9 @@ struct TcAttnParams {
   float* lse;
   float* track;
   int track_ld;
+  float* trk_part;          // deterministic tracker partials (null: atomics into track)
+  unsigned* trk_ticket;
+  int trk_ld;
   int H, d, R;
   int C;                    // splits per item (cluster size)
   float scale_log2;         // log2(e) / sqrt(head_dim)
@@ -229,7 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ml_ready + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* kinds = reinterpret_cast<int*>(misc + OFF_KINDS);            // [128]
-  float* colacc = reinterpret_cast<float*>(misc + OFF_COLACC);      // [2][64]
+  float* colacc = reinterpret_cast<float*>(misc + OFF_COLACC);      // [2][4][64]
+  uint32_t* wbits = reinterpret_cast<uint32_t*>(misc + OFF_WBITS);   // [kTrkWords], [kTrkWords]: overflow, +1: last
   uint32_t* bitmap = reinterpret_cast<uint32_t*>(misc + OFF_BITMAP);  // [bitmap_words] (<= 768)
   float* halfml = reinterpret_cast<float*>(misc + OFF_HALFML);      // [2][128][2]
   // per row-staging warp: its 32 rows hold a WINDOW row (written by that
@@ -289,6 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int* s_cu = reinterpret_cast<int*>(misc + OFF_CU);
     for (int i = threadIdx.x; i <= p.B; i += kThreads) s_cu[i] = p.cu[i];
     if (threadIdx.x == 0) s_item[5] = 0;
+    if (threadIdx.x < kTrkWords + 1) wbits[threadIdx.x] = 0u;
     __syncthreads();
     if (warp == 0) {
       bool bad = s_cu[0] != 0 || s_cu[p.B] != p.R;
@@ -423,12 +429,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) win_flags[r >> 5] = w ? 1 : 0;
     }
     for (int w = t_local; w < p.bitmap_words; w += 256) bitmap[w] = 0u;
-    if (t_local < 128) colacc[t_local] = 0.f;
     if (!p.wl && p.track) {
-      // WINDOW rows of the whole sequence (the tracker's |M_b|)
+      // WINDOW rows of the whole sequence (the tracker's |M_b|), and the
+      // sequence's 128-row tiles that hold them (the tracker's slots)
       const int* s_cu = reinterpret_cast<const int*>(misc + OFF_CU);
       int cnt = 0;
-      for (int r = s_cu[b] + t_local; r < s_cu[b + 1]; r += 256) cnt += p.row_kind[r] == FDL_KIND_WINDOW ? 1 : 0;
+      for (int r = s_cu[b] + t_local; r < s_cu[b + 1]; r += 256) {
+        if (p.row_kind[r] != FDL_KIND_WINDOW) continue;
+        ++cnt;
+        const int tt = (r - s_cu[b]) / kBM;
+        if (tt < 32 * kTrkWords) atomicOr(&wbits[tt >> 5], 1u << (tt & 31));
+        else wbits[kTrkWords] = 1u;
+      }
       for (int off = 16; off; off >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
       if (lane == 0 && cnt) atomicAdd(&s_item[5], cnt);
     }
@@ -445,6 +457,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool do_track = p.track != nullptr && n_masked_b > 0;
   const bool any_window = (win_flags[0] | win_flags[1] | win_flags[2] | win_flags[3]) != 0;
   const bool track_item = do_track && any_window;
+  // deterministic tracker: this tile's slot among the sequence's WINDOW
+  // tiles (decode mode with the context's partial buffer; the same decision
+  // in every CTA of the sequence)
+  int trk_n = 0, trk_slot = 0;
+  if (!p.wl && p.trk_part) trk_slot = trk_rank(wbits, (q0 - reinterpret_cast<const int*>(misc + OFF_CU)[b]) / kBM, trk_n);
+  const bool trk_det = !p.wl && p.trk_part && wbits[kTrkWords] == 0u && trk_n <= FDL_TRK_SLOTS;
   // Split items and items that feed the tracker take two exact passes; the
   // others one online pass.
   const bool two_pass = C > 1 || track_item;
@@ -798,15 +816,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           float* hi = pr + 32;
           warp_colsum32(*reinterpret_cast<float(*)[32]>(lo), lane);
           warp_colsum32(*reinterpret_cast<float(*)[32]>(hi), lane);
-          atomicAdd(&colacc[g * 64 + lane], pr[0]);
-          atomicAdd(&colacc[g * 64 + 32 + lane], pr[32]);
+          colacc[(g * 4 + qd) * 64 + lane] = pr[0];
+          colacc[(g * 4 + qd) * 64 + 32 + lane] = pr[32];
+        } else {
+          colacc[(g * 4 + qd) * 64 + lane] = 0.f;
+          colacc[(g * 4 + qd) * 64 + 32 + lane] = 0.f;
         }
+        // the group's four warps' column sums, added in a fixed order
         tc::named_bar(4 + g, 128);
         if (t_g < 64) {
           const int c = c0 + t_g;
-          const float v = colacc[g * 64 + t_g];
-          colacc[g * 64 + t_g] = 0.f;
-          if (c < kvl && v != 0.f) atomicAdd(p.track + (size_t)b * p.track_ld + c, v * wscale);
+          const float v = ((colacc[(g * 4 + 0) * 64 + t_g] + colacc[(g * 4 + 1) * 64 + t_g]) +
+                           colacc[(g * 4 + 2) * 64 + t_g]) + colacc[(g * 4 + 3) * 64 + t_g];
+          if (c < kvl) {
+            if (trk_det) {
+              trk_row(p.trk_part, b, trk_slot, h, p.H, p.trk_ld)[c] = v * wscale;
+            } else if (v != 0.f) {
+              atomicAdd(p.track + (size_t)b * p.track_ld + c, v * wscale);
+            }
+          }
         }
         tc::named_bar(4 + g, 128);
       }
@@ -909,10 +937,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::cluster_sync();  // peers finished reading this CTA's staged O
   }
 
+  if (trk_det && track_item && softmax_warp) __threadfence();  // this thread's partials, before the ticket below
   tc::fence_before_sync();
   __syncthreads();
   if (threadIdx.x == 0 && *abort_flag) fdl::raise_error(p.err, FDL_DEVERR_TIMEOUT);
   if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
+  // deterministic tracker: per KV split rank (a disjoint column range), the
+  // last contributing CTA (of the sequence's WINDOW tiles x heads) adds that
+  // range's partials to the scores
+  static_assert(kMaxC <= kTrkTickets, "a ticket per split rank");
+  if (trk_det && track_item &&
+      trk_last(p.trk_ticket + b * kTrkTickets + rank, (unsigned)(trk_n * p.H),
+               reinterpret_cast<int*>(wbits + kTrkWords + 1)))
+    trk_finalize(p.trk_part, p.track, p.track_ld, b, trk_n, p.H, p.trk_ld, t0 * kBN, min(kvl, t1 * kBN),
+                 reinterpret_cast<float*>(kring), (kKS * KT_BYTES) / 4);
 }
 
 }  // namespace
@@ -976,6 +1014,9 @@ cudaError_t fdl_launch_attn_tc(fdl_ctx* ctx, const void* q, const void* k_cache,
   p.lse = lse_out;
   p.track = track;
   p.track_ld = track_ld;
+  p.trk_part = ctx->trk_part;
+  p.trk_ticket = ctx->trk_ticket;
+  p.trk_ld = ctx->trk_ld;
   p.H = c.n_heads;
   p.d = c.d_model;
   p.R = R;

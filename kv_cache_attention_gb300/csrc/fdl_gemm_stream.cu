@@ -489,14 +489,16 @@ __global__ void __launch_bounds__(kMergeThreads) merge_qkv_kernel(const MergeQkv
 }
 
 // ------------------------------------------------------------ consumers
-// Kernels that merge the shares while consuming the product, so that a
-// dense product needs no launch of its own for the merge. CTA c's share of
+// A kernel that merges the shares while consuming the product (the SwiGLU
+// product of the gate/up projection), so that the product needs no launch
+// of its own for the merge. (Folding the W_o and down merges into the
+// residual add + RMSNorm, one CTA per row, was measured slower than the
+// separate merge with a CTA per tile and row block.) CTA c's share of
 // tile t gets index c + t in a flat table (CTA ranges are ordered like the
 // tiles, so no two (c, t) pairs collide), filled from the schedule alone
 // before the programmatic-launch wait.
 constexpr int kMaxTable = 1024;  // G + T - 1 entries at most
 constexpr int kRowThreads = 256;
-constexpr int kNormGroups = 4;   // 8-feature groups per thread in the fused RMSNorm (d <= 8192)
 
 __device__ __forceinline__ void fill_table(const Sched& s, unsigned* tab) {
   for (unsigned c = threadIdx.x; c < s.G; c += blockDim.x) {
@@ -519,72 +521,6 @@ __device__ __forceinline__ void merged8(const Sched& s, const float* partials, c
     const float4 x0 = __ldcg(src), x1 = __ldcg(src + 1);
     acc[0] += x0.x, acc[1] += x0.y, acc[2] += x0.z, acc[3] += x0.w;
     acc[4] += x1.x, acc[5] += x1.y, acc[6] += x1.z, acc[7] += x1.w;
-  }
-}
-
-// One CTA per row: h += merged product (written back), then the RMSNorm of
-// the new row with the sum of squares in a fixed order (each thread's
-// elements in order, a fixed xor tree per warp, the warps' sums in warp
-// order).
-__global__ void __launch_bounds__(kRowThreads) add_rmsnorm_shares_kernel(const Sched s, const float* partials,
-                                                                         float* __restrict__ h, int d,
-                                                                         const __nv_bfloat16* __restrict__ g,
-                                                                         float eps, __nv_bfloat16* __restrict__ out) {
-  __shared__ unsigned tab[kMaxTable];
-  __shared__ float warp_sum[kRowThreads / 32];
-  __shared__ float scale;
-  fill_table(s, tab);
-  __syncthreads();
-  fdl::grid_dep_wait();
-  fdl::grid_dep_launch();
-  const int r = blockIdx.x;
-  float* hr = h + (size_t)r * d;
-  float v[kNormGroups][8];
-  float ss = 0.f;
-#pragma unroll
-  for (int k = 0; k < kNormGroups; ++k) {
-    const int f = (k * kRowThreads + (int)threadIdx.x) * 8;
-    if (f < d) {
-      float acc[8];
-      merged8(s, partials, tab, r, f, acc);
-      float4* hp = reinterpret_cast<float4*>(hr + f);
-      float4 h0 = hp[0], h1 = hp[1];
-      h0.x += acc[0], h0.y += acc[1], h0.z += acc[2], h0.w += acc[3];
-      h1.x += acc[4], h1.y += acc[5], h1.z += acc[6], h1.w += acc[7];
-      hp[0] = h0;
-      hp[1] = h1;
-      v[k][0] = h0.x, v[k][1] = h0.y, v[k][2] = h0.z, v[k][3] = h0.w;
-      v[k][4] = h1.x, v[k][5] = h1.y, v[k][6] = h1.z, v[k][7] = h1.w;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) ss = fmaf(v[k][i], v[k][i], ss);
-    }
-  }
-  for (int off = 16; off; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-  if ((threadIdx.x & 31) == 0) warp_sum[threadIdx.x >> 5] = ss;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float t = 0.f;
-    for (int w = 0; w < kRowThreads / 32; ++w) t += warp_sum[w];
-    scale = rsqrtf(t / (float)d + eps);
-  }
-  __syncthreads();
-  const float sc = scale;
-#pragma unroll
-  for (int k = 0; k < kNormGroups; ++k) {
-    const int f = (k * kRowThreads + (int)threadIdx.x) * 8;
-    if (f < d) {
-      uint2 gw[2];  // (g is 8-byte aligned, like the plain RMSNorm's)
-      gw[0] = *reinterpret_cast<const uint2*>(g + f);
-      gw[1] = *reinterpret_cast<const uint2*>(g + f + 4);
-      const __nv_bfloat162* ga = reinterpret_cast<const __nv_bfloat162*>(gw);
-      float y[8];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        y[2 * i] = v[k][2 * i] * sc * __low2float(ga[i]);
-        y[2 * i + 1] = v[k][2 * i + 1] * sc * __high2float(ga[i]);
-      }
-      *reinterpret_cast<int4*>(out + (size_t)r * d + f) = pack_bf16x8(y);
-    }
   }
 }
 
@@ -731,15 +667,10 @@ cudaError_t fdl_launch_qkv_stream(fdl_ctx* ctx, const void* X, const void* W, in
                         dim3(kMergeThreads, 1, 1), 0, ctx->stream, 1, m);
 }
 
-bool fdl_stream_consumers_apply(const fdl_ctx* ctx, int R, int d, int F) {
-  if (d % 8 != 0 || d > kNormGroups * kRowThreads * 8 || F % 8 != 0) return false;
-  const int shapes[3][2] = {{d, d}, {d, 2 * F}, {F, d}};  // (K, N) of W_o, gate/up, down
-  for (const auto& kn : shapes) {
-    Sched s;
-    if (!fdl_stream_gemm_applies(ctx, R, kn[0], kn[1]) || !make_sched(ctx, kn[0], kn[1], s)) return false;
-    if (s.G + s.T - 1 > (unsigned)kMaxTable) return false;
-  }
-  return true;
+bool fdl_stream_swiglu_applies(const fdl_ctx* ctx, int R, int d, int F) {
+  Sched s;
+  return F % 8 == 0 && fdl_stream_gemm_applies(ctx, R, d, 2 * F) && make_sched(ctx, d, 2 * F, s) &&
+         s.G + s.T - 1 <= (unsigned)kMaxTable;
 }
 
 cudaError_t fdl_launch_dense_stream_shares(fdl_ctx* ctx, const void* X, const void* W, int R, int K, int N,
@@ -754,18 +685,6 @@ cudaError_t fdl_launch_dense_stream_shares(fdl_ctx* ctx, const void* X, const vo
   out->U = s.U;
   out->partials = ctx->qkv_partials;
   return launch_stream(ctx, s, R, X, W, K, N);
-}
-
-cudaError_t fdl_launch_add_rmsnorm_shares(fdl_ctx* ctx, const fdl_stream_shares& sh, float* h, int R, const void* g,
-                                          float eps, void* out) {
-  const int d = ctx->cfg.d_model;
-  if (R <= 0) return cudaSuccess;
-  if (sh.T * kBM != (unsigned)d || d > kNormGroups * kRowThreads * 8 ||
-      ((reinterpret_cast<uintptr_t>(h) | reinterpret_cast<uintptr_t>(out)) & 15) || (reinterpret_cast<uintptr_t>(g) & 7))
-    return cudaErrorMisalignedAddress;
-  const Sched s{sh.nkb, sh.T, sh.G, sh.U};
-  return fdl_launch_pdl(add_rmsnorm_shares_kernel, dim3(R), dim3(kRowThreads), 0, ctx->stream, 1, s, sh.partials, h,
-                        d, reinterpret_cast<const __nv_bfloat16*>(g), eps, reinterpret_cast<__nv_bfloat16*>(out));
 }
 
 cudaError_t fdl_launch_swiglu_shares(fdl_ctx* ctx, const fdl_stream_shares& sh, int R, int F, void* u) {

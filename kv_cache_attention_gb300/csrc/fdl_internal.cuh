@@ -18,6 +18,11 @@
 #define FDL_TILE_M_SIMT 16
 #define FDL_TILE_M_TC 128
 
+// Eq. (2) tracker partial slots per sequence (the tensor-core attention's
+// 128-row query tiles that hold WINDOW rows; a sequence whose WINDOW rows
+// span more tiles adds its column sums with atomics instead).
+#define FDL_TRK_SLOTS 2
+
 struct fdl_ctx {
   fdl_config cfg;
   cudaStream_t stream;
@@ -40,6 +45,9 @@ struct fdl_ctx {
   size_t lm_part_floats;
   unsigned* lm_rt_tickets;  // per-row-tile arrival counters of the many-row LM head (zero between calls)
   int lm_rt_ticket_count;
+  float* trk_part;       // tracker column sums [max_batch][FDL_TRK_SLOTS][n_heads][trk_ld] (tensor-core attention)
+  unsigned* trk_ticket;  // [max_batch][8] arrivals of the tracker's contributing CTAs per KV split rank (zero between calls)
+  int trk_ld;
   long long wait_budget;  // projection main-loop wait budget in cycles (0 = the default ~2 s)
   char last_error[512];
 };

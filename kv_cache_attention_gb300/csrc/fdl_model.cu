@@ -209,19 +209,14 @@ extern "C" fdl_status fdl_model_forward(fdl_ctx* ctx, const fdl_model* m, const 
   if (R == 0) return FDL_OK;
 
   const int d = c.d_model, F = m->ffn;
-  // Up to 64 rows the dense products take the weight-streaming GEMM and
-  // their fp32 shares are merged by the kernel that consumes them: W_o's by
-  // the residual add + RMSNorm, gate/up's by the SwiGLU product, down's by
-  // the next layer's (or the final) residual add + RMSNorm.
-  const bool fused = fdl_stream_consumers_apply(ctx, R, d, F);
-  fdl_stream_shares sh{}, pending{};
-  bool have_pending = false;
+  // Up to 64 rows the gate/up product's fp32 shares (weight-streaming GEMM)
+  // are merged by the SwiGLU kernel that consumes them.
+  const bool fused_swiglu = fdl_stream_swiglu_applies(ctx, R, d, F);
+  fdl_stream_shares sh{};
   fdl_status st = FDL_OK;
   cudaError_t e = fdl_launch_embed(ctx, tokens, R, m->embed, w.h);
   for (int l = 0; e == cudaSuccess && st == FDL_OK && l < m->n_layers; ++l) {
-    e = have_pending ? fdl_launch_add_rmsnorm_shares(ctx, pending, w.h, R, m->g_attn[l], m->rms_eps, w.xn)
-                     : fdl_launch_rmsnorm(ctx, w.h, R, m->g_attn[l], m->rms_eps, w.xn);
-    have_pending = false;
+    e = fdl_launch_rmsnorm(ctx, w.h, R, m->g_attn[l], m->rms_eps, w.xn);
     if (e != cudaSuccess) break;
     st = fdl_qkv_rope_cache_write(ctx, w.xn, m->w_qkv[l], R, row_seq, row_rope_pos, row_cache_pos, block_table,
                                   bt_stride, k_caches[l], v_caches[l], w.q);
@@ -229,25 +224,19 @@ extern "C" fdl_status fdl_model_forward(fdl_ctx* ctx, const fdl_model* m, const 
     st = fdl_sched_attn(ctx, w.q, k_caches[l], v_caches[l], block_table, bt_stride, cu_seqlens_q, kv_len, B, R,
                         row_kind, search_pos, search_ld, n_search, w.o, nullptr, track_scores, track_ld, nullptr);
     if (st != FDL_OK) break;
-    if (fused) {
-      e = fdl_launch_dense_stream_shares(ctx, w.o, m->w_o[l], R, d, d, &sh);
-      if (e == cudaSuccess) e = fdl_launch_add_rmsnorm_shares(ctx, sh, w.h, R, m->g_mlp[l], m->rms_eps, w.xn);
+    e = fdl_launch_dense_tc(ctx, w.o, m->w_o[l], R, d, d, w.h, true);
+    if (e == cudaSuccess) e = fdl_launch_rmsnorm(ctx, w.h, R, m->g_mlp[l], m->rms_eps, w.xn);
+    if (fused_swiglu) {
       if (e == cudaSuccess) e = fdl_launch_dense_stream_shares(ctx, w.xn, m->w_gu[l], R, d, 2 * F, &sh);
       if (e == cudaSuccess) e = fdl_launch_swiglu_shares(ctx, sh, R, F, w.u);
-      if (e == cudaSuccess) e = fdl_launch_dense_stream_shares(ctx, w.u, m->w_down[l], R, F, d, &pending);
-      have_pending = e == cudaSuccess;
     } else {
-      e = fdl_launch_dense_tc(ctx, w.o, m->w_o[l], R, d, d, w.h, true);
-      if (e == cudaSuccess) e = fdl_launch_rmsnorm(ctx, w.h, R, m->g_mlp[l], m->rms_eps, w.xn);
       if (e == cudaSuccess) e = fdl_launch_dense_tc(ctx, w.xn, m->w_gu[l], R, d, 2 * F, w.gu, false);
       if (e == cudaSuccess) e = fdl_launch_swiglu(ctx, w.gu, R, F, w.u);
-      if (e == cudaSuccess) e = fdl_launch_dense_tc(ctx, w.u, m->w_down[l], R, F, d, w.h, true);
     }
+    if (e == cudaSuccess) e = fdl_launch_dense_tc(ctx, w.u, m->w_down[l], R, F, d, w.h, true);
   }
   if (st != FDL_OK) return st;
-  if (e == cudaSuccess)
-    e = have_pending ? fdl_launch_add_rmsnorm_shares(ctx, pending, w.h, R, m->g_final, m->rms_eps, final_out)
-                     : fdl_launch_rmsnorm(ctx, w.h, R, m->g_final, m->rms_eps, final_out);
+  if (e == cudaSuccess) e = fdl_launch_rmsnorm(ctx, w.h, R, m->g_final, m->rms_eps, final_out);
   if (e != cudaSuccess)
     return model_fail(ctx, FDL_ERR_CUDA, "fdl_model_forward launch: %s", cudaGetErrorString(e));
   ctx->last_error[0] = 0;

@@ -31,18 +31,14 @@ struct fdl_stream_shares {
   const float* partials;
 };
 
-// Whether the model forward's W_o, gate/up and down products over R rows
-// take the weight-streaming GEMM with the merges below (d = d_model, F = ffn).
-bool fdl_stream_consumers_apply(const fdl_ctx* ctx, int R, int d, int F);
+// Whether the model forward's gate/up product over R rows takes the
+// weight-streaming GEMM with its merge in the SwiGLU kernel below (d =
+// d_model, F = ffn).
+bool fdl_stream_swiglu_applies(const fdl_ctx* ctx, int R, int d, int F);
 
 // The GEMM alone: X [R, K] x W [N, K]^T into the context's share workspace.
 cudaError_t fdl_launch_dense_stream_shares(fdl_ctx* ctx, const void* X, const void* W, int R, int K, int N,
                                            fdl_stream_shares* out);
-
-// h[r, :] += the merged product (fixed order), then
-// out[r, :] = bf16(h[r, :] / sqrt(mean(h[r, :]^2) + eps) * g) as fdl_launch_rmsnorm.
-cudaError_t fdl_launch_add_rmsnorm_shares(fdl_ctx* ctx, const fdl_stream_shares& sh, float* h, int R, const void* g,
-                                          float eps, void* out);
 
 // u[r, i] = bf16(silu(gate) * up) with gate = bf16(merged product[r, i]) and
 // up = bf16(merged product[r, F + i]), as fdl_launch_swiglu over a bf16 store.
