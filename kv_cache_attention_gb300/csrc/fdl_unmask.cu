@@ -315,19 +315,14 @@ __device__ void decide_unmask(const RowParams& p, const int* st_seq, const int* 
         // an uncommitted row's key for the comparison; committed and absent
         // rows take -1 (below every confidence) so they never outrank
         const float kb = (vb && !(cb >= eps) && rb != forced) ? cb : -1.f;
-        // eight (key, position) pairs per round: their shuffles issue back to
-        // back, and the rolled loop keeps this one-off code small
-#pragma unroll 1
-        for (int k0 = 0; k0 < 32; k0 += 8) {
-          float co[8];
-          int po[8];
+        // every lane's (key, position) in turn, fully unrolled (shuffles from
+        // constant lanes; a rolled loop over dynamic source lanes measured
+        // three times slower on this one-warp path)
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            co[k] = __shfl_sync(0xffffffffu, kb, k0 + k);
-            po[k] = __shfl_sync(0xffffffffu, pb, k0 + k);
-          }
-#pragma unroll
-          for (int k = 0; k < 8; ++k) rank += (co[k] > ca || (co[k] == ca && po[k] < pa)) ? 1 : 0;
+        for (int k = 0; k < 32; ++k) {
+          const float co = __shfl_sync(0xffffffffu, kb, k);
+          const int po = __shfl_sync(0xffffffffu, pb, k);
+          rank += (co > ca || (co == ca && po < pa)) ? 1 : 0;
         }
       }
       n_unc += ua ? 1 : 0;
