@@ -113,7 +113,7 @@ struct PairParams {
   float* track;
   int track_ld;
   float* trk_part;        // deterministic tracker partials (null: atomics into track)
-  unsigned* trk_ticket;
+  int* trk_nslots;        // [B] slots of each sequence's partials (0: none, atomics)
   int trk_ld;
   int H, d, R;
   float scale_log2;       // log2(e) / sqrt(head_dim)
@@ -370,14 +370,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool any_window = false;
   for (int i = 0; i < 8; ++i) any_window |= win_flags[i] != 0;
   const bool two_pass = do_track && any_window;
-  // deterministic tracker: each tile's slot among the sequence's WINDOW
-  // tiles, and the pairs (CTAs per head) that hold any of them
+  // deterministic tracker: each tile's slot among the sequence's WINDOW tiles
   const int tile0 = (q0 - s_cu[b]) / kBM;
-  int trk_n = 0, trk_pairs = 0;
+  int trk_n = 0;
   const int trk_slot0 = trk_rank(wbits, tile0, trk_n);
   const int trk_slot1 = trk_slot0 + (int)((wbits[tile0 >> 5] >> (tile0 & 31)) & 1u);
-  for (int w = 0; w < kTrkWords; ++w) trk_pairs += __popc((wbits[w] | (wbits[w] >> 1)) & 0x55555555u);
   const bool trk_det = p.trk_part != nullptr && wbits[kTrkWords] == 0u && trk_n <= FDL_TRK_SLOTS;
+  if (p.trk_part && threadIdx.x == 0 && h == 0 && tile0 == 0) p.trk_nslots[b] = trk_det && do_track ? trk_n : 0;
   const int sA = two_pass ? n_tiles : 0;  // S products of pass A per group
   const int n_s = sA + n_tiles;          // S products per group = K tile loads
 
@@ -763,18 +762,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  if (trk_det && two_pass && softmax_warp) __threadfence();  // this thread's partials, before the ticket below
   tc::fence_before_sync();
   __syncthreads();
   if (threadIdx.x == 0 && *abort_flag) fdl::raise_error(p.err, FDL_DEVERR_TIMEOUT);
   if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
-  // deterministic tracker: the sequence's last contributing CTA (of its
-  // pairs with WINDOW tiles x heads) adds the partials to the scores
-  if (trk_det && two_pass &&
-      trk_last(p.trk_ticket + b * kTrkTickets, (unsigned)(trk_pairs * p.H),
-               reinterpret_cast<int*>(wbits + kTrkWords + 1)))
-    trk_finalize(p.trk_part, p.track, p.track_ld, b, trk_n, p.H, p.trk_ld, 0, kvl, reinterpret_cast<float*>(kring),
-                 (kKS * KT_BYTES) / 4);
 }
 
 }  // namespace
@@ -817,8 +808,8 @@ cudaError_t fdl_launch_attn_pair(fdl_ctx* ctx, const void* q, const void* k_cach
   p.lse = lse_out;
   p.track = track;
   p.track_ld = track_ld;
-  p.trk_part = ctx->trk_part;
-  p.trk_ticket = ctx->trk_ticket;
+  p.trk_part = track ? ctx->trk_part : nullptr;
+  p.trk_nslots = ctx->trk_nslots;
   p.trk_ld = ctx->trk_ld;
   p.H = c.n_heads;
   p.d = c.d_model;

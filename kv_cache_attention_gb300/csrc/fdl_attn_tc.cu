@@ -116,7 +116,7 @@ struct TcAttnParams {
   float* track;
   int track_ld;
   float* trk_part;          // deterministic tracker partials (null: atomics into track)
-  unsigned* trk_ticket;
+  int* trk_nslots;          // [B] slots of each sequence's partials (0: none, atomics)
   int trk_ld;
   int H, d, R;
   int C;                    // splits per item (cluster size)
@@ -460,9 +460,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // deterministic tracker: this tile's slot among the sequence's WINDOW
   // tiles (decode mode with the context's partial buffer; the same decision
   // in every CTA of the sequence)
-  int trk_n = 0, trk_slot = 0;
-  if (!p.wl && p.trk_part) trk_slot = trk_rank(wbits, (q0 - reinterpret_cast<const int*>(misc + OFF_CU)[b]) / kBM, trk_n);
-  const bool trk_det = !p.wl && p.trk_part && wbits[kTrkWords] == 0u && trk_n <= FDL_TRK_SLOTS;
+  // (found once, by one softmax thread, from the shared bitmap, and kept in
+  // shared memory, s_item[6], so that it holds no register across the main
+  // loops): the slot, or -1 for atomic adds
+  auto trk_slot = [&]() -> int {
+    if (p.wl || !p.trk_part || wbits[kTrkWords] != 0u) return -1;
+    int n = 0;
+    const int slot = trk_rank(wbits, (q0 - reinterpret_cast<const int*>(misc + OFF_CU)[b]) / kBM, n);
+    return n <= FDL_TRK_SLOTS ? slot : -1;
+  };
   // Split items and items that feed the tracker take two exact passes; the
   // others one online pass.
   const bool two_pass = C > 1 || track_item;
@@ -585,6 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int s = p.search_pos[(size_t)b * p.search_ld + j];
       if (s >= 0 && s < kvl && (s >> 5) < p.bitmap_words) atomicOr(&bitmap[s >> 5], 1u << (s & 31));
     }
+    if (t_local == 0) s_item[6] = trk_slot();  // the tracker's slot, ordered by the barrier below
     tc::named_bar(3, 256);
     const int kind = kinds[row];
 
@@ -829,8 +836,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float v = ((colacc[(g * 4 + 0) * 64 + t_g] + colacc[(g * 4 + 1) * 64 + t_g]) +
                            colacc[(g * 4 + 2) * 64 + t_g]) + colacc[(g * 4 + 3) * 64 + t_g];
           if (c < kvl) {
-            if (trk_det) {
-              trk_row(p.trk_part, b, trk_slot, h, p.H, p.trk_ld)[c] = v * wscale;
+            const int slot = s_item[6];
+            if (slot >= 0) {
+              trk_row(p.trk_part, b, slot, h, p.H, p.trk_ld)[c] = v * wscale;
             } else if (v != 0.f) {
               atomicAdd(p.track + (size_t)b * p.track_ld + c, v * wscale);
             }
@@ -937,20 +945,54 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::cluster_sync();  // peers finished reading this CTA's staged O
   }
 
-  if (trk_det && track_item && softmax_warp) __threadfence();  // this thread's partials, before the ticket below
   tc::fence_before_sync();
   __syncthreads();
   if (threadIdx.x == 0 && *abort_flag) fdl::raise_error(p.err, FDL_DEVERR_TIMEOUT);
   if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
-  // deterministic tracker: per KV split rank (a disjoint column range), the
-  // last contributing CTA (of the sequence's WINDOW tiles x heads) adds that
-  // range's partials to the scores
-  static_assert(kMaxC <= kTrkTickets, "a ticket per split rank");
-  if (trk_det && track_item &&
-      trk_last(p.trk_ticket + b * kTrkTickets + rank, (unsigned)(trk_n * p.H),
-               reinterpret_cast<int*>(wbits + kTrkWords + 1)))
-    trk_finalize(p.trk_part, p.track, p.track_ld, b, trk_n, p.H, p.trk_ld, t0 * kBN, min(kvl, t1 * kBN),
-                 reinterpret_cast<float*>(kring), (kKS * KT_BYTES) / 4);
+  // the sequence's first CTA records its partial slots for the sums below
+  // (recomputed from the shared bitmap, which is still intact)
+  // (everything re-read from shared memory and the grid indices, so that no
+  // register stays live across the main loops for it)
+  if (!p.wl && p.trk_part && threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.x == 0) {
+    const int sb = s_item[1];
+    if (s_item[2] == reinterpret_cast<const int*>(misc + OFF_CU)[sb]) {
+      int n = 0;
+      trk_rank(wbits, 0, n);
+      p.trk_nslots[sb] = p.track && s_item[5] > 0 && wbits[kTrkWords] == 0u && n <= FDL_TRK_SLOTS ? n : 0;
+    }
+  }
+}
+
+// The tracker's fixed-order sums: grid (sequence, 64-column chunk), 256
+// threads = 4 groups of a quarter of the heads x 64 columns. Each thread adds
+// its group's heads for every slot (slots outer, heads in order), then each
+// column adds the four group sums in group order into the scores.
+constexpr int kFinThreads = 256;
+__global__ void __launch_bounds__(kFinThreads)
+    trk_finalize_kernel(const float* part, const int* nslots, const int* cu, const int* kv_len, int max_seq, int H,
+                        int ld, float* track, int track_ld) {
+  __shared__ float gsum[4][64];
+  fdl::grid_dep_wait();
+  fdl::grid_dep_launch();
+  const int b = blockIdx.x, c = blockIdx.y * 64 + (threadIdx.x & 63), grp = threadIdx.x >> 6;
+  if (cu[b + 1] - cu[b] <= 0) return;  // no rows: no CTA recorded this sequence
+  const int n = nslots[b];
+  const int kvl = max(0, min(kv_len[b], max_seq));
+  if (n <= 0 || blockIdx.y * 64 >= kvl) return;
+  const int hpg = (H + 3) / 4, h0 = grp * hpg, h1 = min(H, h0 + hpg);
+  float acc = 0.f;
+  if (c < kvl) {
+    for (int sl = 0; sl < n; ++sl) {
+      const float* src = part + ((size_t)(b * FDL_TRK_SLOTS + sl) * H) * ld + c;
+#pragma unroll 8
+      for (int hh = h0; hh < h1; ++hh) acc += __ldcg(src + (size_t)hh * ld);
+    }
+  }
+  gsum[grp][threadIdx.x & 63] = acc;
+  __syncthreads();
+  if (threadIdx.x < 64 && c < kvl)
+    track[(size_t)b * track_ld + c] += ((gsum[0][threadIdx.x] + gsum[1][threadIdx.x]) + gsum[2][threadIdx.x]) +
+                                       gsum[3][threadIdx.x];
 }
 
 }  // namespace
@@ -1014,8 +1056,8 @@ cudaError_t fdl_launch_attn_tc(fdl_ctx* ctx, const void* q, const void* k_cache,
   p.lse = lse_out;
   p.track = track;
   p.track_ld = track_ld;
-  p.trk_part = ctx->trk_part;
-  p.trk_ticket = ctx->trk_ticket;
+  p.trk_part = track ? ctx->trk_part : nullptr;
+  p.trk_nslots = ctx->trk_nslots;
   p.trk_ld = ctx->trk_ld;
   p.H = c.n_heads;
   p.d = c.d_model;
@@ -1029,16 +1071,25 @@ cudaError_t fdl_launch_attn_tc(fdl_ctx* ctx, const void* q, const void* k_cache,
   while (C < kMaxC && est_items * c.n_heads * (2 * C) <= ctx->num_sms) C *= 2;
   p.C = C;
   // sequences of two or more query tiles without a KV split: two tiles per CTA
+  // the tracker's fixed-order sums follow the attention launch (decode mode
+  // with the context's partial buffer)
+  auto finalize = [&](cudaError_t e) -> cudaError_t {
+    if (e != cudaSuccess || !p.trk_part || !decode || B <= 0) return e;
+    return fdl_launch_pdl(trk_finalize_kernel, dim3((unsigned)B, (unsigned)((c.max_seq + 63) / 64)),
+                          dim3(kFinThreads, 1, 1), 0, ctx->stream, 1, (const float*)ctx->trk_part,
+                          (const int*)ctx->trk_nslots, cu_seqlens_q, kv_len, c.max_seq, c.n_heads, ctx->trk_ld, track,
+                          track_ld);
+  };
   if (decode && fdl_attn_pair_applies(R, B, C))
-    return fdl_launch_attn_pair(ctx, q, k_cache, v_cache, block_table, bt_stride, cu_seqlens_q, kv_len, B, R,
-                                row_kind, search_pos, search_ld, n_search, max_search_tokens, o_out, lse_out, track,
-                                track_ld, worklist_out);
+    return finalize(fdl_launch_attn_pair(ctx, q, k_cache, v_cache, block_table, bt_stride, cu_seqlens_q, kv_len, B,
+                                         R, row_kind, search_pos, search_ld, n_search, max_search_tokens, o_out,
+                                         lse_out, track, track_ld, worklist_out));
   // grid (split, head, item): items vary slowest, so the CTAs of real items
   // are scheduled before any idle tail. Sequence b contributes
   // ceil(rows_b / 128) items, and summed over the sequences with rows that
   // is at most ceil(R / 128) + B - 1, so no more CTAs are launched.
   const int items = min(cap, est_items);
   if (items > 65535) return cudaErrorInvalidConfiguration;
-  return fdl_launch_pdl(attn_tc_kernel, dim3((unsigned)C, (unsigned)c.n_heads, (unsigned)items), dim3(kThreads, 1, 1),
-                        SMEM_BYTES, ctx->stream, C, mq, mk, mv, p);
+  return finalize(fdl_launch_pdl(attn_tc_kernel, dim3((unsigned)C, (unsigned)c.n_heads, (unsigned)items),
+                                 dim3(kThreads, 1, 1), SMEM_BYTES, ctx->stream, C, mq, mk, mv, p));
 }

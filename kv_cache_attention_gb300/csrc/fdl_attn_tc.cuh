@@ -118,13 +118,14 @@ __device__ __forceinline__ void warp_colsum32(float (&v)[32], int lane) {
 // Deterministic Eq. (2) tracker. A CTA whose query tile holds WINDOW rows
 // stores its per-head column sums (already in a fixed order over its warps)
 // into the context's partial buffer, at the slot of its tile among the
-// sequence's tiles with WINDOW rows; every such CTA then takes the
-// sequence's ticket, and the last to arrive adds, column by column, the
-// slots' and heads' partials in (slot, head) order to the scores. Each
-// (sequence, slot, head, column) has exactly one writer per call and every
-// sum has a fixed order, so the scores do not depend on timing.
+// sequence's tiles with WINDOW rows, and the first CTA of every sequence
+// records how many slots the sequence has (0 when its WINDOW rows span more
+// tiles than there are slots: those CTAs add with atomics instead). A
+// separate kernel then adds, column by column, the slots' and heads'
+// partials in a fixed order to the scores. Each (sequence, slot, head,
+// column) has exactly one writer per call and every sum has a fixed order,
+// so the scores do not depend on timing.
 constexpr int kTrkWords = 16;  // bitmap of a sequence's 128-row tiles with WINDOW rows (<= 512 tiles)
-constexpr int kTrkTickets = 8; // tickets per sequence: one per KV split rank
 
 // Rank of tile t among the set tiles of `bits`, and their count.
 __device__ __forceinline__ int trk_rank(const uint32_t* bits, int t, int& n) {
@@ -143,74 +144,6 @@ __device__ __forceinline__ int trk_rank(const uint32_t* bits, int t, int& n) {
 // Row of partial sums of (sequence b, slot s, head h).
 __device__ __forceinline__ float* trk_row(float* part, int b, int s, int h, int H, int ld) {
   return part + ((size_t)(b * FDL_TRK_SLOTS + s) * H + h) * ld;
-}
-
-// Thread 0 of a CTA that has stored its partials (and fenced them): true,
-// for every thread, in the CTA that arrives last of `expected`. Call from all
-// threads.
-__device__ __forceinline__ bool trk_last(unsigned* ticket, unsigned expected, int* flag_smem) {
-  if (threadIdx.x == 0) {
-    unsigned t;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(t) : "l"(ticket) : "memory");
-    *flag_smem = t == expected - 1u;
-    if (t == expected - 1u) *ticket = 0u;  // every contributor has arrived: ready for the next call
-  }
-  __syncthreads();
-  return *flag_smem != 0;
-}
-
-// The last CTA of sequence b (and of KV split range [c_lo, c_hi) when the
-// item is split): track[b][c] += the partials of slots s < n_slots and heads
-// h < H, for c_lo <= c < c_hi. Every thread of the CTA takes part (call from
-// all of them): a thread sums four columns over one group of heads (slots
-// outer, the group's heads inner) into `buf` (the drained rings), then each
-// column adds its groups in group order, so the order is fixed. (ld and c_lo
-// are multiples of 4; buf holds buf_floats floats.)
-constexpr int kTrkGroups = 8;  // head groups summed in parallel
-__device__ __forceinline__ void trk_finalize(const float* part, float* track, int track_ld, int b, int n_slots,
-                                             int H, int ld, int c_lo, int c_hi, float* buf, int buf_floats) {
-  const int ng = H < kTrkGroups ? H : kTrkGroups;
-  const int hpg = (H + ng - 1) / ng;                 // heads per group
-  const int chunk = buf_floats / (4 * ng) * 4;       // columns staged per round (a multiple of 4)
-  for (int cb = c_lo; cb < c_hi; cb += chunk) {
-    const int ce = min(c_hi, cb + chunk);
-    const int nq = (ce - cb + 3) / 4;
-    for (int w = threadIdx.x; w < nq * ng; w += blockDim.x) {
-      const int qi = w % nq, gi = w / nq;
-      const int c0 = cb + 4 * qi;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int s = 0; s < n_slots; ++s) {
-        const float* src = part + ((size_t)(b * FDL_TRK_SLOTS + s) * H) * ld + c0;
-        float4 x[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int h = gi * hpg + u;
-          x[u] = u < hpg && h < H ? __ldcg(reinterpret_cast<const float4*>(src + (size_t)h * ld))
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        for (int u0 = 8; u0 < hpg; u0 += 8) {  // more than 8 heads per group
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int h = gi * hpg + u0 + u;
-            const float4 y = u0 + u < hpg && h < H ? __ldcg(reinterpret_cast<const float4*>(src + (size_t)h * ld))
-                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-            x[u].x += y.x, x[u].y += y.y, x[u].z += y.z, x[u].w += y.w;
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) v.x += x[u].x, v.y += x[u].y, v.z += x[u].z, v.w += x[u].w;
-      }
-      reinterpret_cast<float4*>(buf)[gi * nq + qi] = v;
-    }
-    __syncthreads();
-    for (int c = cb + threadIdx.x; c < ce; c += blockDim.x) {
-      const int k = c - cb;
-      float v = 0.f;
-      for (int gi = 0; gi < ng; ++gi) v += buf[gi * 4 * nq + k];
-      track[(size_t)b * track_ld + c] += v;
-    }
-    __syncthreads();
-  }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {

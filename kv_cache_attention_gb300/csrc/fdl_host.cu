@@ -123,9 +123,7 @@ fdl_status fdl_create(const fdl_config* cfg, void* cuda_stream, fdl_ctx** out) {
     ctx->trk_ld = (cfg->max_seq + 3) / 4 * 4;
     const size_t trk = (size_t)cfg->max_batch * FDL_TRK_SLOTS * cfg->n_heads * ctx->trk_ld;
     e = e ? e : cudaMalloc(&ctx->trk_part, trk * sizeof(float));
-    // a ticket per sequence and KV split rank (up to 8)
-    e = e ? e : cudaMalloc(&ctx->trk_ticket, 8 * (size_t)cfg->max_batch * sizeof(unsigned));
-    e = e ? e : cudaMemset(ctx->trk_ticket, 0, 8 * (size_t)cfg->max_batch * sizeof(unsigned));
+    e = e ? e : cudaMalloc(&ctx->trk_nslots, (size_t)cfg->max_batch * sizeof(int));
   }
   e = e ? e : cudaMemcpy(ctx->rope_cos, hc.data(), n_tab * sizeof(float), cudaMemcpyHostToDevice);
   e = e ? e : cudaMemcpy(ctx->rope_sin, hs.data(), n_tab * sizeof(float), cudaMemcpyHostToDevice);
@@ -152,7 +150,7 @@ void fdl_destroy(fdl_ctx* ctx) {
   cudaFree(ctx->lm_part);
   cudaFree(ctx->lm_rt_tickets);
   cudaFree(ctx->trk_part);
-  cudaFree(ctx->trk_ticket);
+  cudaFree(ctx->trk_nslots);
   free(ctx);
 }
 

@@ -46,7 +46,7 @@ struct fdl_ctx {
   unsigned* lm_rt_tickets;  // per-row-tile arrival counters of the many-row LM head (zero between calls)
   int lm_rt_ticket_count;
   float* trk_part;       // tracker column sums [max_batch][FDL_TRK_SLOTS][n_heads][trk_ld] (tensor-core attention)
-  unsigned* trk_ticket;  // [max_batch][8] arrivals of the tracker's contributing CTAs per KV split rank (zero between calls)
+  int* trk_nslots;       // [max_batch] partial slots of each sequence in the last tracked attention call
   int trk_ld;
   long long wait_budget;  // projection main-loop wait budget in cycles (0 = the default ~2 s)
   char last_error[512];
