@@ -440,7 +440,7 @@ def run_gpu(args, world, rank, local):
     res = {name: res_buf[res_off[name]:res_off[name] + int(np.prod(shp)) * torch.empty((), dtype=dt).element_size()]
            .view(dt).view(shp) for name, dt, shp in res_layout}
     conf, arg, com, srows, nsr, idx, cnt = (res[n] for n in ("conf", "arg", "com", "srows", "nsr", "idx", "cnt"))
-    launches_per_step = 5  # projection (weight stream + merge), attention (finds its own work items), top-k, unmask
+    launches_per_step = 6  # projection (weight stream + merge), attention + tracker sums, top-k, unmask
 
     def qkv_part(c, X=None):
         X = Xs[c] if X is None else X
