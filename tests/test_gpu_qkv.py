@@ -1,6 +1,7 @@
 """Fused QKV + RoPE + cache scatter (tensor-core path for bf16 contexts)
 against the float64 oracle, over shapes that exercise every tile width
-(64/128/256 query rows), split-K clusters, ragged row tails, paged caches,
+(up to 64 query rows: the weight stream and its merge; 64/128/256-row tiles
+of the split-K kernels above), ragged row tails, paged caches,
 rows without a cache write, and head_dim 64 and 128."""
 import numpy as np
 import pytest
@@ -18,6 +19,7 @@ CASES = [
     (1024, 8, 64),
     (1024, 8, 100),
     (1024, 8, 300),
+    (1024, 16, 37),   # head_dim 64 through the weight stream (up to 64 rows)
     (1024, 16, 777),
     (4096, 32, 64),
     (4096, 32, 520),
