@@ -44,13 +44,14 @@ METRIC = "layer-step query-tokens/s at LLaDA-8B shapes; % of bf16 TC peak / HBM 
 WORKLOAD = "llada8b_layer_bf16_b1_p512_g256_w32_t32"
 
 
-# DRAM traffic of one launch of the projection kernel on this workload
-# (dram__bytes_read.sum + dram__bytes_write.sum), from the ncu capture
-# summarised in profiles/qkv_tc_kernel_llada8b_traffic.txt. It is reported
+# DRAM traffic of one projection call on this workload (its two kernels,
+# the weight stream and the merge: dram__bytes_read.sum +
+# dram__bytes_write.sum with the caches left alone), from the ncu capture
+# summarised in profiles/gemm_stream_kernel_llada8b_layer.txt. It is reported
 # only while the sources it was taken from hash to the recorded value; after
 # any change to them the figure is stale and the line carries null.
-QKV_TRAFFIC = {"sources_sha256": None,
-               "bytes": None}
+QKV_TRAFFIC = {"sources_sha256": "cd7394a544fe5532b0b3abeb5585180b5d29b034d722885116752d2dbcff51b0",
+               "bytes": 102338304 + 3235584 + 256 + 562176}
 QKV_SOURCES = ("kv_cache_attention_gb300/csrc/fdl_qkv_tc.cu", "kv_cache_attention_gb300/csrc/fdl_gemm_tc.cu", "kv_cache_attention_gb300/csrc/fdl_gemm_stream.cu", "kv_cache_attention_gb300/csrc/fdl_qkv.cu",
                "kv_cache_attention_gb300/csrc/tc_ptx.cuh", "kv_cache_attention_gb300/csrc/fdl_internal.cuh")
 
