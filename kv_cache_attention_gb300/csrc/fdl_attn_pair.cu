@@ -617,15 +617,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
           const int c0 = j * kBN;
           float x[64];
-          const float mx1 = load_half(c0, 1, x, true);
-          const float mx0 = load_half(c0, 0, x, true);
-          float alpha;
-          update_max(fmaxf(mx0, mx1), alpha);
+          // each half's max moves the reference on its own (each score read
+          // once); a move at half 1 rescales half 0's sum
+          float a0, a1;
+          update_max(load_half(c0, 0, x, true), a0);
           float sum = exp_sum(x, m_run);
-          load_half(c0, 1, x, false);
-          sum += exp_sum(x, m_run);
+          const float mx1 = load_half(c0, 1, x, true);
           tc::fence_before_sync();  // the scores are read: the buffer may be refilled
-          l_run = l_run * alpha + sum;
+          if (update_max(mx1, a1)) sum *= a1;
+          sum += exp_sum(x, m_run);
+          l_run = l_run * (a0 * a1) + sum;
         }
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&s_free_a[g]);
@@ -645,21 +646,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool ok = wait_s(sA + jj);
       if (ok) {
         float x[64];
-        float alpha = 1.f;
-        bool resc = false;
-        float m = lse2;
+        // Online: each half's max moves the running reference on its own (a
+        // move beyond 2^kRescale is rare), so each score is read once; a
+        // move at half 1 rescales half 0's P (already in TMEM) and sum.
+        // Two-pass: P = exp(S - lse).
+        float a0 = 1.f, a1 = 1.f;
+        bool r0 = false, r1 = false;
+        if (!two_pass) r0 = update_max(load_half(c0, 0, x, true), a0);
+        else load_half(c0, 0, x, false);
+        // half 0's P goes into columns 0..31, whose scores (half 0) are
+        // already read; half 1's scores (columns 64..127) are read next and
+        // its P goes into columns 32..63
+        float sum = exp_sum(x, two_pass ? lse2 : m_run);
+        store_p(0, x);
+        if (two_pass) colsum(0, x, track_row);
         if (!two_pass) {
-          // the tile max first (half 1, then half 0, which stays in x)
-          const float mx1 = load_half(c0, 1, x, true);
-          const float mx0 = load_half(c0, 0, x, true);
-          resc = update_max(fmaxf(mx0, mx1), alpha);
-          m = m_run;
+          r1 = update_max(load_half(c0, 1, x, true), a1);
+          if (__any_sync(0xffffffffu, r1)) {
+            tc::tmem_wait_st();  // half 0's P has landed
+            float pw[32];
+            tc::tmem_ld_32x32b_x32(s_buf, pw);
+            uint32_t pk[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              uint32_t w = __float_as_uint(pw[e]);
+              const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+              __nv_bfloat162 h2 = __floats2bfloat162_rn(f.x * a1, f.y * a1);
+              pk[e] = *reinterpret_cast<uint32_t*>(&h2);
+            }
+            tc::tmem_st_32x32b_x32_u(s_buf, pk);
+            sum *= a1;
+          }
         } else {
-          load_half(c0, 0, x, false);
+          load_half(c0, 1, x, false);
         }
-        if (__any_sync(0xffffffffu, resc)) {
+        sum += exp_sum(x, two_pass ? lse2 : m_run);
+        store_p(1, x);
+        if (two_pass) colsum(1, x, track_row);
+        if (__any_sync(0xffffffffu, r0 || r1)) {
           // O_g rows move to the new max (the group's previous P V product
-          // finished before this tile's scores were computed)
+          // finished before this tile's scores were computed, and this
+          // tile's is issued only after P is complete)
+          const float alpha = a0 * a1;
 #pragma unroll 1
           for (int cc = 0; cc < kHD; cc += 32) {
             float o[32];
@@ -669,18 +697,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::tmem_st_32x32b_x32(tm_og + cc + lane_off, o);
           }
         }
-        // half 0's P goes into columns 0..31, whose scores (half 0) are
-        // already read; half 1's scores (columns 64..127) are read next and
-        // its P goes into columns 32..63
-        float sum = exp_sum(x, m);
-        store_p(0, x);
-        if (two_pass) colsum(0, x, track_row);
-        load_half(c0, 1, x, false);
-        sum += exp_sum(x, m);
-        store_p(1, x);
-        if (two_pass) colsum(1, x, track_row);
         tc::tmem_wait_st();
-        l_run = l_run * alpha + sum;
+        l_run = l_run * (a0 * a1) + sum;
         // keys past the sequence end may hold anything: zero their V rows so
         // that 0 * V stays 0 (group 0's product of the tile runs first)
         if (g == 0 && c0 + kBN > nkeys &&
