@@ -182,7 +182,13 @@ fdl_status fdl_qkv_rope_cache_write(fdl_ctx* ctx, const void* X, const void* Wqk
  * Tracker (track_scores != NULL): for every base key i of sequence b,
  *   track_scores[b*track_ld + i] += sum_h sum_{WINDOW rows j} p_{h,j,i} / (H*M_b)
  * with M_b the number of WINDOW rows of b; the caller zeroes the buffer
- * once per step and every layer's call accumulates into it.
+ * once per step and every layer's call accumulates into it. On the
+ * tensor-core path (bf16, head_dim 128, B <= 1024) the sums are in a fixed
+ * order, so a call reproduces its scores bit for bit, for every sequence
+ * whose WINDOW rows lie within two 128-row query tiles; other sequences, and
+ * the CUDA-core path, add with atomics (exact up to fp32 reassociation).
+ * Several calls on one context must not overlap on the GPU (each call's
+ * partial sums use the context's workspace).
  * o_out: [R, n_heads, head_dim] (context dtype); lse_out: [R, n_heads] fp32
  * (nullable); worklist_out (nullable, fdl_worklist_capacity ints): count,
  * then (b, q_start, q_len, n_keys) per item, n_keys = kv_len[b] + 2m.
