@@ -29,8 +29,8 @@
 // or a stream-K kernel that merges in the last share, puts those merges at
 // the end of the launch, after every SM's stream has finished; measured,
 // they cost as much as a third of the launch. Here the shares go to an
-// L2-resident workspace and the merge is a separate launch in which every
-// output element has its own thread.
+// L2-resident workspace and the merge is a separate launch with a thread
+// for every 8 or 16 output elements.
 //
 // Schedule (stream-K): the work is T tiles x nkb k-blocks of 64 ("units"),
 // in tile-major order; CTA c of G takes the contiguous units [c*U/G,
