@@ -50,7 +50,7 @@ WORKLOAD = "llada8b_layer_bf16_b1_p512_g256_w32_t32"
 # summarised in profiles/gemm_stream_kernel_llada8b_layer.txt. It is reported
 # only while the sources it was taken from hash to the recorded value; after
 # any change to them the figure is stale and the line carries null.
-QKV_TRAFFIC = {"sources_sha256": "cd7394a544fe5532b0b3abeb5585180b5d29b034d722885116752d2dbcff51b0",
+QKV_TRAFFIC = {"sources_sha256": "cf3bad7dad7c9043b34f7298f0bbe083a682322157db4c31d44a1b42fd64df9d",
                "bytes": 102338304 + 3235584 + 256 + 562176}
 QKV_SOURCES = ("kv_cache_attention_gb300/csrc/fdl_qkv_tc.cu", "kv_cache_attention_gb300/csrc/fdl_gemm_tc.cu", "kv_cache_attention_gb300/csrc/fdl_gemm_stream.cu", "kv_cache_attention_gb300/csrc/fdl_qkv.cu",
                "kv_cache_attention_gb300/csrc/tc_ptx.cuh", "kv_cache_attention_gb300/csrc/fdl_internal.cuh")
