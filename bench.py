@@ -458,16 +458,21 @@ def run_gpu(args, world, rank, local):
                           conf=conf, argmax=arg, commit=com, search_rows=srows, n_search=nsr)
         side_stream.wait_event(layer_done)
         ctx_side.track_topk(track, elig, seq_len, k, idx, cnt)
+        # the top-k has consumed this step's scores: reset them for the next
+        # step's first layer here, on the side stream, beside the unmasking
+        with torch.cuda.stream(side_stream):
+            track.zero_()
         side_done.record(side_stream)
         stream.wait_event(side_done)
 
     def step(c, X=None, L=None):
-        # the tracker accumulates over a step's layers: zeroed once per step,
-        # before its first layer
-        track.zero_()
+        # the tracker accumulates over a step's layers and is zero before a
+        # step's first layer: zeroed once before the first step, then by each
+        # step after its top-k has read it
         qkv_part(c, X)
         rest_part(c, L)
 
+    track.zero_()
     for i in range(args.warmup):
         step(i % n_copies)
     ctx.sync_status()
